@@ -1,0 +1,237 @@
+"""Seeded synthetic inputs for vocab-parallel cross-entropy.
+
+This module is the ONLY thing the CUDA path and the oracle share: it draws the
+logits and the row metadata (targets, ignored rows, boosted rows, spike
+columns).  It holds none of the loss arithmetic.
+
+Generator (published definitions, restated):
+
+* SplitMix64 (Steele, Lea & Flood, "Fast splittable pseudorandom number
+  generators", OOPSLA 2014): output ``n`` (0-based) of the generator seeded with
+  ``key`` is ``mix(key + (n + 1) * GAMMA) mod 2**64``, with ``mix`` the
+  xor-shift-multiply finaliser of that paper.  It is counter based, so any
+  element can be drawn on its own, on the host or on the device, with integer
+  arithmetic only (bit exact on both).
+* Box-Muller (Box & Muller, 1958), cosine branch, in float64:
+  ``n = sqrt(-2 ln u1) * cos(2 pi u2)`` with ``u1 = (a + 1) / 2**53`` in (0, 1]
+  and ``u2 = b / 2**53`` in [0, 1), ``a``/``b`` the top 53 bits of outputs
+  ``2g`` and ``2g + 1`` of the value stream for the element's global index
+  ``g = r * V + c``.  The stored logit is ``float32(sigma * n + boost)``
+  (float64 multiply, then add, then one round-to-nearest-even to binary32) and,
+  for bf16 logits, that binary32 rounded to nearest-even bfloat16.
+
+The device twin of the element generator lives in ``csrc/synth_gen.cu``
+(library ``libvpce_synth.so``); the float64 ``log``/``cos`` of the two sides may
+differ in the last bit, so a stored value can (rarely) differ by one ulp.  Row
+metadata is drawn only here, on the host, and uploaded.
+
+Workloads: the five configurations the method is exercised on, with the
+shapes, value distributions and row structure of the LM-head cross-entropy:
+the pages' Llama-3-70B head (V = 128256, t = 8, 16032 columns per card) plus
+smaller and larger vocabularies.
+"""
+from __future__ import annotations
+
+import dataclasses
+import numpy as np
+
+GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+_TWO_PI = 6.283185307179586  # float64 nearest to 2*pi
+_INV_2_53 = 1.0 / 9007199254740992.0
+
+# stream numbers (outputs of the generator seeded with the workload seed)
+STREAM_VALUES = 0
+STREAM_TARGETS = 1
+STREAM_IGNORE = 2
+STREAM_BOOST = 3
+STREAM_SPIKE = 4
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def splitmix64_at(key, n) -> np.ndarray:
+    """Output number ``n`` (array, 0-based) of SplitMix64 seeded with ``key``."""
+    with np.errstate(over="ignore"):
+        n = np.asarray(n, dtype=np.uint64)
+        return _mix(np.uint64(key) + (n + np.uint64(1)) * GAMMA)
+
+
+def stream_key(seed: int, stream: int) -> np.uint64:
+    return np.uint64(splitmix64_at(np.uint64(seed), np.uint64(stream)))
+
+
+def uniform_int(h: np.ndarray, n: int) -> np.ndarray:
+    """Map 64-bit hashes to [0, n) by the top 32 bits (multiply-shift)."""
+    return ((h >> np.uint64(32)) * np.uint64(n)) >> np.uint64(32)
+
+
+def _normals_from_index(key: np.uint64, g: np.ndarray) -> np.ndarray:
+    g = np.asarray(g, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        h1 = splitmix64_at(key, g * np.uint64(2))
+        h2 = splitmix64_at(key, g * np.uint64(2) + np.uint64(1))
+    u1 = ((h1 >> np.uint64(11)) + np.uint64(1)).astype(np.float64) * _INV_2_53
+    u2 = (h2 >> np.uint64(11)).astype(np.float64) * _INV_2_53
+    return np.sqrt(-2.0 * np.log(u1)) * np.cos(_TWO_PI * u2)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round binary32 values to nearest-even bfloat16; returns uint16 patterns."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    with np.errstate(over="ignore"):
+        r = (b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+# --------------------------------------------------------------------------
+# workload recipes
+# --------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int            # 1..5; seed = 20261202 + index
+    s: int                # rows (tokens)
+    V: int                # vocabulary
+    t: int                # shards
+    dtype: str            # 'fp32' | 'bf16'
+    sigma: float          # logits ~ N(0, sigma^2)
+    targets: str          # 'uniform' | 'zipf1.1'
+    ignore_frac: float = 0.0
+    boost_frac: float = 0.0   # rows whose target column gets +boost
+    boost: float = 0.0
+    spike: float = 0.0        # +spike at one uniform column of every row
+    ignore_index: int = -100
+
+    @property
+    def seed(self) -> int:
+        return 20261202 + self.index
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("tiny_s64_v1000", 1, 64, 1000, 2, "fp32", 1.0, "uniform"),
+        Workload("s4096_v50304", 2, 4096, 50304, 4, "bf16", 2.0, "uniform", ignore_frac=0.02),
+        Workload("s8192_v128256", 3, 8192, 128256, 8, "bf16", 3.0, "uniform",
+                 boost_frac=0.30, boost=5.0),
+        Workload("s16384_v152064", 4, 16384, 152064, 8, "fp32", 1.0, "uniform",
+                 ignore_frac=0.05, spike=20.0),
+        Workload("s32768_v256000", 5, 32768, 256000, 16, "bf16", 2.0, "zipf1.1"),
+    ]
+}
+BENCH_WORKLOAD = "s8192_v128256"
+
+
+def even_vocab_start(V: int, t: int) -> list[int]:
+    """Shard boundaries for t shards; widths differ by at most one column
+    when t does not divide V (the first V % t shards are one wider)."""
+    base, extra = divmod(V, t)
+    out = [0]
+    for i in range(t):
+        out.append(out[-1] + base + (1 if i < extra else 0))
+    return out
+
+
+@dataclasses.dataclass
+class RowMeta:
+    targets: np.ndarray      # int64[s]; ignore_index on ignored rows
+    boost_col: np.ndarray    # int64[s]; global column that gets +boost_val, -1 if none
+    boost_val: float
+
+
+def _pick_rows(seed: int, stream: int, s: int, count: int) -> np.ndarray:
+    """Exactly ``count`` distinct rows: the first ``count`` of a seeded shuffle
+    (rows ordered by a 64-bit key each)."""
+    keys = splitmix64_at(stream_key(seed, stream), np.arange(s, dtype=np.uint64))
+    order = np.argsort(keys, kind="stable")
+    return np.sort(order[:count])
+
+
+def row_meta(w: Workload, s: int | None = None) -> RowMeta:
+    """Targets and per-row boost columns of workload ``w`` (first ``s`` rows
+    of a batch of ``s`` rows; ``s`` defaults to ``w.s``)."""
+    s = w.s if s is None else s
+    rows = np.arange(s, dtype=np.uint64)
+    if w.targets == "uniform":
+        h = splitmix64_at(stream_key(w.seed, STREAM_TARGETS), rows)
+        y = uniform_int(h, w.V).astype(np.int64)
+    elif w.targets == "zipf1.1":
+        # truncated Zipf over ranks k = 1..V with P(k) ~ k^-1.1; token id = k-1;
+        # inverse-CDF sampling with a 53-bit uniform
+        k = np.arange(1, w.V + 1, dtype=np.float64)
+        cdf = np.cumsum(k ** -1.1)
+        cdf /= cdf[-1]
+        h = splitmix64_at(stream_key(w.seed, STREAM_TARGETS), rows)
+        u = (h >> np.uint64(11)).astype(np.float64) * _INV_2_53
+        y = np.minimum(np.searchsorted(cdf, u, side="right"), w.V - 1).astype(np.int64)
+    else:
+        raise ValueError(w.targets)
+    boost_col = np.full(s, -1, dtype=np.int64)
+    boost_val = 0.0
+    if w.boost_frac > 0:
+        picked = _pick_rows(w.seed, STREAM_BOOST, s, int(round(w.boost_frac * s)))
+        boost_col[picked] = y[picked]
+        boost_val = w.boost
+    if w.spike > 0:
+        h = splitmix64_at(stream_key(w.seed, STREAM_SPIKE), rows)
+        boost_col[:] = uniform_int(h, w.V).astype(np.int64)
+        boost_val = w.spike
+    if w.ignore_frac > 0:
+        picked = _pick_rows(w.seed, STREAM_IGNORE, s, int(round(w.ignore_frac * s)))
+        y = y.copy()
+        y[picked] = w.ignore_index
+    return RowMeta(targets=y, boost_col=boost_col, boost_val=boost_val)
+
+
+def logits_rows(w: Workload, rows, col_lo: int, col_hi: int, meta: RowMeta) -> np.ndarray:
+    """Stored logits of ``rows`` x global columns [col_lo, col_hi).
+
+    Returns float32 for fp32 workloads and uint16 bfloat16 patterns for bf16.
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.arange(col_lo, col_hi, dtype=np.int64)
+    key = stream_key(w.seed, STREAM_VALUES)
+    g = (rows[:, None].astype(np.uint64) * np.uint64(w.V) + cols[None, :].astype(np.uint64))
+    v = _normals_from_index(key, g) * w.sigma
+    bc = meta.boost_col[rows]
+    hit = bc[:, None] == cols[None, :]
+    if hit.any():
+        v = np.where(hit, v + meta.boost_val, v)
+    f = v.astype(np.float32)
+    return f32_to_bf16_bits(f) if w.dtype == "bf16" else f
+
+
+def shards_host(w: Workload, meta: RowMeta, vocab_start=None, ld=None, rows=None):
+    """Host shard arrays ``[len(rows), ld_i]`` (padding columns hold a NaN
+    canary).  ``ld`` is None (each shard as wide as its columns) or one row
+    stride (elements) for all shards."""
+    vs = even_vocab_start(w.V, w.t) if vocab_start is None else list(vocab_start)
+    rows = np.arange(w.s) if rows is None else np.asarray(rows)
+    out = []
+    for i in range(len(vs) - 1):
+        width = vs[i + 1] - vs[i]
+        lda = width if ld is None else int(ld)
+        vals = logits_rows(w, rows, vs[i], vs[i + 1], meta)
+        if lda == width:
+            out.append(np.ascontiguousarray(vals))
+            continue
+        if w.dtype == "bf16":
+            buf = np.full((len(rows), lda), 0x7FC1, dtype=np.uint16)
+        else:
+            buf = np.full((len(rows), lda), np.nan, dtype=np.float32)
+        buf[:, :width] = vals
+        out.append(buf)
+    return out
