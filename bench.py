@@ -1,0 +1,435 @@
+"""Benchmark of the vocab-parallel cross-entropy forward + backward on GB300.
+
+One step = vpce_forward (partial statistics + combine) and vpce_backward (dlogits
+in place) over one batch of seeded synthetic logits: s = 8192 rows,
+V = 128256 (t = 8 shards of 16032 columns, bf16), N(0, 3^2) with +5 on the
+target column of 30% of rows -- the Llama-3-70B LM-head shape.
+
+Prints one JSON line (rank 0).  `value` is tokens/s over all ranks; the line
+also carries the 3-pass HBM GB/s, the roofline of the dominant kernel, the
+end-to-end number with host buffers, the clocks seen during the timed region,
+and (rank 0, N = 1) the fp64 CPU oracle timed on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from vocab_sharded_lm_gb300 import synth  # noqa: E402
+
+METRIC = "VPCE fwd+bwd tokens/s & HBM GB/s (% of peak), s=8192 V=128256 bf16, 1 GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def _workload_desc(w):
+    return (f"{w.name}: s={w.s} V={w.V} t={w.t} x {w.V // w.t} {w.dtype} logits ~N(0,{w.sigma:g}^2)"
+            + (f", +{w.boost:g} on the target of {int(w.boost_frac * 100)}% of rows" if w.boost_frac else "")
+            + (f", {int(w.ignore_frac * 100)}% ignore_index" if w.ignore_frac else "")
+            + (f", +{w.spike:g} spike per row" if w.spike else "")
+            + f", targets {w.targets}")
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.dev)], stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [l.strip().split(", ") for l in self.out.read().splitlines() if l.strip()]
+        self.out.close()
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+                for n, v in zip(names, r[5:9]):
+                    if v.strip() == "Active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# traffic recorded by ncu for the dominant kernel (per launch), if still current
+# ----------------------------------------------------------------------------
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("vpce_device.cuh", "vpce_kernels.cuh", "vpce_forward.cu", "vpce_backward.cu"):
+        with open(os.path.join(ROOT, "vocab_sharded_lm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(kernel: str, workload: str):
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    ent = d.get(kernel, {}).get(workload)
+    if not ent or ent.get("source_hash") != _kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from vocab_sharded_lm_gb300 import _build, vpce
+
+    rank, world, local = _env_rank()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    vpce.load_library()
+
+    w = synth.WORKLOADS[args.workload]
+    # every rank runs its own batch (independent problems, weak scaling)
+    if world > 1:
+        w = w.replace(index=w.index + 100 * rank) if rank else w
+    meta = synth.row_meta(w)
+    vs = synth.even_vocab_start(w.V, w.t)
+    e = w.elem_bytes
+    buf_bytes = w.s * w.V * e
+    free, _ = torch.cuda.mem_get_info(dev)
+    nbuf = max(2, min(args.warmup + args.steps, int(0.5 * free // buf_bytes), args.max_buffers))
+
+    pristine = synth.device_shards(w, meta, vs, device=dev)
+    bufs = [[p.clone() for p in pristine] for _ in range(nbuf)]
+    y = torch.from_numpy(meta.targets).to(dev)
+    ws = [vpce.new_workspace(w.t, w.s, dev) for _ in range(2)]
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(k, ev=None):
+        b = bufs[k % nbuf]
+        wk = ws[k % 2]
+        if ev is not None:
+            ev[0].record(stream)
+        vpce.vpce_forward(b, y, vs, ignore_index=w.ignore_index, loss_out=loss, workspace=wk)
+        if ev is not None:
+            ev[1].record(stream)
+        vpce.vpce_backward(b, y, wk, vs, ignore_index=w.ignore_index)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize(dev)
+    # restore every buffer so that the timed steps start from generated logits
+    for b in bufs:
+        for d, p in zip(b, pristine):
+            d.copy_(p)
+    torch.cuda.synchronize(dev)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(k, evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    fwd_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
+    bwd_ms = [ev[1].elapsed_time(ev[2]) for ev in evs]
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    # ---------------- end to end: pinned host logits in, dlogits + loss out
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    host_in = [p.cpu().pin_memory() for p in pristine]
+    host_out = [torch.empty_like(h).pin_memory() for h in host_in]
+    host_y = torch.from_numpy(meta.targets).pin_memory()
+    host_loss = torch.empty((), dtype=torch.float32).pin_memory()
+    dbuf = bufs[1 % nbuf]
+    ydev = torch.empty_like(y)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(e2e_steps):
+        for d, h in zip(dbuf, host_in):
+            d.copy_(h, non_blocking=True)
+        ydev.copy_(host_y, non_blocking=True)
+        vpce.vpce_forward(dbuf, ydev, vs, ignore_index=w.ignore_index, loss_out=loss, workspace=ws[0])
+        vpce.vpce_backward(dbuf, ydev, ws[0], vs, ignore_index=w.ignore_index)
+        for d, h in zip(dbuf, host_out):
+            h.copy_(d, non_blocking=True)
+        host_loss.copy_(loss, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = buf_bytes + w.s * 8
+    d2h = buf_bytes + 4
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = _peaks()
+    ms_step = total_ms / args.steps
+    tokens_s = world * w.s * args.steps / (total_ms * 1e-3)
+    n_valid = int(np.sum(meta.targets != w.ignore_index))
+    three_pass = 3 * w.s * w.V * e
+    gbs_3pass = three_pass / (ms_step * 1e-3) / 1e9
+    # dominant kernel: the in-place backward; algorithmic bytes per launch =
+    # read + write of every valid row's logits, ignored rows written only,
+    # plus the per-row target (8 B) and logsumexp (4 B)
+    bwd_bytes = (2 * n_valid + (w.s - n_valid)) * w.V * e + w.s * 12
+    bwd_mean_ms = statistics.mean(bwd_ms)
+    achieved = bwd_bytes / (bwd_mean_ms * 1e-3) / 1e9
+    fwd_bytes = n_valid * w.V * e + w.s * (8 + 8 * w.t + 4)
+    fwd_mean_ms = statistics.mean(fwd_ms)
+    traffic = _ncu_traffic("backward_kernel", w.name)
+    out = {
+        "metric": METRIC,
+        "value": round(tokens_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator; no dataset)",
+        "config": {
+            "workload": _workload_desc(w),
+            "global_batch": w.s * world,
+            "seq_len": w.s,
+            "logits_dtype": w.dtype,
+            "parallelism": f"vocab shards t={w.t} on one GPU; {world} independent replica(s)",
+            "l2": f"inputs larger than L2: each step's logits are {buf_bytes / 1e9:.2f} GB, "
+                  f"{nbuf} distinct buffers cycled (beyond {nbuf} steps a buffer holds the previous "
+                  f"pass's dlogits: same shape and work)",
+            "path": "vpce_forward + vpce_backward (split, 3 logit passes)",
+        },
+        "hbm_gbs_3pass": round(gbs_3pass, 1),
+        "hbm_frac_nominal_8000": round(gbs_3pass / NOMINAL_HBM_GBS, 4),
+        "hbm_frac_measured_peak": round(gbs_3pass / peak, 4),
+        "fwd_ms": round(fwd_mean_ms, 5),
+        "bwd_ms": round(bwd_mean_ms, 5),
+        "fwd_gbs": round(fwd_bytes / (fwd_mean_ms * 1e-3) / 1e9, 1),
+        "roofline": {
+            "kernel": "backward_kernel",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": bwd_bytes,
+        },
+        "e2e": {
+            "value": round(w.s * world / (e2e_ms * 1e-3), 1),
+            "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "steps": e2e_steps,
+            "ms_per_step": round(e2e_ms, 4),
+        },
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, meta, vs, budget_s=args.cpu_seconds)
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# the fp64 oracle on the host cores: CPU baseline and the reference arm
+# ----------------------------------------------------------------------------
+def _oracle_sample(w, meta, vs, rows):
+    from oracle import vpce_oracle as O
+
+    host = [synth.logits_rows(w, rows, vs[i], vs[i + 1], meta) for i in range(w.t)]
+    return O, host
+
+
+def _oracle_step(O, host, vs, w, y_rows, n_valid):
+    z = O.assemble(host, vs, w.dtype)
+    ref = O.cross_entropy(z, y_rows, w.ignore_index, n_valid=n_valid)
+    O.dlogits(z, y_rows, w.ignore_index, n_valid=n_valid, lse=ref["lse"])
+
+
+def cpu_baseline(w, meta, vs, budget_s=15.0, rows_per_batch=64):
+    n_valid = int(np.sum(meta.targets != w.ignore_index))
+    rng = np.random.default_rng(1)
+    done = 0
+    elapsed = 0.0
+    batches = 0
+    while elapsed < budget_s and done < w.s:
+        rows = np.sort(rng.choice(w.s, size=rows_per_batch, replace=False))
+        O, host = _oracle_sample(w, meta, vs, rows)
+        t0 = time.perf_counter()
+        _oracle_step(O, host, vs, w, meta.targets[rows], n_valid)
+        elapsed += time.perf_counter() - t0
+        done += rows_per_batch
+        batches += 1
+    return {"value": round(done / elapsed, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} rows of the workload ({batches} batches of {rows_per_batch}, full V={w.V}), "
+                      f"fp64 numpy on one host core, forward loss + dlogits, {elapsed:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = _env_rank()
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    meta = synth.row_meta(w)
+    vs = synth.even_vocab_start(w.V, w.t)
+    n_valid = int(np.sum(meta.targets != w.ignore_index))
+    rows_per_step = args.ref_rows
+    rng = np.random.default_rng(2)
+    samples = []
+    for k in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(w.s, size=rows_per_step, replace=False))
+        from oracle import vpce_oracle as O
+
+        host = [synth.logits_rows(w, rows, vs[i], vs[i + 1], meta) for i in range(w.t)]
+        samples.append((rows, host))
+    for k in range(args.warmup):
+        rows, host = samples[k]
+        _oracle_step(O, host, vs, w, meta.targets[rows], n_valid)
+    t0 = time.perf_counter()
+    for k in range(args.warmup, args.warmup + args.steps):
+        rows, host = samples[k]
+        _oracle_step(O, host, vs, w, meta.targets[rows], n_valid)
+    dt = time.perf_counter() - t0
+    value = rows_per_step * args.steps / dt
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded counter-based generator; no dataset)",
+        "config": {"workload": _workload_desc(w), "global_batch": w.s, "seq_len": w.s,
+                   "logits_dtype": w.dtype,
+                   "parallelism": "fp64 CPU oracle (no reference implementation exists; the pages print no code)",
+                   "sample": f"{rows_per_step} rows per step, full V={w.V}"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows_per_step} rows of the workload per step, fp64 numpy, one core"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=synth.BENCH_WORKLOAD, choices=list(synth.WORKLOADS))
+    ap.add_argument("--max-buffers", type=int, default=48)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,144 @@
+/*
+ * vpce.h -- vocab-parallel cross-entropy on one GB300 (sm_103a).
+ *
+ * The operation ("Distributed Training III: Model Parallelism", CMU 11-868
+ * Lecture 16 notes, §5.5 "Embedding and output layer"; "LLM Internals" §7.3
+ * "Model and tensor parallelism", §7.3.4): the LM-head logits z[s, V] are split
+ * along the vocabulary into t shards.  Each shard reduces, per row, its
+ * maximum, its sum of exponentials and -- if the row's target column falls in
+ * the shard's [vocab_start, vocab_end) -- the target logit.  The partials
+ * combine into logsumexp(z_r) and the loss CE_r = logsumexp(z_r) - z_r[y_r]
+ * without ever gathering the full rows.  Here all t shards live on one GPU and
+ * the combine runs on the device, in a fixed order.
+ *
+ * The backward (not given by the pages; the standard derivative of the reduced
+ * loss) overwrites the shards in place with
+ *     dlogits_rk = g * (softmax(z_r)_k - [k == y_r]) / n_valid    (mean)
+ *     dlogits_rk = g * (softmax(z_r)_k - [k == y_r])              (sum)
+ * and with zeros on rows whose target is ignore_index.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - All calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL
+ *   is the legacy default stream), except vpce_read_error_flag, which
+ *   synchronises the stream.  The current CUDA device must be the one that
+ *   owns every device pointer, and it must be a compute-capability 10.3 GPU.
+ * - The caller owns every buffer.  The library allocates nothing and keeps no
+ *   per-call state; the only thing carried from forward to backward is the
+ *   caller's workspace.
+ * - Host-detectable argument errors return a non-OK status and launch
+ *   nothing.  A launch failure returns VPCE_ERR_CUDA.
+ * - Logits layout: shard i is a row-major [s, w_i] array of `dtype` elements
+ *   at device address shards[i], w_i = vocab_start[i+1] - vocab_start[i], with
+ *   a row stride of `ld` elements (ld = 0: each shard is dense, stride w_i).
+ *   A shard may be a column block of one big [s, V] tensor (shards[i] =
+ *   base + vocab_start[i], ld = V).  Shard pointers need only element
+ *   alignment; rows that are not 16-byte aligned take a scalar path for their
+ *   ragged head and tail elements.
+ * - Targets: int64[s] on the device, replicated view of the whole batch.  A
+ *   target equal to ignore_index drops its row; any other target outside
+ *   [0, V) is not trapped: the row's loss, lse and gradient become NaN and the
+ *   workspace error flag gets bit 0 (read it with vpce_read_error_flag).
+ */
+#ifndef VPCE_H
+#define VPCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the runtime's opaque stream handle). */
+typedef struct CUstream_st* vpce_stream_t;
+
+typedef enum {
+  VPCE_OK = 0,
+  VPCE_ERR_INVALID_ARG = 1,       /* null pointer, bad t/s/ld/vocab_start/reduction */
+  VPCE_ERR_ALIGNMENT = 2,         /* a pointer not aligned to its element / 256 B workspace */
+  VPCE_ERR_DTYPE = 3,             /* dtype is not VPCE_FP32 or VPCE_BF16 */
+  VPCE_ERR_WORKSPACE = 4,         /* workspace_bytes < vpce_workspace_bytes(t, s) */
+  VPCE_ERR_CUDA = 5,              /* a CUDA runtime call or a launch failed */
+  VPCE_ERR_UNSUPPORTED_DEVICE = 6 /* current device is not compute capability 10.3 */
+} vpce_status;
+
+typedef enum { VPCE_FP32 = 0, VPCE_BF16 = 1 } vpce_dtype;
+
+/* Reduction of the per-row losses, as torch.nn.functional.cross_entropy. */
+typedef enum { VPCE_MEAN = 0, VPCE_SUM = 1 } vpce_reduction;
+
+#define VPCE_MAX_SHARDS 64
+
+/* Error-flag bits written to the workspace by the device. */
+#define VPCE_FLAG_BAD_TARGET 1    /* some target is neither ignore_index nor in [0, V) */
+#define VPCE_FLAG_WAIT_TIMEOUT 2  /* a pipeline wait gave up (never expected) */
+
+/*
+ * Bytes of device workspace vpce_forward / vpce_backward need for t shards
+ * and s rows (t in [1, VPCE_MAX_SHARDS], s >= 0).  Returns 0 for arguments out
+ * of range.  The workspace holds the per-(shard, row) partials (8 B each), the
+ * per-row target logit and logsumexp (4 B each), the batch count n_valid, the
+ * error flag and the combine's per-block sums.  Caller allocated, 256-byte
+ * aligned, no initialisation needed.
+ */
+size_t vpce_workspace_bytes(int t, int64_t s);
+
+/*
+ * Forward: loss of the vocab-sharded logits.
+ *   shards       host array of t device pointers (read only here).
+ *   dtype        element type of every shard.
+ *   t            number of shards, 1..VPCE_MAX_SHARDS.
+ *   s            rows (tokens), >= 0.  s = 0 gives loss NaN (mean) or 0 (sum).
+ *   vocab_start  host array of t+1 offsets: vocab_start[0] = 0, strictly
+ *                increasing, V = vocab_start[t] < 2^31.  Shard i holds global
+ *                columns [vocab_start[i], vocab_start[i+1]); widths may differ
+ *                (a V not divisible by t needs no padding).
+ *   ld           row stride in elements shared by all shards, >= every
+ *                width; 0 means each shard is dense.
+ *   targets      device int64[s].
+ *   ignore_index target value that drops a row (torch default -100).
+ *   reduction    VPCE_MEAN: sum of valid-row losses / n_valid (NaN when
+ *                n_valid = 0); VPCE_SUM: the plain sum.
+ *   loss_out     device float, receives the reduced loss.
+ *   row_loss_out device float[s] or NULL; receives CE_r for valid rows, 0 for
+ *                ignored rows, NaN for out-of-range targets.
+ *   workspace    device buffer of workspace_bytes >= vpce_workspace_bytes.
+ * Results are bitwise reproducible for fixed inputs and t: the shards fold
+ * in ascending index order and the batch sum runs in a fixed order (fp64).
+ */
+vpce_status vpce_forward(const void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                         const int64_t* vocab_start, int64_t ld,
+                         const int64_t* targets, int64_t ignore_index,
+                         vpce_reduction reduction, float* loss_out, float* row_loss_out,
+                         void* workspace, size_t workspace_bytes, vpce_stream_t stream);
+
+/*
+ * Backward: overwrite the shards in place with dlogits (same dtype; bf16 is
+ * rounded to nearest-even from the fp32 value).  Every argument describing the
+ * logits and targets must equal the preceding vpce_forward's, the shards must
+ * still hold that call's logits, and `workspace` must be that call's,
+ * unmodified (it carries logsumexp, n_valid and the reduction).
+ * grad_output is the upstream gradient g of the reduced loss (1.0 normally).
+ * Padding columns (ld > w_i) are neither read nor written.
+ */
+vpce_status vpce_backward(void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                          const int64_t* vocab_start, int64_t ld,
+                          const int64_t* targets, int64_t ignore_index,
+                          float grad_output, const void* workspace, size_t workspace_bytes,
+                          vpce_stream_t stream);
+
+/*
+ * Synchronise `stream`, then copy the workspace error flag to *flag (bit 0:
+ * bad target seen by the last forward; bit 1: a device wait timed out).
+ */
+vpce_status vpce_read_error_flag(const void* workspace, int* flag, vpce_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* vpce_status_string(vpce_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VPCE_H */

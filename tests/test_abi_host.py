@@ -1,0 +1,117 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from vocab_sharded_lm_gb300 import _build, vpce
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vpce.h")
+
+FAKE = 0x7F0000000000  # a 256-byte aligned "device" address, never dereferenced on the host
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return vpce.load_library()
+
+
+def _declared_functions(path):
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vpce_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions(HEADER)
+    assert "vpce_forward" in names and "vpce_backward" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = vpce.vpce_status_string(code)
+        assert s.startswith(vpce.STATUS_NAMES[code])
+
+
+def test_workspace_bytes(lib):
+    assert vpce.vpce_workspace_bytes(0, 10) == 0
+    assert vpce.vpce_workspace_bytes(65, 10) == 0
+    assert vpce.vpce_workspace_bytes(1, -1) == 0
+    a = vpce.vpce_workspace_bytes(8, 8192)
+    assert a >= 8 * 8192 * 8 + 8192 * 8 and a % 256 == 0
+    assert vpce.vpce_workspace_bytes(8, 0) > 0
+
+
+def _fwd(**kw):
+    t = kw.get("t", 2)
+    args = dict(shard_ptrs=[FAKE, FAKE + 4096][:t] + [FAKE] * max(0, t - 2), dtype=vpce.VPCE_BF16, t=t, s=4,
+                vocab_start=[0, 8, 16] if t == 2 else list(range(0, 8 * (t + 1), 8)), ld=0,
+                targets_ptr=ctypes.c_void_p(FAKE), ignore_index=-100, reduction=vpce.VPCE_MEAN,
+                loss_ptr=ctypes.c_void_p(FAKE), row_loss_ptr=None, ws_ptr=ctypes.c_void_p(FAKE),
+                ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    args.pop("t", None)
+    return vpce.forward_raw(t=t, **args)
+
+
+def _bwd(**kw):
+    args = dict(shard_ptrs=[FAKE, FAKE + 4096], dtype=vpce.VPCE_FP32, t=2, s=4, vocab_start=[0, 8, 16], ld=0,
+                targets_ptr=ctypes.c_void_p(FAKE), ignore_index=-100, grad=1.0, ws_ptr=ctypes.c_void_p(FAKE),
+                ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return vpce.backward_raw(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=7), 3),
+    (dict(t=0, shard_ptrs=[], vocab_start=[0]), 1),
+    (dict(t=65, shard_ptrs=[FAKE] * 65, vocab_start=list(range(0, 66 * 8, 8))), 1),
+    (dict(s=-1), 1),
+    (dict(shard_ptrs=None), 1),
+    (dict(shard_ptrs=[FAKE, 0]), 1),
+    (dict(shard_ptrs=[FAKE + 1, FAKE]), 2),       # bf16 needs 2-byte alignment
+    (dict(vocab_start=None), 1),
+    (dict(vocab_start=[1, 8, 16]), 1),            # must start at 0
+    (dict(vocab_start=[0, 8, 8]), 1),             # empty shard
+    (dict(vocab_start=[0, 9, 8]), 1),             # decreasing
+    (dict(ld=-1), 1),
+    (dict(ld=7), 1),                              # narrower than a shard
+    (dict(targets_ptr=None), 1),
+    (dict(targets_ptr=ctypes.c_void_p(FAKE + 4)), 2),
+    (dict(reduction=5), 1),
+    (dict(loss_ptr=None), 1),
+    (dict(loss_ptr=ctypes.c_void_p(FAKE + 2)), 2),
+    (dict(ws_ptr=None), 1),
+    (dict(ws_ptr=ctypes.c_void_p(FAKE + 16)), 2),
+    (dict(ws_bytes=64), 4),
+])
+def test_forward_rejects_bad_arguments(lib, kw, code):
+    assert _fwd(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=2), 3),
+    (dict(grad=float("nan")), 1),
+    (dict(grad=float("inf")), 1),
+    (dict(ws_bytes=100), 4),
+    (dict(shard_ptrs=[FAKE + 2, FAKE]), 2),       # fp32 needs 4-byte alignment
+    (dict(vocab_start=[0, 0, 16]), 1),
+])
+def test_backward_rejects_bad_arguments(lib, kw, code):
+    assert _bwd(**kw) == code
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this checks the host-only path")
+    # all arguments valid: the first CUDA call (device query) fails, nothing runs
+    assert _fwd() == 5
+    assert _bwd() == 5

@@ -1,0 +1,246 @@
+// C ABI of the vocab-parallel cross-entropy library (declared in include/vpce.h):
+// argument validation, launch configuration, and nothing else.  No buffers
+// are allocated; every call is stream ordered.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "vpce_kernels.cuh"
+
+namespace vpce {
+cudaError_t set_stats_smem();
+cudaError_t set_backward_smem();
+}  // namespace vpce
+
+using namespace vpce;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int sms = 0;
+  bool ready = false;
+  vpce_status status = VPCE_OK;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Per-device one-time set-up: check the architecture, read the SM count and
+// raise the dynamic shared-memory limit of the streaming kernels.
+vpce_status device_setup(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return VPCE_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return VPCE_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms_ = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms_, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return VPCE_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) {
+      d.status = VPCE_ERR_UNSUPPORTED_DEVICE;
+    } else if (set_stats_smem() != cudaSuccess || set_backward_smem() != cudaSuccess) {
+      cudaGetLastError();
+      return VPCE_ERR_CUDA;
+    } else {
+      d.sms = sms_;
+      d.status = VPCE_OK;
+    }
+    d.ready = true;
+  }
+  *sms = d.sms;
+  return d.status;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shared validation of the logits description; fills the geometry.
+vpce_status check_logits(const void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                         const int64_t* vocab_start, int64_t ld, const int64_t* targets, ShardSet* sh,
+                         long long* V) {
+  if (dtype != VPCE_FP32 && dtype != VPCE_BF16) return VPCE_ERR_DTYPE;
+  if (t < 1 || t > VPCE_MAX_SHARDS || s < 0 || s > (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  if (shards == nullptr || vocab_start == nullptr) return VPCE_ERR_INVALID_ARG;
+  if (s > 0 && targets == nullptr) return VPCE_ERR_INVALID_ARG;
+  if (targets != nullptr && !aligned(targets, 8)) return VPCE_ERR_ALIGNMENT;
+  const int eb = dtype == VPCE_BF16 ? 2 : 4;
+  if (vocab_start[0] != 0) return VPCE_ERR_INVALID_ARG;
+  int64_t wmax = 0;
+  for (int i = 0; i < t; ++i) {
+    const int64_t w = vocab_start[i + 1] - vocab_start[i];
+    if (w < 1) return VPCE_ERR_INVALID_ARG;
+    if (w * eb >= (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+    if (w > wmax) wmax = w;
+  }
+  if (vocab_start[t] >= (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  if (ld < 0 || (ld > 0 && ld < wmax)) return VPCE_ERR_INVALID_ARG;
+  std::memset(sh, 0, sizeof(*sh));
+  for (int i = 0; i < t; ++i) {
+    if (s > 0 && shards[i] == nullptr) return VPCE_ERR_INVALID_ARG;
+    if (!aligned(shards[i], eb)) return VPCE_ERR_ALIGNMENT;
+    const int64_t w = vocab_start[i + 1] - vocab_start[i];
+    sh->ptr[i] = static_cast<const unsigned char*>(shards[i]);
+    sh->ld_bytes[i] = (ld > 0 ? ld : w) * eb;
+    sh->start[i] = vocab_start[i];
+  }
+  sh->start[t] = vocab_start[t];
+  *V = vocab_start[t];
+  return VPCE_OK;
+}
+
+vpce_status check_workspace(const void* ws, size_t bytes, int t, int64_t s) {
+  if (ws == nullptr) return VPCE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return VPCE_ERR_ALIGNMENT;
+  if (bytes < WsLayout(t, s).total) return VPCE_ERR_WORKSPACE;
+  return VPCE_OK;
+}
+
+int stream_grid(int sms, long long units) {
+  const long long want = (units + kWarps - 1) / kWarps;
+  return int(want < sms ? (want > 0 ? want : 1) : sms);
+}
+
+vpce_status launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? VPCE_OK : VPCE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t vpce_workspace_bytes(int t, int64_t s) {
+  if (t < 1 || t > VPCE_MAX_SHARDS || s < 0 || s > (int64_t(1) << 31)) return 0;
+  return WsLayout(t, s).total;
+}
+
+vpce_status vpce_forward(const void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                         const int64_t* vocab_start, int64_t ld, const int64_t* targets, int64_t ignore_index,
+                         vpce_reduction reduction, float* loss_out, float* row_loss_out, void* workspace,
+                         size_t workspace_bytes, vpce_stream_t stream) {
+  ShardSet sh;
+  long long V = 0;
+  vpce_status st = check_logits(shards, dtype, t, s, vocab_start, ld, targets, &sh, &V);
+  if (st != VPCE_OK) return st;
+  if (reduction != VPCE_MEAN && reduction != VPCE_SUM) return VPCE_ERR_INVALID_ARG;
+  if (loss_out == nullptr) return VPCE_ERR_INVALID_ARG;
+  if (!aligned(loss_out, 4) || (row_loss_out != nullptr && !aligned(row_loss_out, 4))) return VPCE_ERR_ALIGNMENT;
+  st = check_workspace(workspace, workspace_bytes, t, s);
+  if (st != VPCE_OK) return st;
+  int sms = 0;
+  st = device_setup(&sms);
+  if (st != VPCE_OK) return st;
+
+  const WsLayout L(t, s);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  Header* hdr = reinterpret_cast<Header*>(ws);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+
+  if (s > 0) {
+    StatsParams p;
+    p.sh = sh;
+    p.s = s;
+    p.units = (long long)t * s;
+    p.targets = reinterpret_cast<const long long*>(targets);
+    p.ignore_index = ignore_index;
+    p.part = reinterpret_cast<float2*>(ws + L.part);
+    p.tgt = reinterpret_cast<float*>(ws + L.tgt);
+    p.hdr = hdr;
+    const int grid = stream_grid(sms, p.units);
+    if (dtype == VPCE_BF16) launch_stats<__nv_bfloat16>(p, grid, cs);
+    else launch_stats<float>(p, grid, cs);
+    if ((st = launch_status()) != VPCE_OK) return st;
+  }
+  CombineParams c;
+  c.s = s;
+  c.t = t;
+  c.V = V;
+  c.targets = reinterpret_cast<const long long*>(targets);
+  c.ignore_index = ignore_index;
+  c.reduction = int(reduction);
+  c.part = reinterpret_cast<const float2*>(ws + L.part);
+  c.tgt = reinterpret_cast<const float*>(ws + L.tgt);
+  c.lse = reinterpret_cast<float*>(ws + L.lse);
+  c.bsum = reinterpret_cast<double*>(ws + L.bsum);
+  c.bcnt = reinterpret_cast<int*>(ws + L.bcnt);
+  c.loss_out = loss_out;
+  c.row_loss = row_loss_out;
+  c.hdr = hdr;
+  const long long blocks = s > 0 ? (s + kCombineThreads - 1) / kCombineThreads : 1;
+  launch_combine(c, int(blocks), cs);
+  return launch_status();
+}
+
+vpce_status vpce_backward(void* const* shards, vpce_dtype dtype, int t, int64_t s, const int64_t* vocab_start,
+                          int64_t ld, const int64_t* targets, int64_t ignore_index, float grad_output,
+                          const void* workspace, size_t workspace_bytes, vpce_stream_t stream) {
+  ShardSet sh;
+  long long V = 0;
+  vpce_status st = check_logits(reinterpret_cast<const void* const*>(shards), dtype, t, s, vocab_start, ld,
+                                targets, &sh, &V);
+  if (st != VPCE_OK) return st;
+  if (!std::isfinite(grad_output)) return VPCE_ERR_INVALID_ARG;
+  st = check_workspace(workspace, workspace_bytes, t, s);
+  if (st != VPCE_OK) return st;
+  int sms = 0;
+  st = device_setup(&sms);
+  if (st != VPCE_OK) return st;
+  if (s == 0) return VPCE_OK;
+
+  const WsLayout L(t, s);
+  const unsigned char* ws = static_cast<const unsigned char*>(workspace);
+  BackwardParams p;
+  p.sh = sh;
+  p.s = s;
+  p.units = (long long)t * s;
+  p.targets = reinterpret_cast<const long long*>(targets);
+  p.ignore_index = ignore_index;
+  p.lse = reinterpret_cast<const float*>(ws + L.lse);
+  p.hdr = reinterpret_cast<const Header*>(ws);
+  p.hdr_flags = reinterpret_cast<Header*>(const_cast<unsigned char*>(ws));
+  p.grad = grad_output;
+  const int grid = stream_grid(sms, p.units);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == VPCE_BF16) launch_backward<__nv_bfloat16>(p, grid, cs);
+  else launch_backward<float>(p, grid, cs);
+  return launch_status();
+}
+
+vpce_status vpce_read_error_flag(const void* workspace, int* flag, vpce_stream_t stream) {
+  if (workspace == nullptr || flag == nullptr) return VPCE_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return VPCE_ERR_ALIGNMENT;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const Header* hdr = static_cast<const Header*>(workspace);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, &hdr->error_flag, sizeof(int), cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+      cudaStreamSynchronize(cs) != cudaSuccess) {
+    cudaGetLastError();
+    return VPCE_ERR_CUDA;
+  }
+  *flag = v;
+  return VPCE_OK;
+}
+
+const char* vpce_status_string(vpce_status status) {
+  switch (status) {
+    case VPCE_OK: return "VPCE_OK";
+    case VPCE_ERR_INVALID_ARG: return "VPCE_ERR_INVALID_ARG: invalid argument";
+    case VPCE_ERR_ALIGNMENT: return "VPCE_ERR_ALIGNMENT: misaligned pointer";
+    case VPCE_ERR_DTYPE: return "VPCE_ERR_DTYPE: unsupported dtype";
+    case VPCE_ERR_WORKSPACE: return "VPCE_ERR_WORKSPACE: workspace too small";
+    case VPCE_ERR_CUDA: return "VPCE_ERR_CUDA: CUDA runtime or launch error";
+    case VPCE_ERR_UNSUPPORTED_DEVICE: return "VPCE_ERR_UNSUPPORTED_DEVICE: needs a compute capability 10.3 GPU";
+  }
+  return "VPCE_ERR_UNKNOWN";
+}
+
+}  // extern "C"

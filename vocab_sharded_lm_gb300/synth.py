@@ -235,3 +235,63 @@ def shards_host(w: Workload, meta: RowMeta, vocab_start=None, ld=None, rows=None
         buf[:, :width] = vals
         out.append(buf)
     return out
+
+
+# --------------------------------------------------------------------------
+# device twin (libvpce_synth.so): fills device shards with the same values
+# --------------------------------------------------------------------------
+_SYNTH_LIB = None
+
+
+def _synth_lib():
+    global _SYNTH_LIB
+    if _SYNTH_LIB is None:
+        import ctypes
+        import os
+
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libvpce_synth.so")
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is not built: run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        lib.vpce_synth_fill.restype = ctypes.c_int
+        lib.vpce_synth_fill.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_longlong,
+                                        ctypes.c_longlong, ctypes.c_longlong, ctypes.c_longlong,
+                                        ctypes.c_longlong, ctypes.c_ulonglong, ctypes.c_double,
+                                        ctypes.c_void_p, ctypes.c_double, ctypes.c_void_p]
+        _SYNTH_LIB = lib
+    return _SYNTH_LIB
+
+
+def device_shards(w: Workload, meta: RowMeta, vocab_start=None, ld=None, device="cuda", row0: int = 0,
+                  s: int | None = None):
+    """Allocate and fill the t device shards of workload ``w`` (rows
+    ``row0 .. row0+s-1`` of the batch described by ``meta``).  Returns a list
+    of torch tensors ``[s, w_i]`` (views with row stride ``ld`` if given;
+    padding columns hold a NaN canary)."""
+    import ctypes
+    import torch
+
+    s = w.s if s is None else s
+    vs = even_vocab_start(w.V, w.t) if vocab_start is None else list(vocab_start)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    boost = torch.from_numpy(np.ascontiguousarray(meta.boost_col)).to(device)
+    key = int(stream_key(w.seed, STREAM_VALUES))
+    stream = torch.cuda.current_stream(device).cuda_stream
+    out = []
+    for i in range(len(vs) - 1):
+        width = vs[i + 1] - vs[i]
+        lda = width if ld is None else int(ld)
+        if lda == width:
+            buf = torch.empty((s, lda), dtype=tdt, device=device)
+        else:
+            buf = torch.full((s, lda), float("nan"), dtype=tdt, device=device)
+        err = _synth_lib().vpce_synth_fill(ctypes.c_void_p(buf.data_ptr()), 1 if w.dtype == "bf16" else 0,
+                                           s, row0, vs[i], width, lda, w.V, key, float(w.sigma),
+                                           ctypes.c_void_p(boost.data_ptr()), float(meta.boost_val),
+                                           ctypes.c_void_p(stream))
+        if err != 0:
+            raise RuntimeError(f"vpce_synth_fill failed with CUDA error {err}")
+        out.append(buf[:, :width])
+    torch.cuda.current_stream(device).synchronize()
+    del boost
+    return out

@@ -1,0 +1,216 @@
+"""ctypes binding of ``libvpce.so`` (C ABI in include/vpce.h).
+
+Argument marshalling only: every step of the loss runs in the library's CUDA
+kernels.  torch supplies device memory and the current stream.  The names are
+the C entry points'.  The library is loaded on first use; if it is missing the
+call raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_lib", "libvpce.so")
+
+VPCE_OK = 0
+STATUS_NAMES = {
+    0: "VPCE_OK",
+    1: "VPCE_ERR_INVALID_ARG",
+    2: "VPCE_ERR_ALIGNMENT",
+    3: "VPCE_ERR_DTYPE",
+    4: "VPCE_ERR_WORKSPACE",
+    5: "VPCE_ERR_CUDA",
+    6: "VPCE_ERR_UNSUPPORTED_DEVICE",
+}
+VPCE_FP32, VPCE_BF16 = 0, 1
+VPCE_MEAN, VPCE_SUM = 0, 1
+VPCE_MAX_SHARDS = 64
+VPCE_FLAG_BAD_TARGET = 1
+VPCE_FLAG_WAIT_TIMEOUT = 2
+
+_lib = None
+_lock = threading.Lock()
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I64P = ctypes.POINTER(ctypes.c_int64)
+
+
+class VPCEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {vpce_status_string(code)} ({code})")
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libvpce.so (once) and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is not built: run __graft_entry__.build() (nvcc, sm_103a)")
+        lib = ctypes.CDLL(p)
+        lib.vpce_workspace_bytes.restype = ctypes.c_size_t
+        lib.vpce_workspace_bytes.argtypes = [ctypes.c_int, _I64]
+        lib.vpce_forward.restype = ctypes.c_int
+        lib.vpce_forward.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
+                                     ctypes.c_int, _P, _P, _P, ctypes.c_size_t, _P]
+        lib.vpce_backward.restype = ctypes.c_int
+        lib.vpce_backward.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
+                                      ctypes.c_float, _P, ctypes.c_size_t, _P]
+        lib.vpce_read_error_flag.restype = ctypes.c_int
+        lib.vpce_read_error_flag.argtypes = [_P, ctypes.POINTER(ctypes.c_int), _P]
+        lib.vpce_status_string.restype = ctypes.c_char_p
+        lib.vpce_status_string.argtypes = [ctypes.c_int]
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def vpce_status_string(code: int) -> str:
+    try:
+        return load_library().vpce_status_string(int(code)).decode()
+    except RuntimeError:
+        return STATUS_NAMES.get(int(code), "VPCE_ERR_UNKNOWN")
+
+
+def vpce_workspace_bytes(t: int, s: int) -> int:
+    return int(load_library().vpce_workspace_bytes(int(t), int(s)))
+
+
+# ----------------------------------------------------------------------------
+# raw-pointer forms (the C signatures one to one)
+# ----------------------------------------------------------------------------
+def _ptr_array(ptrs):
+    arr = (ctypes.c_void_p * len(ptrs))(*[int(p) for p in ptrs])
+    return arr
+
+
+def _i64_array(vals):
+    return (ctypes.c_int64 * len(vals))(*[int(v) for v in vals])
+
+
+def forward_raw(shard_ptrs, dtype, t, s, vocab_start, ld, targets_ptr, ignore_index, reduction,
+                loss_ptr, row_loss_ptr, ws_ptr, ws_bytes, stream) -> int:
+    lib = load_library()
+    ptrs = _ptr_array(shard_ptrs) if shard_ptrs is not None else None
+    vs = _i64_array(vocab_start) if vocab_start is not None else None
+    return int(lib.vpce_forward(ctypes.cast(ptrs, _P) if ptrs is not None else None, int(dtype), int(t),
+                                int(s), vs, int(ld), targets_ptr, int(ignore_index), int(reduction),
+                                loss_ptr, row_loss_ptr, ws_ptr, int(ws_bytes), stream))
+
+
+def backward_raw(shard_ptrs, dtype, t, s, vocab_start, ld, targets_ptr, ignore_index, grad,
+                 ws_ptr, ws_bytes, stream) -> int:
+    lib = load_library()
+    ptrs = _ptr_array(shard_ptrs) if shard_ptrs is not None else None
+    vs = _i64_array(vocab_start) if vocab_start is not None else None
+    return int(lib.vpce_backward(ctypes.cast(ptrs, _P) if ptrs is not None else None, int(dtype), int(t),
+                                 int(s), vs, int(ld), targets_ptr, int(ignore_index), float(grad),
+                                 ws_ptr, int(ws_bytes), stream))
+
+
+# ----------------------------------------------------------------------------
+# torch-tensor forms
+# ----------------------------------------------------------------------------
+def _describe(shards, vocab_start):
+    import torch
+
+    if not shards:
+        raise ValueError("need at least one shard")
+    dt = shards[0].dtype
+    if dt == torch.bfloat16:
+        dtype = VPCE_BF16
+    elif dt == torch.float32:
+        dtype = VPCE_FP32
+    else:
+        raise TypeError(f"unsupported logits dtype {dt}")
+    s = shards[0].shape[0]
+    widths = []
+    for sh in shards:
+        if sh.dtype != dt or sh.dim() != 2 or sh.shape[0] != s or not sh.is_cuda:
+            raise ValueError("shards must be 2-D CUDA tensors of one dtype and row count")
+        if sh.stride(1) != 1:
+            raise ValueError("shard columns must be contiguous")
+        widths.append(sh.shape[1])
+    if vocab_start is None:
+        vocab_start = [0]
+        for w in widths:
+            vocab_start.append(vocab_start[-1] + w)
+    vocab_start = [int(v) for v in vocab_start]
+    strides = {sh.stride(0) for sh in shards}
+    if s <= 1 or all(sh.stride(0) == sh.shape[1] for sh in shards):
+        ld = 0
+    elif len(strides) == 1:
+        ld = strides.pop()
+    else:
+        raise ValueError("shards must share one row stride or each be dense")
+    return dtype, s, vocab_start, ld
+
+
+def _stream_ptr(stream):
+    import torch
+
+    st = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(st.cuda_stream)
+
+
+def new_workspace(t: int, s: int, device=None):
+    import torch
+
+    n = vpce_workspace_bytes(t, s)
+    if n == 0:
+        raise ValueError("t or s out of range")
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def vpce_forward(shards, targets, vocab_start=None, *, ignore_index: int = -100, reduction: str = "mean",
+                 loss_out=None, row_loss_out=None, workspace=None, stream=None):
+    """Loss of vocab-sharded logits.  Returns ``(loss, workspace)``; pass the
+    workspace unchanged to :func:`vpce_backward`."""
+    import torch
+
+    dtype, s, vs, ld = _describe(shards, vocab_start)
+    t = len(shards)
+    dev = shards[0].device
+    if targets.dtype != torch.int64 or not targets.is_cuda or targets.numel() != s:
+        raise ValueError("targets must be a CUDA int64 tensor with one entry per row")
+    if workspace is None:
+        workspace = new_workspace(t, s, dev)
+    if loss_out is None:
+        loss_out = torch.empty((), dtype=torch.float32, device=dev)
+    red = {"mean": VPCE_MEAN, "sum": VPCE_SUM}[reduction]
+    code = forward_raw([sh.data_ptr() for sh in shards], dtype, t, s, vs, ld,
+                       ctypes.c_void_p(targets.data_ptr()), ignore_index, red,
+                       ctypes.c_void_p(loss_out.data_ptr()),
+                       ctypes.c_void_p(row_loss_out.data_ptr()) if row_loss_out is not None else None,
+                       ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+    if code != VPCE_OK:
+        raise VPCEError(code, "vpce_forward")
+    return loss_out, workspace
+
+
+def vpce_backward(shards, targets, workspace, vocab_start=None, *, ignore_index: int = -100,
+                  grad_output: float = 1.0, stream=None):
+    """Overwrite ``shards`` in place with dlogits of the preceding forward."""
+    dtype, s, vs, ld = _describe(shards, vocab_start)
+    code = backward_raw([sh.data_ptr() for sh in shards], dtype, len(shards), s, vs, ld,
+                        ctypes.c_void_p(targets.data_ptr()), ignore_index, grad_output,
+                        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+    if code != VPCE_OK:
+        raise VPCEError(code, "vpce_backward")
+    return shards
+
+
+def vpce_read_error_flag(workspace, stream=None) -> int:
+    flag = ctypes.c_int(0)
+    code = load_library().vpce_read_error_flag(ctypes.c_void_p(workspace.data_ptr()), ctypes.byref(flag),
+                                               _stream_ptr(stream))
+    if code != VPCE_OK:
+        raise VPCEError(code, "vpce_read_error_flag")
+    return flag.value
