@@ -83,7 +83,7 @@ def test_column_views_of_one_tensor():
     check_loss(float(loss), ref["loss"])
     vpce.vpce_backward(views, y, ws, vs)
     got = O.widen(from_device(big, w.dtype), w.dtype)
-    check_dlogits(got, O.dlogits(z, meta.targets), w.dtype, ref["n_valid"], 1.0)
+    check_dlogits(got, O.dlogits(z, meta.targets), w.dtype, 1.0 / ref["n_valid"])
 
 
 @pytest.mark.parametrize("reduction,grad", [("sum", 0.5), ("mean", 2.5), ("mean", 0.0)])
@@ -158,7 +158,7 @@ def test_uniform_logits_closed_form_on_gpu():
     got = O.assemble([from_device(d, "bf16") for d in dev], vs, "bf16")
     expect = np.full((s, V), 1.0 / V)
     expect[np.arange(s), np.arange(s) * 1000] -= 1.0
-    check_dlogits(got, expect / s, "bf16", s, 1.0)
+    check_dlogits(got, expect / s, "bf16", 1.0 / s)
 
 
 def test_deterministic_and_t_invariant():
