@@ -156,6 +156,8 @@ def run_ours(args):
     vpce.load_library()
 
     w = synth.WORKLOADS[args.workload]
+    if args.rows:
+        w = w.replace(s=args.rows)  # smaller batch of the same shard geometry (profiling captures)
     # every rank runs its own batch (independent problems, weak scaling)
     if world > 1:
         w = w.replace(index=w.index + 100 * rank) if rank else w
@@ -422,6 +424,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="override the workload's row count (small profiling captures only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
