@@ -129,6 +129,38 @@ vpce_status vpce_backward(void* const* shards, vpce_dtype dtype, int t, int64_t 
                           vpce_stream_t stream);
 
 /*
+ * Forward without a workspace argument, for callers that cannot allocate
+ * device memory where they need the loss: a plugin inside a framework whose
+ * pooling allocator already owns the GPU's memory (a raw cudaMalloc would fail
+ * or fragment that pool), a path that cannot afford cudaMalloc's implicit
+ * device synchronisation, or a deployment that forbids device allocation
+ * after start-up.  The pages have no counterpart: this is a packaging
+ * variant of vpce_forward, with identical arguments and results except that
+ * the scratch is a file-scope device array of VPCE_STATIC_SCRATCH_BYTES held
+ * by every GPU that loads this library until the process exits.  The caller
+ * still passes the logits, targets and outputs.
+ *   - Calls the library makes: no cudaMalloc, cudaFree or other allocating
+ *     routine; the first call on each device looks the array's address up
+ *     (cudaGetSymbolAddress, with that device current), so make that first
+ *     call before any stream capture.
+ *   - Limit: returns VPCE_ERR_WORKSPACE, launching nothing, when
+ *     vpce_workspace_bytes(t, s) > VPCE_STATIC_SCRATCH_BYTES (8 MiB covers,
+ *     e.g., t = 16 at s = 32768, t = 8 at s = 65536 and t = 64 at s = 8192;
+ *     roughly 8 * t * s + 8 * s bytes are needed).
+ *   - Every call on a device shares the one array and the next call overwrites
+ *     it (the kernels clear what must start at zero), so calls that may
+ *     overlap on the GPU -- on different streams, or from different threads --
+ *     race: serialise them on one stream.  The workspace stays inside the
+ *     library, so no vpce_backward can follow this forward.
+ */
+#define VPCE_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+vpce_status vpce_forward_static(const void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                                const int64_t* vocab_start, int64_t ld,
+                                const int64_t* targets, int64_t ignore_index,
+                                vpce_reduction reduction, float* loss_out, float* row_loss_out,
+                                vpce_stream_t stream);
+
+/*
  * Synchronise `stream`, then copy the workspace error flag to *flag (bit 0:
  * bad target seen by the last forward; bit 1: a device wait timed out).
  */

@@ -29,6 +29,7 @@ VPCE_MEAN, VPCE_SUM = 0, 1
 VPCE_MAX_SHARDS = 64
 VPCE_FLAG_BAD_TARGET = 1
 VPCE_FLAG_WAIT_TIMEOUT = 2
+VPCE_STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 _lib = None
 _lock = threading.Lock()
@@ -62,6 +63,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.vpce_backward.restype = ctypes.c_int
         lib.vpce_backward.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
                                       ctypes.c_float, _P, ctypes.c_size_t, _P]
+        lib.vpce_forward_static.restype = ctypes.c_int
+        lib.vpce_forward_static.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
+                                            ctypes.c_int, _P, _P, _P]
         lib.vpce_read_error_flag.restype = ctypes.c_int
         lib.vpce_read_error_flag.argtypes = [_P, ctypes.POINTER(ctypes.c_int), _P]
         lib.vpce_status_string.restype = ctypes.c_char_p
@@ -214,3 +218,35 @@ def vpce_read_error_flag(workspace, stream=None) -> int:
     if code != VPCE_OK:
         raise VPCEError(code, "vpce_read_error_flag")
     return flag.value
+
+
+# ----------------------------------------------------------------------------
+# forward with the library's own static scratch (no workspace argument)
+# ----------------------------------------------------------------------------
+def forward_static_raw(shard_ptrs, dtype, t, s, vocab_start, ld, targets_ptr, ignore_index, reduction,
+                       loss_ptr, row_loss_ptr, stream) -> int:
+    """vpce_forward_static one to one.  For callers that cannot allocate
+    device memory: the scratch is a fixed array inside the library (see
+    include/vpce.h); calls that overlap on the GPU share it and race."""
+    lib = load_library()
+    ptrs = _ptr_array(shard_ptrs) if shard_ptrs is not None else None
+    vs = _i64_array(vocab_start) if vocab_start is not None else None
+    return int(lib.vpce_forward_static(ctypes.cast(ptrs, _P) if ptrs is not None else None, int(dtype), int(t),
+                                       int(s), vs, int(ld), targets_ptr, int(ignore_index), int(reduction),
+                                       loss_ptr, row_loss_ptr, stream))
+
+
+def vpce_forward_static(shards, targets, loss_out, vocab_start=None, *, ignore_index: int = -100,
+                        reduction: str = "mean", row_loss_out=None, stream=None):
+    """Loss of vocab-sharded logits into the caller's ``loss_out`` (and
+    ``row_loss_out``), using no workspace from the caller."""
+    dtype, s, vs, ld = _describe(shards, vocab_start)
+    red = {"mean": VPCE_MEAN, "sum": VPCE_SUM}[reduction]
+    code = forward_static_raw([sh.data_ptr() for sh in shards], dtype, len(shards), s, vs, ld,
+                              ctypes.c_void_p(targets.data_ptr()), ignore_index, red,
+                              ctypes.c_void_p(loss_out.data_ptr()),
+                              ctypes.c_void_p(row_loss_out.data_ptr()) if row_loss_out is not None else None,
+                              _stream_ptr(stream))
+    if code != VPCE_OK:
+        raise VPCEError(code, "vpce_forward_static")
+    return loss_out
