@@ -119,7 +119,8 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 def _kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("vpce_device.cuh", "vpce_kernels.cuh", "vpce_forward.cu", "vpce_backward.cu"):
+    for f in ("vpce_device.cuh", "vpce_kernels.cuh", "vpce_chunk.cuh", "vpce_forward.cu", "vpce_backward.cu",
+              "vpce_fused.cu", "vpce_resident.cu"):
         with open(os.path.join(ROOT, "vocab_sharded_lm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -175,15 +176,29 @@ def run_ours(args):
     loss = torch.empty((), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    fused = args.path == "fused"
+
+    def run_step(b, yy, wk):
+        if fused:
+            vpce.vpce_forward_backward(b, yy, vs, ignore_index=w.ignore_index, loss_out=loss, workspace=wk)
+        else:
+            vpce.vpce_forward(b, yy, vs, ignore_index=w.ignore_index, loss_out=loss, workspace=wk)
+            vpce.vpce_backward(b, yy, wk, vs, ignore_index=w.ignore_index)
+
     def step(k, ev=None):
         b = bufs[k % nbuf]
         wk = ws[k % 2]
         if ev is not None:
             ev[0].record(stream)
-        vpce.vpce_forward(b, y, vs, ignore_index=w.ignore_index, loss_out=loss, workspace=wk)
-        if ev is not None:
-            ev[1].record(stream)
-        vpce.vpce_backward(b, y, wk, vs, ignore_index=w.ignore_index)
+        if fused:
+            vpce.vpce_forward_backward(b, y, vs, ignore_index=w.ignore_index, loss_out=loss, workspace=wk)
+            if ev is not None:
+                ev[1].record(stream)
+        else:
+            vpce.vpce_forward(b, y, vs, ignore_index=w.ignore_index, loss_out=loss, workspace=wk)
+            if ev is not None:
+                ev[1].record(stream)
+            vpce.vpce_backward(b, y, wk, vs, ignore_index=w.ignore_index)
         if ev is not None:
             ev[2].record(stream)
 
@@ -236,8 +251,7 @@ def run_ours(args):
         for d, h in zip(dbuf, host_in):
             d.copy_(h, non_blocking=True)
         ydev.copy_(host_y, non_blocking=True)
-        vpce.vpce_forward(dbuf, ydev, vs, ignore_index=w.ignore_index, loss_out=loss, workspace=ws[0])
-        vpce.vpce_backward(dbuf, ydev, ws[0], vs, ignore_index=w.ignore_index)
+        run_step(dbuf, ydev, ws[0])
         for d, h in zip(dbuf, host_out):
             h.copy_(d, non_blocking=True)
         host_loss.copy_(loss, non_blocking=True)
@@ -258,15 +272,21 @@ def run_ours(args):
     n_valid = int(np.sum(meta.targets != w.ignore_index))
     three_pass = 3 * w.s * w.V * e
     gbs_3pass = three_pass / (ms_step * 1e-3) / 1e9
-    # dominant kernel: the in-place backward; algorithmic bytes per launch =
-    # read + write of every valid row's logits, ignored rows written only,
-    # plus the per-row target (8 B) and logsumexp (4 B)
-    bwd_bytes = (2 * n_valid + (w.s - n_valid)) * w.V * e + w.s * 12
-    bwd_mean_ms = statistics.mean(bwd_ms)
-    achieved = bwd_bytes / (bwd_mean_ms * 1e-3) / 1e9
+    # algorithmic HBM bytes of the in-place gradient writer: read + write of
+    # every valid row's logits, ignored rows written only, plus the per-row
+    # target (8 B) and logsumexp (4 B)
+    grad_bytes = (2 * n_valid + (w.s - n_valid)) * w.V * e + w.s * 12
     fwd_bytes = n_valid * w.V * e + w.s * (8 + 8 * w.t + 4)
     fwd_mean_ms = statistics.mean(fwd_ms)
-    traffic = _ncu_traffic("backward_kernel", w.name)
+    bwd_mean_ms = statistics.mean(bwd_ms) if not fused else None
+    if fused:
+        # dominant (only) kernel pair: prologue + fused forward/backward, whose
+        # HBM floor is one read and one write of the logits
+        dom_kernel, dom_ms, dom_bytes = "fused_kernel", fwd_mean_ms, grad_bytes
+    else:
+        dom_kernel, dom_ms, dom_bytes = "backward_kernel", bwd_mean_ms, grad_bytes
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = _ncu_traffic(dom_kernel, w.name)
     out = {
         "metric": METRIC,
         "value": round(tokens_s, 1),
@@ -289,16 +309,20 @@ def run_ours(args):
             "l2": f"inputs larger than L2: each step's logits are {buf_bytes / 1e9:.2f} GB, "
                   f"{nbuf} distinct buffers cycled (beyond {nbuf} steps a buffer holds the previous "
                   f"pass's dlogits: same shape and work)",
-            "path": "vpce_forward + vpce_backward (split, 3 logit passes)",
+            "path": ("vpce_forward_backward (fused: each row's backward follows its forward from L2; "
+                     "1 HBM read + 1 HBM write of the logits)") if fused else
+                    "vpce_forward + vpce_backward (split, 3 logit passes)",
         },
         "hbm_gbs_3pass": round(gbs_3pass, 1),
         "hbm_frac_nominal_8000": round(gbs_3pass / NOMINAL_HBM_GBS, 4),
         "hbm_frac_measured_peak": round(gbs_3pass / peak, 4),
-        "fwd_ms": round(fwd_mean_ms, 5),
-        "bwd_ms": round(bwd_mean_ms, 5),
-        "fwd_gbs": round(fwd_bytes / (fwd_mean_ms * 1e-3) / 1e9, 1),
+        "fwd_ms": None if fused else round(fwd_mean_ms, 5),
+        "bwd_ms": None if fused else round(bwd_mean_ms, 5),
+        "fused_ms": round(fwd_mean_ms, 5) if fused else None,
+        "fwd_gbs": None if fused else round(fwd_bytes / (fwd_mean_ms * 1e-3) / 1e9, 1),
+        "hbm_gbs_floor_fused": round(2 * w.s * w.V * e / (ms_step * 1e-3) / 1e9, 1) if fused else None,
         "roofline": {
-            "kernel": "backward_kernel",
+            "kernel": dom_kernel,
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -306,7 +330,7 @@ def run_ours(args):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
-            "algorithmic_bytes_per_launch": bwd_bytes,
+            "algorithmic_bytes_per_launch": dom_bytes,
         },
         "e2e": {
             "value": round(w.s * world / (e2e_ms * 1e-3), 1),
@@ -316,9 +340,12 @@ def run_ours(args):
             "steps": e2e_steps,
             "ms_per_step": round(e2e_ms, 4),
         },
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (2 if fused else 3) * args.steps,
         "clocks": clk,
     }
+    if fused:
+        out["config"]["fused_plan"] = vpce.vpce_fused_plan(
+            vpce.VPCE_BF16 if w.dtype == "bf16" else vpce.VPCE_FP32, vs, w.s)
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, meta, vs, budget_s=args.cpu_seconds)
     print(json.dumps(out), flush=True)
@@ -424,6 +451,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["fused", "split"], default="split",
+                    help="fused: vpce_forward_backward; split: vpce_forward then vpce_backward")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the workload's row count (small profiling captures only)")
     args = ap.parse_args()

@@ -129,6 +129,37 @@ vpce_status vpce_backward(void* const* shards, vpce_dtype dtype, int t, int64_t 
                           vpce_stream_t stream);
 
 /*
+ * Forward and backward in one call: the loss (as vpce_forward) and the shards
+ * overwritten in place with dlogits for upstream gradient grad_output (as
+ * vpce_backward), for the common case where the loss is the last op and g is
+ * known before the forward runs (1.0, or a loss scale).  Each row's backward
+ * follows its forward while the row is still in L2, so the logits cross HBM
+ * once in each direction (two passes of traffic instead of three).  Arguments
+ * as vpce_forward plus grad_output; the workspace afterwards holds logsumexp
+ * and n_valid like a forward's.  Rows that are not 16-byte aligned (shard
+ * pointer, row stride or width in bytes) run the two-call path instead, with
+ * the same results.  The batch loss is summed in a fixed order (fp64), so
+ * results are bitwise reproducible; they agree with the two-call path within
+ * rounding.
+ */
+vpce_status vpce_forward_backward(void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                                  const int64_t* vocab_start, int64_t ld,
+                                  const int64_t* targets, int64_t ignore_index,
+                                  vpce_reduction reduction, float grad_output,
+                                  float* loss_out, float* row_loss_out,
+                                  void* workspace, size_t workspace_bytes, vpce_stream_t stream);
+
+/*
+ * How vpce_forward_backward would run the given problem on the current
+ * device, assuming 16-byte aligned shard pointers and row strides (no launch):
+ * *kernel = 0 two-call path (a shard's width in bytes is not a multiple of 16),
+ * 1 L2-reuse kernel (rows too long to keep resident), 2 resident kernel with
+ * clusters of *cluster CTAs on a persistent grid of *grid CTAs.
+ */
+vpce_status vpce_fused_plan(vpce_dtype dtype, int t, const int64_t* vocab_start, int64_t s,
+                            int* kernel, int* cluster, int* grid);
+
+/*
  * Forward without a workspace argument, for callers that cannot allocate
  * device memory where they need the loss: a plugin inside a framework whose
  * pooling allocator already owns the GPU's memory (a raw cudaMalloc would fail

@@ -97,8 +97,9 @@ def grad_scale(reduction: str, grad: float, n_valid: int) -> float:
 
 
 def run_full(w: synth.Workload, *, t: int | None = None, s: int | None = None, vocab_start=None, ld=None,
-             reduction: str = "mean", grad: float = 1.0, misalign: int = 0, targets=None):
-    """Whole-batch parity: oracle on every row and every element."""
+             reduction: str = "mean", grad: float = 1.0, misalign: int = 0, targets=None, path: str = "split"):
+    """Whole-batch parity: oracle on every row and every element.  ``path``:
+    'split' (vpce_forward then vpce_backward) or 'fused' (vpce_forward_backward)."""
     t = w.t if t is None else t
     s = w.s if s is None else s
     w = w.replace(t=t, s=s)
@@ -115,12 +116,19 @@ def run_full(w: synth.Workload, *, t: int | None = None, s: int | None = None, v
     views = [d[:, :vs[i + 1] - vs[i]] for i, d in enumerate(dev)]
     y = torch.from_numpy(meta.targets).cuda()
     row_loss = torch.full((s,), -7.0, dtype=torch.float32, device="cuda")
-    loss, ws = vpce.vpce_forward(views, y, vs, ignore_index=w.ignore_index, reduction=reduction,
-                                 row_loss_out=row_loss)
-    flag = vpce.vpce_read_error_flag(ws)
-    loss_v = float(loss.item())
-    rl = row_loss.cpu().numpy()
-    vpce.vpce_backward(views, y, ws, vs, ignore_index=w.ignore_index, grad_output=grad)
+    if path == "split":
+        loss, ws = vpce.vpce_forward(views, y, vs, ignore_index=w.ignore_index, reduction=reduction,
+                                     row_loss_out=row_loss)
+        flag = vpce.vpce_read_error_flag(ws)
+        loss_v = float(loss.item())
+        rl = row_loss.cpu().numpy()
+        vpce.vpce_backward(views, y, ws, vs, ignore_index=w.ignore_index, grad_output=grad)
+    else:
+        loss, ws = vpce.vpce_forward_backward(views, y, vs, ignore_index=w.ignore_index, reduction=reduction,
+                                              grad_output=grad, row_loss_out=row_loss)
+        flag = vpce.vpce_read_error_flag(ws)
+        loss_v = float(loss.item())
+        rl = row_loss.cpu().numpy()
     torch.cuda.synchronize()
     back = [from_device(d, w.dtype) for d in dev]
     return dict(w=w, vs=vs, meta=meta, host=host, ref=ref, dref=dref, loss=loss_v, row_loss=rl, flag=flag,

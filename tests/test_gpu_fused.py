@@ -1,0 +1,116 @@
+"""GPU parity of vpce_forward_backward (loss and in-place dlogits in one call)
+against the fp64 oracle, element by element: every workload at every shard
+count that divides V, reductions, ignored and bad targets, the fallback for
+rows that are not 16-byte aligned, and agreement with the two-call path."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from vocab_sharded_lm_gb300 import synth, vpce
+
+from _parity import check_full, run_full
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from vocab_sharded_lm_gb300 import _build
+
+    _build.build()
+    vpce.load_library()
+
+
+@pytest.mark.parametrize("name", list(W))
+@pytest.mark.parametrize("t", [1, 2, 4, 8, 16])
+def test_fused_every_workload_every_t(name, t):
+    w = W[name]
+    if w.V % t:
+        pytest.skip("t does not divide V")
+    s = min(w.s, 40 if w.V > 100000 else 64)
+    check_full(run_full(w, t=t, s=s, path="fused"))
+
+
+def test_fused_more_rows_than_blocks():
+    # several rows per row group, ignored rows interleaved
+    check_full(run_full(W["s4096_v50304"].replace(s=700), path="fused"))
+
+
+@pytest.mark.parametrize("reduction,grad", [("sum", 0.5), ("mean", 2.5), ("mean", 0.0)])
+def test_fused_reductions(reduction, grad):
+    check_full(run_full(W["s16384_v152064"].replace(s=48), reduction=reduction, grad=grad, path="fused"))
+
+
+@pytest.mark.parametrize("widths", [[8, 8, 16], [16, 1024, 8000, 24], [4] * 64])
+def test_fused_narrow_aligned_shards(widths):
+    # 16-byte multiples, some narrower than a warp's share of a row
+    vs = [0]
+    for x in widths:
+        vs.append(vs[-1] + x)
+    w = synth.Workload("narrow", 12, 40, vs[-1], len(widths), "fp32", 2.0, "uniform", ignore_frac=0.1)
+    check_full(run_full(w, vocab_start=vs, path="fused"))
+
+
+@pytest.mark.parametrize("kw", [dict(misalign=1), dict(ld=4001 + 5)])
+def test_fused_unaligned_rows_fall_back(kw):
+    w = synth.Workload("fallback", 13, 24, 3 * 4001, 3, "bf16", 2.0, "uniform", ignore_frac=0.1)
+    check_full(run_full(w, path="fused", **kw))
+
+
+def test_fused_bad_and_all_ignored_targets():
+    w = W["tiny_s64_v1000"]
+    y = synth.row_meta(w).targets.copy()
+    y[3] = 5000
+    res = run_full(w, targets=y, path="fused")
+    assert res["flag"] & vpce.VPCE_FLAG_BAD_TARGET and math.isnan(res["loss"])
+    check_full(res)
+    res = run_full(W["s4096_v50304"].replace(s=20), targets=np.full(20, -100), path="fused")
+    assert math.isnan(res["loss"])
+    check_full(res)
+
+
+def test_fused_empty_batch():
+    dev = [torch.empty((0, 16), dtype=torch.float32, device="cuda") for _ in range(2)]
+    y = torch.empty(0, dtype=torch.int64, device="cuda")
+    loss, _ = vpce.vpce_forward_backward(dev, y, [0, 16, 32])
+    assert math.isnan(float(loss))
+    loss, _ = vpce.vpce_forward_backward(dev, y, [0, 16, 32], reduction="sum")
+    assert float(loss) == 0.0
+
+
+def test_fused_matches_split_and_is_deterministic():
+    w = W["s8192_v128256"].replace(s=96)
+    a = run_full(w, path="fused")
+    b = run_full(w, path="fused")
+    c = run_full(w, path="split")
+    assert a["loss"] == b["loss"]
+    for x, y in zip(a["back"], b["back"]):
+        np.testing.assert_array_equal(x, y)
+    assert abs(a["loss"] - c["loss"]) <= 1e-6 * abs(c["loss"])
+    np.testing.assert_allclose(a["row_loss"], c["row_loss"], rtol=2e-6)
+
+
+def test_fused_rows_too_long_for_clusters_use_the_l2_kernel():
+    # 2 MB fp32 rows need more than 8 CTAs of shared memory: the L2-reuse kernel runs
+    w = synth.Workload("longrows", 14, 6, 500000, 4, "fp32", 2.0, "uniform")
+    check_full(run_full(w, path="fused"))
+
+
+@pytest.mark.parametrize("name,C", [("tiny_s64_v1000", 1), ("s4096_v50304", 2), ("s8192_v128256", 4),
+                                    ("s16384_v152064", 0), ("s32768_v256000", 8)])
+def test_fused_cluster_sizes(name, C):
+    # the resident kernel's cluster size for each workload, and the library agrees
+    w = W[name]
+    vs = synth.even_vocab_start(w.V, w.t)
+    assert vpce.resident_cluster_size(vs, w.elem_bytes) == C
+    plan = vpce.vpce_fused_plan(vpce.VPCE_BF16 if w.dtype == "bf16" else vpce.VPCE_FP32, vs, w.s)
+    if C == 0:
+        assert plan["kernel"] != "resident"
+    else:
+        assert plan["kernel"] == "resident" and plan["cluster"] == C and plan["grid"] % C == 0

@@ -10,6 +10,19 @@
 namespace vpce {
 cudaError_t set_stats_smem();
 cudaError_t set_backward_smem();
+cudaError_t set_fused_smem();
+cudaError_t set_resident_smem();
+bool fused_supported(const ShardSet& sh, int t, int elem);
+void launch_prep(const long long* targets, long long s, long long V, long long ignore_index, Header* hdr,
+                 int reduction, float* loss_out, cudaStream_t st);
+void launch_l2fused(const ShardSet& sh, bool bf16, int t, long long s, long long V, const long long* targets,
+                    long long ignore_index, int reduction, float grad, float* lse, float* rowl, float* row_loss,
+                    float* loss_out, Header* hdr, int sms, cudaStream_t st);
+int resident_cluster_size(const ShardSet& sh, int t, int eb);
+int resident_max_clusters(bool bf16, int C, int dev);
+bool launch_resident(const ShardSet& sh, bool bf16, int C, int t, long long s, long long V, const long long* targets,
+                     long long ignore_index, int reduction, float grad, float* lse, float* rowl, float* row_loss,
+                     float* loss_out, Header* hdr, int dev, cudaStream_t st);
 }  // namespace vpce
 
 using namespace vpce;
@@ -48,7 +61,8 @@ vpce_status device_setup(int* sms) {
     }
     if (major != 10 || minor != 3) {
       d.status = VPCE_ERR_UNSUPPORTED_DEVICE;
-    } else if (set_stats_smem() != cudaSuccess || set_backward_smem() != cudaSuccess) {
+    } else if (set_stats_smem() != cudaSuccess || set_backward_smem() != cudaSuccess ||
+               set_fused_smem() != cudaSuccess || set_resident_smem() != cudaSuccess) {
       cudaGetLastError();
       return VPCE_ERR_CUDA;
     } else {
@@ -213,6 +227,93 @@ vpce_status vpce_backward(void* const* shards, vpce_dtype dtype, int t, int64_t 
   if (dtype == VPCE_BF16) launch_backward<__nv_bfloat16>(p, grid, cs);
   else launch_backward<float>(p, grid, cs);
   return launch_status();
+}
+
+vpce_status vpce_forward_backward(void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                                  const int64_t* vocab_start, int64_t ld, const int64_t* targets,
+                                  int64_t ignore_index, vpce_reduction reduction, float grad_output,
+                                  float* loss_out, float* row_loss_out, void* workspace, size_t workspace_bytes,
+                                  vpce_stream_t stream) {
+  ShardSet sh;
+  long long V = 0;
+  vpce_status st = check_logits(reinterpret_cast<const void* const*>(shards), dtype, t, s, vocab_start, ld,
+                                targets, &sh, &V);
+  if (st != VPCE_OK) return st;
+  if (reduction != VPCE_MEAN && reduction != VPCE_SUM) return VPCE_ERR_INVALID_ARG;
+  if (!std::isfinite(grad_output)) return VPCE_ERR_INVALID_ARG;
+  if (loss_out == nullptr) return VPCE_ERR_INVALID_ARG;
+  if (!aligned(loss_out, 4) || (row_loss_out != nullptr && !aligned(row_loss_out, 4))) return VPCE_ERR_ALIGNMENT;
+  st = check_workspace(workspace, workspace_bytes, t, s);
+  if (st != VPCE_OK) return st;
+  int sms = 0;
+  st = device_setup(&sms);
+  if (st != VPCE_OK) return st;
+  const int eb = dtype == VPCE_BF16 ? 2 : 4;
+  if (s > 0 && !fused_supported(sh, t, eb)) {
+    // rows that are not 16-byte aligned: the two-kernel path (same results)
+    st = vpce_forward(reinterpret_cast<const void* const*>(shards), dtype, t, s, vocab_start, ld, targets,
+                      ignore_index, reduction, loss_out, row_loss_out, workspace, workspace_bytes, stream);
+    if (st != VPCE_OK) return st;
+    return vpce_backward(shards, dtype, t, s, vocab_start, ld, targets, ignore_index, grad_output, workspace,
+                         workspace_bytes, stream);
+  }
+  const WsLayout L(t, s);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  const long long* tg = reinterpret_cast<const long long*>(targets);
+  Header* hdr = reinterpret_cast<Header*>(ws);
+  float* lse = reinterpret_cast<float*>(ws + L.lse);
+  float* rowl = reinterpret_cast<float*>(ws + L.tgt);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  launch_prep(tg, s, V, ignore_index, hdr, int(reduction), loss_out, cs);
+  if ((st = launch_status()) != VPCE_OK || s == 0) return st;
+  // rows resident in (clusters of) CTAs when they fit, else the L2-reuse kernel
+  const int C = resident_cluster_size(sh, t, eb);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (C > 0 && launch_resident(sh, dtype == VPCE_BF16, C, t, s, V, tg, ignore_index, int(reduction), grad_output,
+                               lse, rowl, row_loss_out, loss_out, hdr, dev, cs))
+    return launch_status();
+  launch_l2fused(sh, dtype == VPCE_BF16, t, s, V, tg, ignore_index, int(reduction), grad_output, lse, rowl,
+                 row_loss_out, loss_out, hdr, sms, cs);
+  return launch_status();
+}
+
+vpce_status vpce_fused_plan(vpce_dtype dtype, int t, const int64_t* vocab_start, int64_t s, int* kernel,
+                           int* cluster, int* grid) {
+  if (kernel == nullptr || cluster == nullptr || grid == nullptr) return VPCE_ERR_INVALID_ARG;
+  if (dtype != VPCE_FP32 && dtype != VPCE_BF16) return VPCE_ERR_DTYPE;
+  if (t < 1 || t > VPCE_MAX_SHARDS || s < 0 || vocab_start == nullptr || vocab_start[0] != 0)
+    return VPCE_ERR_INVALID_ARG;
+  ShardSet sh;
+  std::memset(&sh, 0, sizeof(sh));
+  for (int i = 0; i <= t; ++i) sh.start[i] = vocab_start[i];
+  for (int i = 0; i < t; ++i)
+    if (vocab_start[i + 1] <= vocab_start[i]) return VPCE_ERR_INVALID_ARG;
+  int sms = 0;
+  vpce_status st = device_setup(&sms);
+  if (st != VPCE_OK) return st;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int eb = dtype == VPCE_BF16 ? 2 : 4;
+  *kernel = 0;
+  *cluster = 0;
+  *grid = 0;
+  for (int i = 0; i < t; ++i)
+    if (((vocab_start[i + 1] - vocab_start[i]) * eb) & 15) return VPCE_OK;
+  const int C = resident_cluster_size(sh, t, eb);
+  if (C > 0) {
+    const int n = resident_max_clusters(dtype == VPCE_BF16, C, dev);
+    if (n > 0) {
+      *kernel = 2;
+      *cluster = C;
+      *grid = int((n < s ? n : s) * C);
+      return VPCE_OK;
+    }
+  }
+  *kernel = 1;
+  *cluster = 1;
+  *grid = sms;
+  return VPCE_OK;
 }
 
 vpce_status vpce_read_error_flag(const void* workspace, int* flag, vpce_stream_t stream) {

@@ -6,7 +6,7 @@
 // segment is streamed through shared memory once: the bulk-copy engine loads a
 // chunk, the warp turns it into dlogits in place, and the bulk-copy engine
 // writes it back over the logits -- one read and one write of the shards.
-#include "vpce_kernels.cuh"
+#include "vpce_chunk.cuh"
 
 namespace vpce {
 
@@ -38,26 +38,6 @@ struct ChunkCursorB {
   __device__ __forceinline__ unsigned bytes() const { return min(unsigned(kChunk), g.body - off); }
   __device__ __forceinline__ const unsigned char* src() const { return g.addr + g.head + off; }
 };
-
-// p_k * scale for every element of the lane's vectors, written back in place.
-template <typename T>
-__device__ __forceinline__ void grad_chunk(unsigned char* buf, unsigned n, int lane, float c, float scale) {
-  constexpr int VPL = kChunk / 512;
-  constexpr int EPV = Elem<T>::kPerVec;
-  uint4* v = reinterpret_cast<uint4*>(buf);
-  const int nv = int(n >> 4);
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int idx = lane + 32 * j;
-    if (idx < nv) {
-      float x[EPV];
-      unpack(v[idx], x, T());
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) x[e] = ex2(fmaf(x[e], kLog2e, c)) * scale;
-      v[idx] = pack(x, T());
-    }
-  }
-}
 
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32, 1) backward_kernel(const __grid_constant__ BackwardParams p) {
@@ -156,7 +136,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) backward_kernel(const __grid_c
         break;
       }
       unsigned char* buf = ring + slot * kChunk;
-      grad_chunk<T>(buf, n, lane, c, scale);
+      grad_chunk<T, kChunk / 512>(buf, n, lane, c, scale);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {

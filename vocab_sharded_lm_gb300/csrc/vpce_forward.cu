@@ -11,7 +11,7 @@
 // Kernel 2 (combine) folds the t partials of each row in ascending shard order
 // (the on-device stand-in for the pages' max / sum / sum all-reduces), masks
 // ignore_index, and reduces the batch in a fixed order in fp64.
-#include "vpce_kernels.cuh"
+#include "vpce_chunk.cuh"
 
 namespace vpce {
 
@@ -45,88 +45,6 @@ struct ChunkCursor {
   __device__ __forceinline__ unsigned bytes() const { return min(unsigned(kChunk), g.body - off); }
   __device__ __forceinline__ const unsigned char* src() const { return g.addr + g.head + off; }
 };
-
-// Max over the lane's vectors of one chunk, then the sum of exponentials
-// against the updated running max (one rescale per chunk, not per element).
-template <typename T>
-__device__ __forceinline__ void stats_chunk(const unsigned char* buf, unsigned n, int lane, float& m, float& sm);
-
-template <>
-__device__ __forceinline__ void stats_chunk<__nv_bfloat16>(const unsigned char* buf, unsigned n, int lane,
-                                                           float& m, float& sm) {
-  constexpr int VPL = kChunk / 512;
-  const uint4* v = reinterpret_cast<const uint4*>(buf);
-  const int nv = int(n >> 4);
-  uint4 q[VPL];
-  const uint4 neg = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);  // bf16 -inf x8
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int idx = lane + 32 * j;
-    q[j] = idx < nv ? v[idx] : neg;
-  }
-  __nv_bfloat162 mx = __halves2bfloat162(__ushort_as_bfloat16(0xff80), __ushort_as_bfloat16(0xff80));
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&q[j].x));
-    mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&q[j].y));
-    mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&q[j].z));
-    mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&q[j].w));
-  }
-  const float cm = fmaxf(__low2float(mx), __high2float(mx));
-  if (cm > m) {
-    sm *= ex2((m - cm) * kLog2e);
-    m = cm;
-  }
-  if (m == -INFINITY) return;
-  const float nb = -m * kLog2e;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    float x[8];
-    unpack(q[j], x, __nv_bfloat16());
-    a0 += ex2(fmaf(x[0], kLog2e, nb));
-    a1 += ex2(fmaf(x[1], kLog2e, nb));
-    a2 += ex2(fmaf(x[2], kLog2e, nb));
-    a3 += ex2(fmaf(x[3], kLog2e, nb));
-    a0 += ex2(fmaf(x[4], kLog2e, nb));
-    a1 += ex2(fmaf(x[5], kLog2e, nb));
-    a2 += ex2(fmaf(x[6], kLog2e, nb));
-    a3 += ex2(fmaf(x[7], kLog2e, nb));
-  }
-  sm += (a0 + a1) + (a2 + a3);
-}
-
-template <>
-__device__ __forceinline__ void stats_chunk<float>(const unsigned char* buf, unsigned n, int lane, float& m,
-                                                   float& sm) {
-  constexpr int VPL = kChunk / 512;
-  const float4* v = reinterpret_cast<const float4*>(buf);
-  const int nv = int(n >> 4);
-  float4 q[VPL];
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int idx = lane + 32 * j;
-    q[j] = idx < nv ? v[idx] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-  }
-  float cm = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) cm = fmaxf(cm, fmaxf(fmaxf(q[j].x, q[j].y), fmaxf(q[j].z, q[j].w)));
-  if (cm > m) {
-    sm *= ex2((m - cm) * kLog2e);
-    m = cm;
-  }
-  if (m == -INFINITY) return;
-  const float nb = -m * kLog2e;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    a0 += ex2(fmaf(q[j].x, kLog2e, nb));
-    a1 += ex2(fmaf(q[j].y, kLog2e, nb));
-    a2 += ex2(fmaf(q[j].z, kLog2e, nb));
-    a3 += ex2(fmaf(q[j].w, kLog2e, nb));
-  }
-  sm += (a0 + a1) + (a2 + a3);
-}
 
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32, 1) partial_stats_kernel(const __grid_constant__ StatsParams p) {
@@ -201,7 +119,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) partial_stats_kernel(const __g
         alive = false;
         break;
       }
-      stats_chunk<T>(ring + slot * kChunk, n, lane, m, sm);
+      stats_chunk<kChunk / 512>(ring + slot * kChunk, n, lane, m, sm, T());
       __syncwarp();
       if (prod.ok) {
         if (lane == 0) {

@@ -63,6 +63,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.vpce_backward.restype = ctypes.c_int
         lib.vpce_backward.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
                                       ctypes.c_float, _P, ctypes.c_size_t, _P]
+        lib.vpce_forward_backward.restype = ctypes.c_int
+        lib.vpce_forward_backward.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
+                                              ctypes.c_int, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+        lib.vpce_fused_plan.restype = ctypes.c_int
+        lib.vpce_fused_plan.argtypes = [ctypes.c_int, ctypes.c_int, _I64P, _I64, ctypes.POINTER(ctypes.c_int),
+                                        ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
         lib.vpce_forward_static.restype = ctypes.c_int
         lib.vpce_forward_static.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
                                             ctypes.c_int, _P, _P, _P]
@@ -211,6 +217,55 @@ def vpce_backward(shards, targets, workspace, vocab_start=None, *, ignore_index:
     return shards
 
 
+def forward_backward_raw(shard_ptrs, dtype, t, s, vocab_start, ld, targets_ptr, ignore_index, reduction, grad,
+                         loss_ptr, row_loss_ptr, ws_ptr, ws_bytes, stream) -> int:
+    lib = load_library()
+    ptrs = _ptr_array(shard_ptrs) if shard_ptrs is not None else None
+    vs = _i64_array(vocab_start) if vocab_start is not None else None
+    return int(lib.vpce_forward_backward(ctypes.cast(ptrs, _P) if ptrs is not None else None, int(dtype),
+                                         int(t), int(s), vs, int(ld), targets_ptr, int(ignore_index),
+                                         int(reduction), float(grad), loss_ptr, row_loss_ptr, ws_ptr,
+                                         int(ws_bytes), stream))
+
+
+def vpce_forward_backward(shards, targets, vocab_start=None, *, ignore_index: int = -100,
+                          reduction: str = "mean", grad_output: float = 1.0, loss_out=None, row_loss_out=None,
+                          workspace=None, stream=None):
+    """Loss and in-place dlogits in one call (the logits cross HBM once each
+    way).  Returns ``(loss, workspace)``; ``shards`` now hold dlogits."""
+    import torch
+
+    dtype, s, vs, ld = _describe(shards, vocab_start)
+    t = len(shards)
+    dev = shards[0].device
+    if targets.dtype != torch.int64 or not targets.is_cuda or targets.numel() != s:
+        raise ValueError("targets must be a CUDA int64 tensor with one entry per row")
+    if workspace is None:
+        workspace = new_workspace(t, s, dev)
+    if loss_out is None:
+        loss_out = torch.empty((), dtype=torch.float32, device=dev)
+    red = {"mean": VPCE_MEAN, "sum": VPCE_SUM}[reduction]
+    code = forward_backward_raw([sh.data_ptr() for sh in shards], dtype, t, s, vs, ld,
+                                ctypes.c_void_p(targets.data_ptr()), ignore_index, red, grad_output,
+                                ctypes.c_void_p(loss_out.data_ptr()),
+                                ctypes.c_void_p(row_loss_out.data_ptr()) if row_loss_out is not None else None,
+                                ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+    if code != VPCE_OK:
+        raise VPCEError(code, "vpce_forward_backward")
+    return loss_out, workspace
+
+
+def vpce_fused_plan(dtype: int, vocab_start, s: int) -> dict:
+    """The launch vpce_forward_backward would use (kernel: 0 two-call path,
+    1 L2-reuse kernel, 2 resident kernel; cluster size; grid in CTAs)."""
+    k, c, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    code = load_library().vpce_fused_plan(int(dtype), len(vocab_start) - 1, _i64_array(vocab_start), int(s),
+                                          ctypes.byref(k), ctypes.byref(c), ctypes.byref(g))
+    if code != VPCE_OK:
+        raise VPCEError(code, "vpce_fused_plan")
+    return {"kernel": ["split", "l2_reuse", "resident"][k.value], "cluster": c.value, "grid": g.value}
+
+
 def vpce_read_error_flag(workspace, stream=None) -> int:
     flag = ctypes.c_int(0)
     code = load_library().vpce_read_error_flag(ctypes.c_void_p(workspace.data_ptr()), ctypes.byref(flag),
@@ -250,3 +305,43 @@ def vpce_forward_static(shards, targets, loss_out, vocab_start=None, *, ignore_i
     if code != VPCE_OK:
         raise VPCEError(code, "vpce_forward_static")
     return loss_out
+
+
+# ----------------------------------------------------------------------------
+# host-side mirror of the resident kernel's cluster-size choice (diagnostics)
+# ----------------------------------------------------------------------------
+RESIDENT_CHUNK = 4096
+RESIDENT_WARPS = 16
+RESIDENT_SLOTS = 3
+RESIDENT_MAX_PER_WARP = 4
+RESIDENT_MAX_CLUSTER = 8
+
+
+def _resident_chunks(vocab_start, eb, C, c, w):
+    widths = [(vocab_start[i + 1] - vocab_start[i]) * eb for i in range(len(vocab_start) - 1)]
+    R = sum(widths)
+    plo = (R * c // C) & ~15
+    phi = R if c == C - 1 else (R * (c + 1) // C) & ~15
+    lo = plo + (((phi - plo) * w // RESIDENT_WARPS) & ~15)
+    hi = phi if w == RESIDENT_WARPS - 1 else plo + (((phi - plo) * (w + 1) // RESIDENT_WARPS) & ~15)
+    pos = n = 0
+    for W in widths:
+        a, b = max(lo, pos), min(hi, pos + W)
+        if a < b:
+            n += (b - a + RESIDENT_CHUNK - 1) // RESIDENT_CHUNK
+        pos += W
+    return n
+
+
+def resident_cluster_size(vocab_start, elem_bytes):
+    """Cluster size vpce_forward_backward uses to keep rows resident (0: the
+    rows are too long; the L2-reuse kernel runs instead).  Mirrors the library."""
+    def worst(C):
+        return max(_resident_chunks(vocab_start, elem_bytes, C, c, w)
+                   for c in range(C) for w in range(RESIDENT_WARPS))
+    for C in range(1, RESIDENT_MAX_CLUSTER + 1):
+        n = worst(C)
+        if n <= RESIDENT_MAX_PER_WARP and 3 * n <= RESIDENT_SLOTS:
+            return C
+    n8 = worst(RESIDENT_MAX_CLUSTER)
+    return RESIDENT_MAX_CLUSTER if (n8 <= RESIDENT_MAX_PER_WARP and 2 * n8 <= RESIDENT_SLOTS) else 0
