@@ -133,8 +133,9 @@ vpce_status vpce_backward(void* const* shards, vpce_dtype dtype, int t, int64_t 
  * overwritten in place with dlogits for upstream gradient grad_output (as
  * vpce_backward), for the common case where the loss is the last op and g is
  * known before the forward runs (1.0, or a loss scale).  Each row's backward
- * follows its forward while the row is still in L2, so the logits cross HBM
- * once in each direction (two passes of traffic instead of three).  Arguments
+ * follows its forward while the row is still in L2 (a CTA's stats warps
+ * stream a row in, its grad warps re-read it from L2 about a row later), so
+ * the logits cross HBM about once in each direction instead of three passes.  Arguments
  * as vpce_forward plus grad_output; the workspace afterwards holds logsumexp
  * and n_valid like a forward's.  Rows that are not 16-byte aligned (shard
  * pointer, row stride or width in bytes) run the two-call path instead, with
@@ -151,10 +152,10 @@ vpce_status vpce_forward_backward(void* const* shards, vpce_dtype dtype, int t, 
 
 /*
  * How vpce_forward_backward would run the given problem on the current
- * device, assuming 16-byte aligned shard pointers and row strides (no launch):
- * *kernel = 0 two-call path (a shard's width in bytes is not a multiple of 16),
- * 1 L2-reuse kernel (rows too long to keep resident), 2 resident kernel with
- * clusters of *cluster CTAs on a persistent grid of *grid CTAs.
+ * device (no launch): *kernel = 0 two-call path (a shard's width in bytes is
+ * not a multiple of 16; misaligned pointers or strides also take it),
+ * 1 fused streaming kernel on a persistent grid of *grid CTAs, one per SM
+ * (*cluster is 1).
  */
 vpce_status vpce_fused_plan(vpce_dtype dtype, int t, const int64_t* vocab_start, int64_t s,
                             int* kernel, int* cluster, int* grid);

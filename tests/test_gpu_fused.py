@@ -96,21 +96,17 @@ def test_fused_matches_split_and_is_deterministic():
     np.testing.assert_allclose(a["row_loss"], c["row_loss"], rtol=2e-6)
 
 
-def test_fused_rows_too_long_for_clusters_use_the_l2_kernel():
-    # 2 MB fp32 rows need more than 8 CTAs of shared memory: the L2-reuse kernel runs
+def test_fused_long_rows():
+    # 2 MB fp32 rows: every stats warp walks several chunks per shard segment
     w = synth.Workload("longrows", 14, 6, 500000, 4, "fp32", 2.0, "uniform")
     check_full(run_full(w, path="fused"))
 
 
-@pytest.mark.parametrize("name,C", [("tiny_s64_v1000", 1), ("s4096_v50304", 2), ("s8192_v128256", 4),
-                                    ("s16384_v152064", 0), ("s32768_v256000", 8)])
-def test_fused_cluster_sizes(name, C):
-    # the resident kernel's cluster size for each workload, and the library agrees
+@pytest.mark.parametrize("name", list(W))
+def test_fused_plan(name):
     w = W[name]
     vs = synth.even_vocab_start(w.V, w.t)
-    assert vpce.resident_cluster_size(vs, w.elem_bytes) == C
     plan = vpce.vpce_fused_plan(vpce.VPCE_BF16 if w.dtype == "bf16" else vpce.VPCE_FP32, vs, w.s)
-    if C == 0:
-        assert plan["kernel"] != "resident"
-    else:
-        assert plan["kernel"] == "resident" and plan["cluster"] == C and plan["grid"] % C == 0
+    assert plan["kernel"] == "stream" and 0 < plan["grid"] <= w.s
+    odd = [0, 3, 10]  # a 3-column bf16 shard is not a 16-byte multiple
+    assert vpce.vpce_fused_plan(vpce.VPCE_BF16, odd, 4)["kernel"] == "split"

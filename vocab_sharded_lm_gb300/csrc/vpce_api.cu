@@ -11,18 +11,13 @@ namespace vpce {
 cudaError_t set_stats_smem();
 cudaError_t set_backward_smem();
 cudaError_t set_fused_smem();
-cudaError_t set_resident_smem();
 bool fused_supported(const ShardSet& sh, int t, int elem);
 void launch_prep(const long long* targets, long long s, long long V, long long ignore_index, Header* hdr,
                  int reduction, float* loss_out, cudaStream_t st);
-void launch_l2fused(const ShardSet& sh, bool bf16, int t, long long s, long long V, const long long* targets,
-                    long long ignore_index, int reduction, float grad, float* lse, float* rowl, float* row_loss,
-                    float* loss_out, Header* hdr, int sms, cudaStream_t st);
-int resident_cluster_size(const ShardSet& sh, int t, int eb);
-int resident_max_clusters(bool bf16, int C, int dev);
-bool launch_resident(const ShardSet& sh, bool bf16, int C, int t, long long s, long long V, const long long* targets,
-                     long long ignore_index, int reduction, float grad, float* lse, float* rowl, float* row_loss,
-                     float* loss_out, Header* hdr, int dev, cudaStream_t st);
+void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long long V, const long long* targets,
+                         long long ignore_index, int reduction, float grad, float* lse, float* rowl,
+                         float* row_loss, float* loss_out, Header* hdr, int sms, cudaStream_t st);
+
 }  // namespace vpce
 
 using namespace vpce;
@@ -62,7 +57,7 @@ vpce_status device_setup(int* sms) {
     if (major != 10 || minor != 3) {
       d.status = VPCE_ERR_UNSUPPORTED_DEVICE;
     } else if (set_stats_smem() != cudaSuccess || set_backward_smem() != cudaSuccess ||
-               set_fused_smem() != cudaSuccess || set_resident_smem() != cudaSuccess) {
+               set_fused_smem() != cudaSuccess) {
       cudaGetLastError();
       return VPCE_ERR_CUDA;
     } else {
@@ -266,15 +261,8 @@ vpce_status vpce_forward_backward(void* const* shards, vpce_dtype dtype, int t, 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   launch_prep(tg, s, V, ignore_index, hdr, int(reduction), loss_out, cs);
   if ((st = launch_status()) != VPCE_OK || s == 0) return st;
-  // rows resident in (clusters of) CTAs when they fit, else the L2-reuse kernel
-  const int C = resident_cluster_size(sh, t, eb);
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (C > 0 && launch_resident(sh, dtype == VPCE_BF16, C, t, s, V, tg, ignore_index, int(reduction), grad_output,
-                               lse, rowl, row_loss_out, loss_out, hdr, dev, cs))
-    return launch_status();
-  launch_l2fused(sh, dtype == VPCE_BF16, t, s, V, tg, ignore_index, int(reduction), grad_output, lse, rowl,
-                 row_loss_out, loss_out, hdr, sms, cs);
+  launch_stream_fused(sh, dtype == VPCE_BF16, t, s, V, tg, ignore_index, int(reduction), grad_output, lse, rowl,
+                      row_loss_out, loss_out, hdr, sms, cs);
   return launch_status();
 }
 
@@ -284,35 +272,20 @@ vpce_status vpce_fused_plan(vpce_dtype dtype, int t, const int64_t* vocab_start,
   if (dtype != VPCE_FP32 && dtype != VPCE_BF16) return VPCE_ERR_DTYPE;
   if (t < 1 || t > VPCE_MAX_SHARDS || s < 0 || vocab_start == nullptr || vocab_start[0] != 0)
     return VPCE_ERR_INVALID_ARG;
-  ShardSet sh;
-  std::memset(&sh, 0, sizeof(sh));
-  for (int i = 0; i <= t; ++i) sh.start[i] = vocab_start[i];
   for (int i = 0; i < t; ++i)
     if (vocab_start[i + 1] <= vocab_start[i]) return VPCE_ERR_INVALID_ARG;
   int sms = 0;
-  vpce_status st = device_setup(&sms);
+  const vpce_status st = device_setup(&sms);
   if (st != VPCE_OK) return st;
-  int dev = 0;
-  cudaGetDevice(&dev);
   const int eb = dtype == VPCE_BF16 ? 2 : 4;
-  *kernel = 0;
-  *cluster = 0;
-  *grid = 0;
-  for (int i = 0; i < t; ++i)
-    if (((vocab_start[i + 1] - vocab_start[i]) * eb) & 15) return VPCE_OK;
-  const int C = resident_cluster_size(sh, t, eb);
-  if (C > 0) {
-    const int n = resident_max_clusters(dtype == VPCE_BF16, C, dev);
-    if (n > 0) {
-      *kernel = 2;
-      *cluster = C;
-      *grid = int((n < s ? n : s) * C);
-      return VPCE_OK;
-    }
-  }
   *kernel = 1;
   *cluster = 1;
-  *grid = sms;
+  *grid = int(s < sms ? s : sms);
+  for (int i = 0; i < t; ++i)
+    if (((vocab_start[i + 1] - vocab_start[i]) * eb) & 15) {
+      *kernel = 0;
+      *grid = 0;
+    }
   return VPCE_OK;
 }
 

@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) backward_kernel(const __grid_c
     const long long lo = p.sh.start[g.shard], hi = p.sh.start[g.shard + 1];
     const long long tcol = (y >= lo && y < hi) ? (y - lo) : -1;  // target column inside this shard
     const float c = -__ldg(p.lse + g.row) * kLog2e;
+    const float cb = folded_offset(c, scale);
 
     // the target element, computed from the original logit before the body
     // is overwritten: (p - 1) * scale
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) backward_kernel(const __grid_c
         break;
       }
       unsigned char* buf = ring + slot * kChunk;
-      grad_chunk<T, kChunk / 512>(buf, n, lane, c, scale);
+      grad_chunk<T, kChunk / 512>(buf, n, lane, c, scale, cb);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {

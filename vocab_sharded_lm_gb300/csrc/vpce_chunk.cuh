@@ -1,12 +1,21 @@
 // Per-chunk arithmetic of the streaming kernels: what a warp does with one
 // shared-memory chunk of logits.  A chunk is n bytes (a multiple of 16) of
 // 16-byte vectors; lane l takes vectors l, l + 32, ...; VPL bounds the vectors
-// per lane (chunk capacity / 512 bytes).
+// per lane (chunk capacity / 512 bytes).  Pairs of elements go through packed
+// fp32x2 instructions; every exponential is one ex2 on the special-function
+// unit.
 #pragma once
 
 #include "vpce_kernels.cuh"
 
 namespace vpce {
+
+// 2^(x * log2 e + b) of an element pair, packed
+__device__ __forceinline__ f32x2 exp2_pair(f32x2 x, f32x2 l2e, f32x2 b) {
+  float e0, e1;
+  f2_unpack(f2_fma(x, l2e, b), e0, e1);
+  return f2_pack(ex2(e0), ex2(e1));
+}
 
 // Running (max m, sum of exp(x - m)) of a lane, updated with the lane's
 // vectors of one chunk: one max over the chunk, one rescale, then the sum.
@@ -36,22 +45,20 @@ __device__ __forceinline__ void stats_chunk(const unsigned char* buf, unsigned n
     m = cm;
   }
   if (m == -INFINITY) return;
-  const float nb = -m * kLog2e;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  const f32x2 l2e = f2_pack(kLog2e, kLog2e);
+  const f32x2 nb = f2_pack(-m * kLog2e, -m * kLog2e);
+  f32x2 a0 = f2_pack(0.f, 0.f), a1 = a0;
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
-    float x[8];
-    unpack(q[j], x, __nv_bfloat16());
-    a0 += ex2(fmaf(x[0], kLog2e, nb));
-    a1 += ex2(fmaf(x[1], kLog2e, nb));
-    a2 += ex2(fmaf(x[2], kLog2e, nb));
-    a3 += ex2(fmaf(x[3], kLog2e, nb));
-    a0 += ex2(fmaf(x[4], kLog2e, nb));
-    a1 += ex2(fmaf(x[5], kLog2e, nb));
-    a2 += ex2(fmaf(x[6], kLog2e, nb));
-    a3 += ex2(fmaf(x[7], kLog2e, nb));
+    a0 = f2_add(a0, exp2_pair(f2_pack(bf16_lo(q[j].x), bf16_hi(q[j].x)), l2e, nb));
+    a1 = f2_add(a1, exp2_pair(f2_pack(bf16_lo(q[j].y), bf16_hi(q[j].y)), l2e, nb));
+    a0 = f2_add(a0, exp2_pair(f2_pack(bf16_lo(q[j].z), bf16_hi(q[j].z)), l2e, nb));
+    a1 = f2_add(a1, exp2_pair(f2_pack(bf16_lo(q[j].w), bf16_hi(q[j].w)), l2e, nb));
   }
-  sm += (a0 + a1) + (a2 + a3);
+  float s0, s1, s2, s3;
+  f2_unpack(a0, s0, s1);
+  f2_unpack(a1, s2, s3);
+  sm += (s0 + s1) + (s2 + s3);
 }
 
 template <int VPL>
@@ -73,22 +80,66 @@ __device__ __forceinline__ void stats_chunk(const unsigned char* buf, unsigned n
     m = cm;
   }
   if (m == -INFINITY) return;
-  const float nb = -m * kLog2e;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  const f32x2 l2e = f2_pack(kLog2e, kLog2e);
+  const f32x2 nb = f2_pack(-m * kLog2e, -m * kLog2e);
+  f32x2 a0 = f2_pack(0.f, 0.f), a1 = a0;
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
-    a0 += ex2(fmaf(q[j].x, kLog2e, nb));
-    a1 += ex2(fmaf(q[j].y, kLog2e, nb));
-    a2 += ex2(fmaf(q[j].z, kLog2e, nb));
-    a3 += ex2(fmaf(q[j].w, kLog2e, nb));
+    a0 = f2_add(a0, exp2_pair(f2_pack(q[j].x, q[j].y), l2e, nb));
+    a1 = f2_add(a1, exp2_pair(f2_pack(q[j].z, q[j].w), l2e, nb));
   }
-  sm += (a0 + a1) + (a2 + a3);
+  float s0, s1, s2, s3;
+  f2_unpack(a0, s0, s1);
+  f2_unpack(a1, s2, s3);
+  sm += (s0 + s1) + (s2 + s3);
 }
 
-// exp(x - lse) * scale for every element of the lane's vectors, in place
-// (c = -lse * log2 e).  The target element is patched by the caller.
+// In place over the lane's vectors: exp(x - lse) * scale.  The exponent
+// offset b folds both: b = -lse * log2 e + log2 scale, so one ex2 per element
+// and no multiply (used for scale > 0, see grad_chunk).  The
+// target element is patched by the caller.
+__device__ __forceinline__ uint4 grad_vec(const uint4& w, f32x2 l2e, f32x2 b, __nv_bfloat16) {
+  float p0, p1, p2, p3, p4, p5, p6, p7;
+  f2_unpack(exp2_pair(f2_pack(bf16_lo(w.x), bf16_hi(w.x)), l2e, b), p0, p1);
+  f2_unpack(exp2_pair(f2_pack(bf16_lo(w.y), bf16_hi(w.y)), l2e, b), p2, p3);
+  f2_unpack(exp2_pair(f2_pack(bf16_lo(w.z), bf16_hi(w.z)), l2e, b), p4, p5);
+  f2_unpack(exp2_pair(f2_pack(bf16_lo(w.w), bf16_hi(w.w)), l2e, b), p6, p7);
+  return make_uint4(pack_bf16x2(p0, p1), pack_bf16x2(p2, p3), pack_bf16x2(p4, p5), pack_bf16x2(p6, p7));
+}
+__device__ __forceinline__ uint4 grad_vec(const uint4& w, f32x2 l2e, f32x2 b, float) {
+  float p0, p1, p2, p3;
+  f2_unpack(exp2_pair(f2_pack(__uint_as_float(w.x), __uint_as_float(w.y)), l2e, b), p0, p1);
+  f2_unpack(exp2_pair(f2_pack(__uint_as_float(w.z), __uint_as_float(w.w)), l2e, b), p2, p3);
+  return make_uint4(__float_as_uint(p0), __float_as_uint(p1), __float_as_uint(p2), __float_as_uint(p3));
+}
+
 template <typename T, int VPL>
-__device__ __forceinline__ void grad_chunk(unsigned char* buf, unsigned n, int lane, float c, float scale) {
+__device__ __forceinline__ void grad_chunk_folded(unsigned char* buf, unsigned n, int lane, float b) {
+  uint4* v = reinterpret_cast<uint4*>(buf);
+  const int nv = int(n >> 4);
+  const f32x2 l2e = f2_pack(kLog2e, kLog2e);
+  const f32x2 bb = f2_pack(b, b);
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int idx = lane + 32 * j;
+    if (idx < nv) v[idx] = grad_vec(v[idx], l2e, bb, T());
+  }
+}
+
+// Exponent offset of a row for grad_chunk: -lse * log2 e + log2 scale (only
+// used when scale > 0).
+__device__ __forceinline__ float folded_offset(float c, float scale) { return scale > 0.f ? c + log2f(scale) : 0.f; }
+
+// exp(x - lse) * scale for every element of the lane's vectors, in place
+// (c = -lse * log2 e, cb = folded_offset(c, scale)).  scale > 0 folds into the
+// exponent; otherwise (g <= 0, or no valid rows) the product is taken
+// explicitly.  The target element is patched by the caller.
+template <typename T, int VPL>
+__device__ __forceinline__ void grad_chunk(unsigned char* buf, unsigned n, int lane, float c, float scale, float cb) {
+  if (scale > 0.f) {
+    grad_chunk_folded<T, VPL>(buf, n, lane, cb);
+    return;
+  }
   constexpr int EPV = Elem<T>::kPerVec;
   uint4* v = reinterpret_cast<uint4*>(buf);
   const int nv = int(n >> 4);

@@ -1,40 +1,45 @@
-// Fused forward + backward of the vocab-parallel cross-entropy: the loss and
-// the in-place dlogits in one pass over HBM.
+// Fused forward + backward of the vocab-parallel cross-entropy for rows of
+// any length: the loss and the in-place dlogits with the logits read from HBM
+// once, re-read from L2 and written once.
 //
 // The method ("Distributed Training III: Model Parallelism", CMU 11-868
 // Lecture 16 notes, §5.5; "LLM Internals" §7.3.4) reduces per row the maximum,
 // the sum of exponentials and the target logit over the vocabulary shards and
 // combines them into logsumexp - target.  When the upstream gradient g is known
 // up front (the loss is the last op, g = 1 or a loss scale), the backward of a
-// row can follow its forward immediately, while the row is still on chip:
+// row can follow its forward while the row is still on chip:
 //
-//   * a group of G warps owns one row at a time; each warp takes a 1/G
-//     sub-range of every shard segment of that row;
-//   * pass 1 streams the sub-ranges from HBM through the warp's shared-memory
-//     ring (cp.async.bulk + mbarrier) and keeps an online (max, sum-exp);
-//   * the G warps meet at a per-row mbarrier, merge their partials in warp
-//     order (every warp gets the same logsumexp) -- the on-chip stand-in for
-//     the pages' max / sum / target all-reduces;
-//   * pass 2 streams the same bytes again -- now L2 hits, the row was read
-//     microseconds earlier -- turns them into dlogits in shared memory and
-//     writes them back over the logits with cp.async.bulk stores.
+//   * a CTA owns whole rows; its 8 "stats" warps each take 1/8 of every shard
+//     segment of a row and stream it from HBM through their own shared-memory
+//     rings (cp.async.bulk + mbarrier), keeping an online (max, sum-exp) --
+//     the streaming pattern of the split forward;
+//   * per row they leave 8 partials (and the target logit) in a two-deep
+//     shared-memory mailbox -- the on-chip stand-in for the pages' max / sum /
+//     target all-reduces;
+//   * 8 "grad" warps follow about a row behind: they fold the partials in warp
+//     order into logsumexp, re-read the same bytes (L2 hits: the stats warps
+//     fetched them microseconds earlier), turn them into dlogits in shared
+//     memory and write them over the logits with cp.async.bulk stores -- the
+//     pattern of the split backward.
 //
-// HBM sees one read and one write of the logits instead of two reads and one
-// write.  The batch count n_valid (needed for the 1/n_valid of the mean before
-// any gradient is written) comes from a one-block prologue kernel that also
-// clears the workspace header; the batch loss is summed in a fixed order by the
-// last block to finish.
+// HBM sees one read and one write of the logits.  The batch count n_valid
+// (needed for the 1/n_valid of the mean before any gradient is written) comes
+// from a one-block prologue kernel that also clears the workspace header; the
+// batch loss is summed in a fixed order by the last block to finish.
 #include "vpce_chunk.cuh"
 
 namespace vpce {
 
 namespace {
 
-constexpr int kFusedWarps = 8;
 constexpr int kPrepThreads = 1024;
+constexpr int kSW = 8;         // stats warps
+constexpr int kDW = 8;         // grad warps
+constexpr int kFThreads = (kSW + kDW) * 32;
 constexpr int kFChunk = 4096;  // bytes per pipeline chunk
-constexpr int kRingA = 4;      // pass-1 (HBM) slots per warp
-constexpr int kRingB = 3;      // pass-2 (L2) slots per warp
+constexpr int kSSlots = 4;     // ring slots per stats warp (HBM latency)
+constexpr int kDSlots = 3;     // ring slots per grad warp (L2 latency)
+constexpr int kFVPL = kFChunk / 512;
 
 struct FusedParams {
   ShardSet sh;
@@ -45,11 +50,22 @@ struct FusedParams {
   long long ignore_index;
   int reduction;
   float grad;
-  float* lse;        // [s]
-  float* rowl;       // [s]: per-row loss (0 ignored, NaN bad target)
-  float* row_loss;   // optional user copy of rowl
+  float* lse;       // [s]
+  float* rowl;      // [s]: per-row loss (0 ignored, NaN bad target)
+  float* row_loss;  // optional user copy of rowl
   float* loss_out;
   Header* hdr;
+};
+
+struct FusedSmem {
+  unsigned char sring[kSW][kSSlots][kFChunk];
+  unsigned char dring[kDW][kDSlots][kFChunk];
+  uint64_t sfull[kSW][kSSlots];
+  uint64_t dfull[kDW][kDSlots];
+  uint64_t rowdone[2];  // stats warps -> grad warps: a row's partials are in
+  uint64_t rowfree[2];  // grad warps -> stats warps: the grad warps have begun that row
+  float2 part[2][kSW];
+  float tz[2];
 };
 
 // Prologue: clear the header, count the valid rows, flag bad targets.
@@ -90,25 +106,26 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const long long* tar
   }
 }
 
-// Byte range [lo, hi) of shard segment `i` owned by warp `wg` of a group of G
-// (16-byte boundaries; the last warp takes the remainder).
-template <int G>
-__device__ __forceinline__ void sub_range(unsigned seg_bytes, int wg, unsigned& lo, unsigned& hi) {
-  lo = unsigned((unsigned long long)seg_bytes * unsigned(wg) / G) & ~15u;
-  hi = wg == G - 1 ? seg_bytes : unsigned((unsigned long long)seg_bytes * unsigned(wg + 1) / G) & ~15u;
+// Byte range [lo, hi) of a shard segment owned by warp w of NW (16-byte
+// boundaries; the last warp takes the remainder).
+template <int NW>
+__device__ __forceinline__ void sub_range(unsigned seg_bytes, int w, unsigned& lo, unsigned& hi) {
+  lo = unsigned((unsigned long long)seg_bytes * unsigned(w) / NW) & ~15u;
+  hi = w == NW - 1 ? seg_bytes : unsigned((unsigned long long)seg_bytes * unsigned(w + 1) / NW) & ~15u;
 }
 
-// Walks the chunks of one row that belong to warp wg: segment by segment,
-// each sub-range cut into near-equal 16-byte aligned chunks of at most kFChunk.
-template <int G, int EB>
+// Walks the chunks of one row that belong to warp w of NW: segment by
+// segment, each sub-range cut into near-equal 16-byte aligned chunks of at
+// most kFChunk.
+template <int EB, int NW>
 struct RowWalk {
   int seg;
   unsigned k, n, lo, hi;
   bool ok;
 
-  __device__ __forceinline__ bool seek(const FusedParams& p, int wg, int from) {
+  __device__ __forceinline__ bool seek(const FusedParams& p, int w, int from) {
     for (seg = from; seg < p.t; ++seg) {
-      sub_range<G>(unsigned(p.sh.start[seg + 1] - p.sh.start[seg]) * EB, wg, lo, hi);
+      sub_range<NW>(unsigned(p.sh.start[seg + 1] - p.sh.start[seg]) * EB, w, lo, hi);
       n = (hi - lo + kFChunk - 1) / kFChunk;
       if (n > 0) {
         k = 0;
@@ -117,11 +134,10 @@ struct RowWalk {
     }
     return ok = false;
   }
-  __device__ __forceinline__ void next(const FusedParams& p, int wg) {
+  __device__ __forceinline__ void next(const FusedParams& p, int w) {
     if (++k < n) return;
-    seek(p, wg, seg + 1);
+    seek(p, w, seg + 1);
   }
-  // byte range [a, b) of the current chunk within its segment's row
   __device__ __forceinline__ void bounds(unsigned& a, unsigned& b) const {
     const unsigned len = hi - lo;
     a = lo + (unsigned((unsigned long long)len * k / n) & ~15u);
@@ -132,236 +148,243 @@ struct RowWalk {
   }
 };
 
-// Pass-1 chunk sequence of one warp across the rows of its group (ignored
-// rows and rows without chunks for this warp are skipped).
-template <int G, int EB>
-struct RowsWalk {
-  long long r, r_step;
-  RowWalk<G, EB> w;
-  bool ok;
-
-  __device__ __forceinline__ void seek_row(const FusedParams& p, int wg, long long from) {
-    ok = false;
-    for (r = from; r < p.s; r += r_step) {
-      if (__ldg(p.targets + r) == p.ignore_index) continue;
-      if (w.seek(p, wg, 0)) {
-        ok = true;
-        return;
-      }
-    }
+// segment and byte offset of target y (segment -1 when out of range)
+template <int EB>
+__device__ __forceinline__ void target_of(const FusedParams& p, long long y, int& ty, unsigned& toff) {
+  ty = -1;
+  toff = 0;
+  if (y >= 0 && y < p.V) {
+    ty = 0;
+    while (p.sh.start[ty + 1] <= y) ++ty;
+    toff = unsigned(y - p.sh.start[ty]) * EB;
   }
-  __device__ __forceinline__ void next(const FusedParams& p, int wg) {
-    w.next(p, wg);
-    if (!w.ok) seek_row(p, wg, r + r_step);
-  }
-};
+}
 
-template <typename T, int G>
-__global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(const __grid_constant__ FusedParams p) {
+template <typename T>
+__global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid_constant__ FusedParams p) {
   constexpr int EB = Elem<T>::kBytes;
-  constexpr int NG = kFusedWarps / G;   // row groups per block
-  constexpr int VPL = kFChunk / 512;
-  extern __shared__ __align__(1024) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  FusedSmem& sm = *reinterpret_cast<FusedSmem*>(smem_raw);
+  __shared__ bool last;
+  __shared__ double sv[kFThreads / 32];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int grp = warp / G, wg = warp % G;
-
-  // shared memory: pass-1 rings [warps][kRingA] | pass-2 rings [warps][kRingB]
-  // | slot barriers | row barriers [NG][2] | row partials [NG][2][G]
-  unsigned char* ringA = smem + size_t(warp) * kRingA * kFChunk;
-  unsigned char* ringB = smem + size_t(kFusedWarps) * kRingA * kFChunk + size_t(warp) * kRingB * kFChunk;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kFusedWarps) * (kRingA + kRingB) * kFChunk);
-  uint64_t* barA = bars + warp * (kRingA + kRingB);
-  uint64_t* barB = barA + kRingA;
-  uint64_t* rowbar = bars + kFusedWarps * (kRingA + kRingB) + grp * 2;
-  float2* red = reinterpret_cast<float2*>(bars + kFusedWarps * (kRingA + kRingB) + NG * 2) + grp * 2 * G;
-  __shared__ bool last;
-  __shared__ double sv[kFusedWarps];
+  const bool stats = warp < kSW;
+  const int w = stats ? warp : warp - kSW;
 
   if (lane == 0) {
-#pragma unroll
-    for (int k = 0; k < kRingA + kRingB; ++k) mbar_init(&barA[k], 1);
-    if (wg == 0) {
-      mbar_init(&rowbar[0], G);
-      mbar_init(&rowbar[1], G);
+    if (stats) {
+      for (int k = 0; k < kSSlots; ++k) mbar_init(&sm.sfull[w][k], 1);
+    } else {
+      for (int k = 0; k < kDSlots; ++k) mbar_init(&sm.dfull[w][k], 1);
+    }
+    if (warp == 0) {
+      mbar_init(&sm.rowdone[0], kSW);
+      mbar_init(&sm.rowdone[1], kSW);
+      mbar_init(&sm.rowfree[0], kDW);
+      mbar_init(&sm.rowfree[1], kDW);
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  const int n_valid = p.hdr->n_valid;
-  const float scale = p.reduction == VPCE_SUM ? p.grad : (n_valid > 0 ? p.grad / float(n_valid) : 0.f);
-  const long long r_step = (long long)gridDim.x * NG;
-  const long long r0 = (long long)blockIdx.x * NG + grp;
-  const uint64_t pol_first = policy_evict_first();
-  const uint64_t pol_last = policy_evict_last();
-
-  // ring A streams pass-1 chunks from HBM kRingA ahead, across rows; the
-  // lines are kept in L2 (evict_last) for pass 2
-  RowsWalk<G, EB> prod;
-  prod.r_step = r_step;
-  prod.seek_row(p, wg, r0);
-  unsigned issuedA = 0, kA = 0;
-  auto issueA = [&](int slot) {
-    unsigned a, b;
-    prod.w.bounds(a, b);
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&barA[slot], b - a);
-      bulk_load(ringA + slot * kFChunk, prod.w.addr(p, prod.r, a), b - a, &barA[slot], pol_last);
-    }
-    ++issuedA;
-    prod.next(p, wg);
-  };
-#pragma unroll 1
-  for (int k = 0; k < kRingA && prod.ok; ++k) issueA(k);
-
-  unsigned issuedB = 0, kB = 0, rounds = 0;
+  const long long r_step = gridDim.x;
+  const long long r0 = blockIdx.x;
   bool alive = true;
-#pragma unroll 1
-  for (long long r = r0; r < p.s && alive; r += r_step) {
-    const long long y = __ldg(p.targets + r);
-    if (y == p.ignore_index) {
-      // ignored row: zeros over this warp's sub-ranges, nothing read
-      for (int i = 0; i < p.t; ++i) {
-        unsigned lo, hi;
-        sub_range<G>(unsigned(p.sh.start[i + 1] - p.sh.start[i]) * EB, wg, lo, hi);
-        uint4* d = reinterpret_cast<uint4*>(const_cast<unsigned char*>(p.sh.ptr[i]) + r * p.sh.ld_bytes[i] + lo);
-        for (unsigned v = lane; v < (hi - lo) >> 4; v += 32) d[v] = make_uint4(0u, 0u, 0u, 0u);
-      }
-      if (wg == 0 && lane == 0) {
-        p.rowl[r] = 0.f;
-        p.lse[r] = 0.f;
-        if (p.row_loss) p.row_loss[r] = 0.f;
-      }
-      continue;
-    }
-    const bool in_range = y >= 0 && y < p.V;
-    // the target logit, read before any warp of the group can overwrite it
-    float zt = 0.f;
-    if (wg == 0 && lane == 0 && in_range) {
-      int i = 0;
-      while (p.sh.start[i + 1] <= y) ++i;
-      zt = Elem<T>::load(p.sh.ptr[i] + r * p.sh.ld_bytes[i] + (y - p.sh.start[i]) * EB);
-    }
-    const int buf = int(rounds & 1u);
-    const uint32_t rpar = (rounds >> 1) & 1u;
-    ++rounds;
 
-    // ---- pass 1: online (max, sum-exp) over this warp's sub-ranges
-    float m = -INFINITY, sm = 0.f;
-    RowWalk<G, EB> cw;
+  if (stats) {
+    // ---------------- stats warps: pass 1 from HBM over the CTA's rows.
+    // A row's loads start only once the grad warps have begun the previous
+    // row, so at most two rows per CTA are live in L2 (the one the grad warps
+    // re-read and the one streaming in).
+    unsigned char(*ring)[kFChunk] = sm.sring[w];
+    uint64_t* full = sm.sfull[w];
+    const uint64_t pol = policy_evict_last();  // the grad warps re-read these bytes
+    unsigned issued = 0;
+    unsigned kc = 0, n = 0;
 #pragma unroll 1
-    for (cw.seek(p, wg, 0); cw.ok; cw.next(p, wg)) {
-      unsigned a, b;
-      cw.bounds(a, b);
-      const int slot = int(kA % kRingA);
-      if (!mbar_wait_warp(&barA[slot], (kA / kRingA) & 1u)) {
+    for (long long r = r0; r < p.s && alive; r += r_step) {
+      const long long y = __ldg(p.targets + r);
+      if (y == p.ignore_index) continue;
+      if (n > 0 && !mbar_wait_warp(&sm.rowfree[(n - 1) & 1u], ((n - 1) >> 1) & 1u)) {
         alive = false;
         break;
       }
-      stats_chunk<VPL>(ringA + slot * kFChunk, b - a, lane, m, sm, T());
-      __syncwarp();
-      if (prod.ok) issueA(slot);
-      ++kA;
-    }
-    if (!alive) break;
-
-    // ---- pass-2 loads (L2 hits) start now, while the group meets
-    RowWalk<G, EB> iw;
-    iw.seek(p, wg, 0);
-    if (lane == 0) bulk_wait_read<0>();
-#pragma unroll 1
-    for (int k = 0; k < kRingB - 1 && iw.ok; ++k, iw.next(p, wg)) {
-      unsigned a, b;
-      iw.bounds(a, b);
-      const int slot = int(issuedB % kRingB);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&barB[slot], b - a);
-        bulk_load(ringB + slot * kFChunk, iw.addr(p, r, a), b - a, &barB[slot], pol_first);
-      }
-      ++issuedB;
-    }
-
-    warp_merge_ms(m, sm);
-    float2* rd = red + buf * G;
-    if (lane == 0) {
-      rd[wg] = make_float2(m, sm);
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&rowbar[buf])) : "memory");
-    }
-    if (!mbar_wait_warp(&rowbar[buf], rpar)) {
-      alive = false;
-      break;
-    }
-    // every warp folds the G partials in the same order -> the same lse
-    float M = rd[0].x, S = rd[0].y;
-#pragma unroll 1
-    for (int j = 1; j < G; ++j) merge_ms(M, S, rd[j].x, rd[j].y);
-    const float lse = in_range ? M + logf(S) : __int_as_float(0x7fc00000);
-    if (wg == 0 && lane == 0) {
-      const float rl = in_range ? lse - zt : lse;
-      p.lse[r] = lse;
-      p.rowl[r] = rl;
-      if (p.row_loss) p.row_loss[r] = rl;
-    }
-    const float c = -lse * kLog2e;
-
-    // ---- pass 2: dlogits in shared memory, bulk-stored over the logits
-#pragma unroll 1
-    for (cw.seek(p, wg, 0); cw.ok; cw.next(p, wg)) {
-      unsigned a, b;
-      cw.bounds(a, b);
-      const int slot = int(kB % kRingB);
-      if (!mbar_wait_warp(&barB[slot], (kB / kRingB) & 1u)) {
-        alive = false;
-        break;
-      }
-      unsigned char* sbuf = ringB + slot * kFChunk;
-      const long long col0 = p.sh.start[cw.seg];
-      const long long tb = (in_range && y >= col0 && y < p.sh.start[cw.seg + 1]) ? (y - col0) * EB : -1;
-      const bool has_t = tb >= (long long)a && tb < (long long)b;
-      float dt = 0.f;
-      if (has_t && lane == 0) {
-        const float z = Elem<T>::load(sbuf + (tb - a));
-        dt = (ex2(fmaf(z, kLog2e, c)) - 1.f) * scale;
-      }
-      __syncwarp();
-      grad_chunk<T, VPL>(sbuf, b - a, lane, c, scale);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        if (has_t) {
-          Elem<T>::store(sbuf + (tb - a), dt);
-          fence_proxy_async_smem();
-        }
-        bulk_store(cw.addr(p, r, a), sbuf, b - a, pol_first);
-        bulk_commit();
-      }
-      if (iw.ok) {
-        unsigned ia, ib;
-        iw.bounds(ia, ib);
-        const int ps = int(issuedB % kRingB);  // the slot of the previous chunk
+      int ty;
+      unsigned toff;
+      target_of<EB>(p, y, ty, toff);
+      RowWalk<EB, kSW> iw, cw;
+      iw.seek(p, w, 0);
+      for (int k = 0; k < kSSlots && iw.ok; ++k, iw.next(p, w)) {
+        unsigned a, b;
+        iw.bounds(a, b);
+        const int slot = int(issued % kSSlots);
         if (lane == 0) {
-          bulk_wait_read<1>();
-          mbar_arrive_expect_tx(&barB[ps], ib - ia);
-          bulk_load(ringB + ps * kFChunk, iw.addr(p, r, ia), ib - ia, &barB[ps], pol_first);
+          mbar_arrive_expect_tx(&full[slot], b - a);
+          bulk_load(ring[slot], iw.addr(p, r, a), b - a, &full[slot], pol);
         }
-        ++issuedB;
-        iw.next(p, wg);
+        ++issued;
       }
-      ++kB;
+      float m = -INFINITY, se = 0.f, zt = 0.f;
+      bool has_t = false;
+#pragma unroll 1
+      for (cw.seek(p, w, 0); cw.ok; cw.next(p, w)) {
+        unsigned a, b;
+        cw.bounds(a, b);
+        const int slot = int(kc % kSSlots);
+        if (!mbar_wait_warp(&full[slot], (kc / kSSlots) & 1u)) {
+          alive = false;
+          break;
+        }
+        stats_chunk<kFVPL>(ring[slot], b - a, lane, m, se, T());
+        if (cw.seg == ty && toff >= a && toff < b) {
+          has_t = true;
+          zt = Elem<T>::load(ring[slot] + (toff - a));
+        }
+        __syncwarp();
+        if (iw.ok) {  // refill this slot with the row's next chunk
+          unsigned ia, ib;
+          iw.bounds(ia, ib);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[slot], ib - ia);
+            bulk_load(ring[slot], iw.addr(p, r, ia), ib - ia, &full[slot], pol);
+          }
+          ++issued;
+          iw.next(p, w);
+        }
+        ++kc;
+      }
+      if (!alive) break;
+      warp_merge_ms(m, se);
+      const int buf = int(n & 1u);
+      if (lane == 0) {
+        sm.part[buf][w] = make_float2(m, se);
+        if (has_t) sm.tz[buf] = zt;
+        mbar_arrive_local(&sm.rowdone[buf]);
+      }
+      ++n;
     }
-  }
+    if (!alive) {
+      if (lane == 0) atomicOr(&p.hdr->error_flag, VPCE_FLAG_WAIT_TIMEOUT);
+      for (unsigned i = kc; i < issued; ++i)
+        if (!mbar_wait_warp(&full[i % kSSlots], (i / kSSlots) & 1u)) break;
+    }
+  } else {
+    // ---------------- grad warps: logsumexp from the mailbox, pass 2 from L2
+    unsigned char(*ring)[kFChunk] = sm.dring[w];
+    uint64_t* full = sm.dfull[w];
+    const uint64_t pol = policy_evict_first();
+    const int n_valid = p.hdr->n_valid;
+    const float scale = p.reduction == VPCE_SUM ? p.grad : (n_valid > 0 ? p.grad / float(n_valid) : 0.f);
+    unsigned kc = 0, issued = 0, n = 0;
+#pragma unroll 1
+    for (long long r = r0; r < p.s && alive; r += r_step) {
+      const long long y = __ldg(p.targets + r);
+      if (y == p.ignore_index) {
+        // ignored row: zeros over this warp's share, nothing read
+        for (int i = 0; i < p.t; ++i) {
+          unsigned lo, hi;
+          sub_range<kDW>(unsigned(p.sh.start[i + 1] - p.sh.start[i]) * EB, w, lo, hi);
+          uint4* d = reinterpret_cast<uint4*>(const_cast<unsigned char*>(p.sh.ptr[i]) + r * p.sh.ld_bytes[i] + lo);
+          for (unsigned v = lane; v < (hi - lo) >> 4; v += 32) d[v] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (w == 0 && lane == 0) {
+          p.rowl[r] = 0.f;
+          p.lse[r] = 0.f;
+          if (p.row_loss) p.row_loss[r] = 0.f;
+        }
+        continue;
+      }
+      int ty;
+      unsigned toff;
+      target_of<EB>(p, y, ty, toff);
+      const bool in_range = ty >= 0;
+      const int buf = int(n & 1u);
+      if (!mbar_wait_warp(&sm.rowdone[buf], (n >> 1) & 1u)) {
+        alive = false;
+        break;
+      }
+      // every grad warp folds the partials in the same order: the same lse
+      float M = sm.part[buf][0].x, S = sm.part[buf][0].y;
+#pragma unroll
+      for (int j = 1; j < kSW; ++j) merge_ms(M, S, sm.part[buf][j].x, sm.part[buf][j].y);
+      const float zt = sm.tz[buf];
+      __syncwarp();
+      if (lane == 0) mbar_arrive_local(&sm.rowfree[buf]);
+      ++n;
+      const float lse = in_range ? M + logf(S) : __int_as_float(0x7fc00000);
+      if (w == 0 && lane == 0) {
+        const float rl = in_range ? lse - zt : lse;
+        p.lse[r] = lse;
+        p.rowl[r] = rl;
+        if (p.row_loss) p.row_loss[r] = rl;
+      }
+      const float c = -lse * kLog2e;
+      const float cb = folded_offset(c, scale);
 
-  if (!alive) {
-    if (lane == 0) atomicOr(&p.hdr->error_flag, VPCE_FLAG_WAIT_TIMEOUT);
-    for (unsigned k = kA; k < issuedA; ++k) {
-      if (!mbar_wait_warp(&barA[k % kRingA], (k / kRingA) & 1u)) break;
+      // this row's chunks, kDSlots - 1 loads ahead; a slot is refilled once
+      // its store has read it
+      RowWalk<EB, kDW> iw, cw;
+      iw.seek(p, w, 0);
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
+      for (int k = 0; k < kDSlots - 1 && iw.ok; ++k, iw.next(p, w)) {
+        unsigned a, b;
+        iw.bounds(a, b);
+        const int slot = int(issued % kDSlots);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[slot], b - a);
+          bulk_load(ring[slot], iw.addr(p, r, a), b - a, &full[slot], pol);
+        }
+        ++issued;
+      }
+#pragma unroll 1
+      for (cw.seek(p, w, 0); cw.ok; cw.next(p, w)) {
+        unsigned a, b;
+        cw.bounds(a, b);
+        const int slot = int(kc % kDSlots);
+        if (!mbar_wait_warp(&full[slot], (kc / kDSlots) & 1u)) {
+          alive = false;
+          break;
+        }
+        unsigned char* sbuf = ring[slot];
+        const bool has_t = cw.seg == ty && toff >= a && toff < b;
+        float dt = 0.f;
+        if (has_t && lane == 0) dt = (ex2(fmaf(Elem<T>::load(sbuf + (toff - a)), kLog2e, c)) - 1.f) * scale;
+        __syncwarp();
+        grad_chunk<T, kFVPL>(sbuf, b - a, lane, c, scale, cb);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (has_t) {
+            Elem<T>::store(sbuf + (toff - a), dt);
+            fence_proxy_async_smem();
+          }
+          bulk_store(cw.addr(p, r, a), sbuf, b - a, pol);
+          bulk_commit();
+        }
+        if (iw.ok) {
+          unsigned ia, ib;
+          iw.bounds(ia, ib);
+          const int ps = int(issued % kDSlots);  // the slot of the previous chunk
+          if (lane == 0) {
+            bulk_wait_read<1>();
+            mbar_arrive_expect_tx(&full[ps], ib - ia);
+            bulk_load(ring[ps], iw.addr(p, r, ia), ib - ia, &full[ps], pol);
+          }
+          ++issued;
+          iw.next(p, w);
+        }
+        ++kc;
+      }
     }
-    for (unsigned k = kB; k < issuedB; ++k) {
-      if (!mbar_wait_warp(&barB[k % kRingB], (k / kRingB) & 1u)) break;
+    if (!alive) {
+      if (lane == 0) atomicOr(&p.hdr->error_flag, VPCE_FLAG_WAIT_TIMEOUT);
+      for (unsigned i = kc; i < issued; ++i)
+        if (!mbar_wait_warp(&full[i % kDSlots], (i / kDSlots) & 1u)) break;
     }
+    if (lane == 0) bulk_wait_all<0>();  // every dlogits store has landed
   }
-  if (lane == 0) bulk_wait_all<0>();
 
   // ---- batch loss: the last block sums the per-row losses in a fixed order
   __threadfence();
@@ -371,10 +394,8 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(const __grid
   if (!last) return;
   __threadfence();
   double v = 0.0;
-  // fixed 256-row blocks, each summed in row order by one thread, then a
-  // fixed tree over the threads
   const long long nb = (p.s + 255) / 256;
-  for (long long b = threadIdx.x; b < nb; b += kFusedWarps * 32) {
+  for (long long b = threadIdx.x; b < nb; b += kFThreads) {
     double bs = 0.0;
     const long long e = min(p.s, (b + 1) * 256);
     for (long long r = b * 256; r < e; ++r) bs += double(__ldcg(p.rowl + r));
@@ -386,26 +407,19 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) fused_kernel(const __grid
   __syncthreads();
   if (threadIdx.x == 0) {
     double tot = 0.0;
-    for (int i = 0; i < kFusedWarps; ++i) tot += sv[i];
-    const int c = p.hdr->n_valid;
+    for (int i = 0; i < kFThreads / 32; ++i) tot += sv[i];
+    const int cnt = p.hdr->n_valid;
     p.hdr->loss_sum = tot;
     p.hdr->ticket = 0u;
     *p.loss_out =
-        p.reduction == VPCE_SUM ? float(tot) : (c > 0 ? float(tot / double(c)) : __int_as_float(0x7fc00000));
+        p.reduction == VPCE_SUM ? float(tot) : (cnt > 0 ? float(tot / double(cnt)) : __int_as_float(0x7fc00000));
   }
-}
-
-template <int G>
-constexpr size_t fused_smem() {
-  return size_t(kFusedWarps) * (kRingA + kRingB) * kFChunk + size_t(kFusedWarps) * (kRingA + kRingB) * 8 +
-         size_t(kFusedWarps / G) * 2 * 8 + size_t(kFusedWarps / G) * 2 * G * sizeof(float2);
 }
 
 }  // namespace
 
-// Rows are handled by groups of kFusedGroup warps.
-constexpr int kFusedGroup = 8;
-
+// All shard pointers, row strides and widths 16-byte aligned (the bulk-copy
+// engine's requirement for the fused kernels).
 bool fused_supported(const ShardSet& sh, int t, int elem) {
   for (int i = 0; i < t; ++i) {
     const long long wb = (sh.start[i + 1] - sh.start[i]) * elem;
@@ -415,11 +429,11 @@ bool fused_supported(const ShardSet& sh, int t, int elem) {
 }
 
 cudaError_t set_fused_smem() {
-  cudaError_t e = cudaFuncSetAttribute(fused_kernel<float, kFusedGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(fused_smem<kFusedGroup>()));
+  cudaError_t e = cudaFuncSetAttribute(stream_fused_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(sizeof(FusedSmem)));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(fused_kernel<__nv_bfloat16, kFusedGroup>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(fused_smem<kFusedGroup>()));
+  return cudaFuncSetAttribute(stream_fused_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(sizeof(FusedSmem)));
 }
 
 void launch_prep(const long long* targets, long long s, long long V, long long ignore_index, Header* hdr,
@@ -427,11 +441,10 @@ void launch_prep(const long long* targets, long long s, long long V, long long i
   prep_kernel<<<1, kPrepThreads, 0, st>>>(targets, s, V, ignore_index, hdr, reduction, loss_out);
 }
 
-// The L2-reuse variant: any row length (rows stream through per-warp rings
-// twice, the second time from L2).  Expects launch_prep before it.
-void launch_l2fused(const ShardSet& sh, bool bf16, int t, long long s, long long V, const long long* targets,
-                    long long ignore_index, int reduction, float grad, float* lse, float* rowl, float* row_loss,
-                    float* loss_out, Header* hdr, int sms, cudaStream_t st) {
+// The streaming fused kernel (expects launch_prep before it): one CTA per SM.
+void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long long V, const long long* targets,
+                         long long ignore_index, int reduction, float grad, float* lse, float* rowl,
+                         float* row_loss, float* loss_out, Header* hdr, int sms, cudaStream_t st) {
   FusedParams p;
   p.sh = sh;
   p.t = t;
@@ -446,14 +459,11 @@ void launch_l2fused(const ShardSet& sh, bool bf16, int t, long long s, long long
   p.row_loss = row_loss;
   p.loss_out = loss_out;
   p.hdr = hdr;
-  constexpr int NG = kFusedWarps / kFusedGroup;
-  const long long want = (s + NG - 1) / NG;
-  const int grid = int(want < sms ? want : sms);
+  const int grid = int(s < sms ? s : sms);
   if (bf16)
-    fused_kernel<__nv_bfloat16, kFusedGroup>
-        <<<grid, kFusedWarps * 32, fused_smem<kFusedGroup>(), st>>>(p);
+    stream_fused_kernel<__nv_bfloat16><<<grid, kFThreads, sizeof(FusedSmem), st>>>(p);
   else
-    fused_kernel<float, kFusedGroup><<<grid, kFusedWarps * 32, fused_smem<kFusedGroup>(), st>>>(p);
+    stream_fused_kernel<float><<<grid, kFThreads, sizeof(FusedSmem), st>>>(p);
 }
 
 }  // namespace vpce

@@ -256,14 +256,14 @@ def vpce_forward_backward(shards, targets, vocab_start=None, *, ignore_index: in
 
 
 def vpce_fused_plan(dtype: int, vocab_start, s: int) -> dict:
-    """The launch vpce_forward_backward would use (kernel: 0 two-call path,
-    1 L2-reuse kernel, 2 resident kernel; cluster size; grid in CTAs)."""
+    """The launch vpce_forward_backward would use (kernel: 'split' two-call
+    path or 'stream' fused kernel; grid in CTAs)."""
     k, c, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     code = load_library().vpce_fused_plan(int(dtype), len(vocab_start) - 1, _i64_array(vocab_start), int(s),
                                           ctypes.byref(k), ctypes.byref(c), ctypes.byref(g))
     if code != VPCE_OK:
         raise VPCEError(code, "vpce_fused_plan")
-    return {"kernel": ["split", "l2_reuse", "resident"][k.value], "cluster": c.value, "grid": g.value}
+    return {"kernel": ["split", "stream"][k.value], "cluster": c.value, "grid": g.value}
 
 
 def vpce_read_error_flag(workspace, stream=None) -> int:
@@ -306,42 +306,3 @@ def vpce_forward_static(shards, targets, loss_out, vocab_start=None, *, ignore_i
         raise VPCEError(code, "vpce_forward_static")
     return loss_out
 
-
-# ----------------------------------------------------------------------------
-# host-side mirror of the resident kernel's cluster-size choice (diagnostics)
-# ----------------------------------------------------------------------------
-RESIDENT_CHUNK = 4096
-RESIDENT_WARPS = 16
-RESIDENT_SLOTS = 3
-RESIDENT_MAX_PER_WARP = 4
-RESIDENT_MAX_CLUSTER = 8
-
-
-def _resident_chunks(vocab_start, eb, C, c, w):
-    widths = [(vocab_start[i + 1] - vocab_start[i]) * eb for i in range(len(vocab_start) - 1)]
-    R = sum(widths)
-    plo = (R * c // C) & ~15
-    phi = R if c == C - 1 else (R * (c + 1) // C) & ~15
-    lo = plo + (((phi - plo) * w // RESIDENT_WARPS) & ~15)
-    hi = phi if w == RESIDENT_WARPS - 1 else plo + (((phi - plo) * (w + 1) // RESIDENT_WARPS) & ~15)
-    pos = n = 0
-    for W in widths:
-        a, b = max(lo, pos), min(hi, pos + W)
-        if a < b:
-            n += (b - a + RESIDENT_CHUNK - 1) // RESIDENT_CHUNK
-        pos += W
-    return n
-
-
-def resident_cluster_size(vocab_start, elem_bytes):
-    """Cluster size vpce_forward_backward uses to keep rows resident (0: the
-    rows are too long; the L2-reuse kernel runs instead).  Mirrors the library."""
-    def worst(C):
-        return max(_resident_chunks(vocab_start, elem_bytes, C, c, w)
-                   for c in range(C) for w in range(RESIDENT_WARPS))
-    for C in range(1, RESIDENT_MAX_CLUSTER + 1):
-        n = worst(C)
-        if n <= RESIDENT_MAX_PER_WARP and 3 * n <= RESIDENT_SLOTS:
-            return C
-    n8 = worst(RESIDENT_MAX_CLUSTER)
-    return RESIDENT_MAX_CLUSTER if (n8 <= RESIDENT_MAX_PER_WARP and 2 * n8 <= RESIDENT_SLOTS) else 0
