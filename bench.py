@@ -142,6 +142,27 @@ def _ncu_traffic(kernel: str, workload: str):
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
+def _bind_to_gpu_cpus(dev) -> None:
+    """Restrict this process to the host CPUs local to the GPU (from sysfs),
+    so that pinned host buffers land on the memory node next to it.  No-op
+    where the information is missing."""
+    import torch
+
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        bus = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bus}/local_cpulist") as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+    except (OSError, ValueError, AttributeError):
+        pass
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -241,6 +262,7 @@ def run_ours(args):
     # while the current step computes (dlogits stay on the device, where the
     # LM-head backward consumes them).
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    _bind_to_gpu_cpus(dev)  # pinned buffers on the GPU's own host memory node
     host_in = [p.cpu().pin_memory() for p in pristine]
     host_y = torch.from_numpy(meta.targets).pin_memory()
     host_loss = torch.empty(e2e_steps, dtype=torch.float32).pin_memory()
@@ -253,11 +275,15 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(copy_stream)
-    for k in range(e2e_steps):
+    warm = 2  # untimed: the first copies from freshly pinned pages are slow
+    for k in range(-warm, e2e_steps):
+        if k == 0:
+            stream.synchronize()
+            copy_stream.synchronize()
+            e0.record(copy_stream)
         b = k % 2
         with torch.cuda.stream(copy_stream):
-            if k >= 2:
+            if k >= 2 - warm:
                 copy_stream.wait_event(used[b])
             for d, h in zip(dbufs[b], host_in):
                 d.copy_(h, non_blocking=True)
@@ -271,7 +297,7 @@ def run_ours(args):
             vpce.vpce_forward(dbufs[b], ydevs[b], vs, ignore_index=w.ignore_index, loss_out=losses[b],
                               workspace=ws[b])
             vpce.vpce_backward(dbufs[b], ydevs[b], ws[b], vs, ignore_index=w.ignore_index)
-        host_loss[k].copy_(losses[b], non_blocking=True)
+        host_loss[max(k, 0)].copy_(losses[b], non_blocking=True)
         used[b].record(stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)

@@ -15,7 +15,11 @@
  * loss) overwrites the shards in place with
  *     dlogits_rk = g * (softmax(z_r)_k - [k == y_r]) / n_valid    (mean)
  *     dlogits_rk = g * (softmax(z_r)_k - [k == y_r])              (sum)
- * and with zeros on rows whose target is ignore_index.
+ *     dlogits_rk = g_r * (softmax(z_r)_k - [k == y_r])            (none)
+ * and with zeros on rows whose target is ignore_index.  'none' is the
+ * per-row mode of torch.nn.functional.cross_entropy, the routine the CMU notes
+ * check the sharded loss against: one loss per row, and one upstream gradient
+ * g_r per row (the *_rows entry points take them as a device vector).
  *
  * Conventions for every entry point
  * ---------------------------------
@@ -66,7 +70,7 @@ typedef enum {
 typedef enum { VPCE_FP32 = 0, VPCE_BF16 = 1 } vpce_dtype;
 
 /* Reduction of the per-row losses, as torch.nn.functional.cross_entropy. */
-typedef enum { VPCE_MEAN = 0, VPCE_SUM = 1 } vpce_reduction;
+typedef enum { VPCE_MEAN = 0, VPCE_SUM = 1, VPCE_NONE = 2 } vpce_reduction;
 
 #define VPCE_MAX_SHARDS 64
 
@@ -99,10 +103,13 @@ size_t vpce_workspace_bytes(int t, int64_t s);
  *   targets      device int64[s].
  *   ignore_index target value that drops a row (torch default -100).
  *   reduction    VPCE_MEAN: sum of valid-row losses / n_valid (NaN when
- *                n_valid = 0); VPCE_SUM: the plain sum.
- *   loss_out     device float, receives the reduced loss.
- *   row_loss_out device float[s] or NULL; receives CE_r for valid rows, 0 for
- *                ignored rows, NaN for out-of-range targets.
+ *                n_valid = 0); VPCE_SUM: the plain sum; VPCE_NONE: the
+ *                per-row losses are the result (row_loss_out required).
+ *   loss_out     device float, receives the reduced loss.  With VPCE_NONE
+ *                it may be NULL; when given it receives the plain sum.
+ *   row_loss_out device float[s] or NULL (required for VPCE_NONE when s > 0); receives
+ *                CE_r for valid rows, 0 for ignored rows, NaN for
+ *                out-of-range targets.
  *   workspace    device buffer of workspace_bytes >= vpce_workspace_bytes.
  * Results are bitwise reproducible for fixed inputs and t: the shards fold
  * in ascending index order and the batch sum runs in a fixed order (fp64).
@@ -119,7 +126,8 @@ vpce_status vpce_forward(const void* const* shards, vpce_dtype dtype, int t, int
  * logits and targets must equal the preceding vpce_forward's, the shards must
  * still hold that call's logits, and `workspace` must be that call's,
  * unmodified (it carries logsumexp, n_valid and the reduction).
- * grad_output is the upstream gradient g of the reduced loss (1.0 normally).
+ * grad_output is the upstream gradient g of the reduced loss (1.0 normally);
+ * after a VPCE_NONE forward it is applied to every row, as VPCE_SUM.
  * Padding columns (ld > w_i) are neither read nor written.
  */
 vpce_status vpce_backward(void* const* shards, vpce_dtype dtype, int t, int64_t s,
@@ -127,6 +135,21 @@ vpce_status vpce_backward(void* const* shards, vpce_dtype dtype, int t, int64_t 
                           const int64_t* targets, int64_t ignore_index,
                           float grad_output, const void* workspace, size_t workspace_bytes,
                           vpce_stream_t stream);
+
+/*
+ * Backward of the per-row losses (reduction 'none'): as vpce_backward, but
+ * with one upstream gradient per row, dlogits_rk = grad_rows[r] *
+ * (softmax(z_r)_k - [k == y_r]), whatever reduction the forward used.
+ *   grad_rows  device float[s] (4-byte aligned), read only; entry r is
+ *              d(outer loss)/d(CE_r).  Ignored rows get zeros whatever their
+ *              entry; any other entry is used as given (0 gives zeros, a
+ *              negative value flips the sign, NaN gives NaN).
+ */
+vpce_status vpce_backward_rows(void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                               const int64_t* vocab_start, int64_t ld,
+                               const int64_t* targets, int64_t ignore_index,
+                               const float* grad_rows, const void* workspace, size_t workspace_bytes,
+                               vpce_stream_t stream);
 
 /*
  * Forward and backward in one call: the loss (as vpce_forward) and the shards
@@ -149,6 +172,19 @@ vpce_status vpce_forward_backward(void* const* shards, vpce_dtype dtype, int t, 
                                   vpce_reduction reduction, float grad_output,
                                   float* loss_out, float* row_loss_out,
                                   void* workspace, size_t workspace_bytes, vpce_stream_t stream);
+
+/*
+ * vpce_forward_backward with one upstream gradient per row (known before the
+ * call, e.g. per-token loss weights): the loss as vpce_forward with
+ * `reduction`, and dlogits as vpce_backward_rows with grad_rows (device
+ * float[s], 4-byte aligned).  Same single pass over HBM and same fallback.
+ */
+vpce_status vpce_forward_backward_rows(void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                                       const int64_t* vocab_start, int64_t ld,
+                                       const int64_t* targets, int64_t ignore_index,
+                                       vpce_reduction reduction, const float* grad_rows,
+                                       float* loss_out, float* row_loss_out,
+                                       void* workspace, size_t workspace_bytes, vpce_stream_t stream);
 
 /*
  * How vpce_forward_backward would run the given problem on the current

@@ -168,13 +168,16 @@ def cross_entropy(z: np.ndarray, y: np.ndarray, ignore_index: int = -100,
 
 
 def dlogits(z: np.ndarray, y: np.ndarray, ignore_index: int = -100,
-            grad: float = 1.0, reduction: str = "mean",
+            grad=1.0, reduction: str = "mean",
             n_valid: int | None = None, lse: np.ndarray | None = None) -> np.ndarray:
     """Gradient of the reduced cross-entropy w.r.t. the logits, in fp64.
 
     For a valid row r: d_rk = g * (exp(z_rk - lse_r) - [k == y_r]) / n_valid
-    ('mean'; the division is dropped for 'sum').  Ignored rows are zero; rows
-    with an out-of-range target are NaN.  ``n_valid`` defaults to the count in
+    ('mean'; the division is dropped for 'sum').  For 'none' the loss is the
+    per-row vector and ``grad`` is its upstream gradient, one g_r per row (a
+    scalar is applied to every row): d_rk = g_r * (exp(z_rk - lse_r) -
+    [k == y_r]).  Ignored rows are zero whatever their g_r; rows with an
+    out-of-range target are NaN.  ``n_valid`` defaults to the count in
     ``y``; pass the batch count when ``z`` holds a sample of the rows.
     """
     z = np.asarray(z, dtype=np.float64)
@@ -185,9 +188,11 @@ def dlogits(z: np.ndarray, y: np.ndarray, ignore_index: int = -100,
         lse = cross_entropy(z, y, ignore_index)["lse"]
     nv = int(valid.sum()) if n_valid is None else int(n_valid)
     if reduction == "mean":
-        scale = grad / nv if nv > 0 else 0.0
+        scale = np.full(s, grad / nv if nv > 0 else 0.0)
     elif reduction == "sum":
-        scale = grad
+        scale = np.full(s, float(grad))
+    elif reduction == "none":
+        scale = np.broadcast_to(np.asarray(grad, dtype=np.float64), (s,))
     else:
         raise ValueError(f"unknown reduction {reduction!r}")
     d = np.zeros((s, V))
@@ -195,7 +200,7 @@ def dlogits(z: np.ndarray, y: np.ndarray, ignore_index: int = -100,
     if rows.size:
         p = np.exp(z[rows] - lse[rows][:, None])
         p[np.arange(rows.size), y[rows]] -= 1.0
-        d[rows] = scale * p
+        d[rows] = scale[rows][:, None] * p
     d[bad] = np.nan
     return d
 

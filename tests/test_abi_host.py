@@ -107,6 +107,53 @@ def test_backward_rejects_bad_arguments(lib, kw, code):
     assert _bwd(**kw) == code
 
 
+def _bwd_rows(**kw):
+    args = dict(shard_ptrs=[FAKE, FAKE + 4096], dtype=vpce.VPCE_FP32, t=2, s=4, vocab_start=[0, 8, 16], ld=0,
+                targets_ptr=ctypes.c_void_p(FAKE), ignore_index=-100, grad_rows_ptr=ctypes.c_void_p(FAKE),
+                ws_ptr=ctypes.c_void_p(FAKE), ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return vpce.backward_rows_raw(**args)
+
+
+def _fb_rows(**kw):
+    args = dict(shard_ptrs=[FAKE, FAKE + 4096], dtype=vpce.VPCE_BF16, t=2, s=4, vocab_start=[0, 8, 16], ld=0,
+                targets_ptr=ctypes.c_void_p(FAKE), ignore_index=-100, reduction=vpce.VPCE_NONE,
+                grad_rows_ptr=ctypes.c_void_p(FAKE), loss_ptr=None, row_loss_ptr=ctypes.c_void_p(FAKE),
+                ws_ptr=ctypes.c_void_p(FAKE), ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return vpce.forward_backward_rows_raw(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(grad_rows_ptr=None), 1),
+    (dict(grad_rows_ptr=ctypes.c_void_p(FAKE + 2)), 2),
+    (dict(dtype=5), 3),
+    (dict(ws_bytes=8), 4),
+])
+def test_backward_rows_rejects_bad_arguments(lib, kw, code):
+    assert _bwd_rows(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(grad_rows_ptr=None), 1),
+    (dict(grad_rows_ptr=ctypes.c_void_p(FAKE + 1)), 2),
+    (dict(row_loss_ptr=None), 1),                 # 'none' needs the per-row output
+    (dict(row_loss_ptr=ctypes.c_void_p(FAKE + 2)), 2),
+    (dict(reduction=3), 1),
+    (dict(reduction=vpce.VPCE_MEAN), 1),          # 'mean' needs loss_out
+])
+def test_forward_backward_rows_rejects_bad_arguments(lib, kw, code):
+    assert _fb_rows(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(reduction=vpce.VPCE_NONE), 1),          # row_loss_out missing
+    (dict(reduction=vpce.VPCE_NONE, loss_ptr=None, row_loss_ptr=ctypes.c_void_p(FAKE + 1)), 2),
+])
+def test_forward_none_needs_row_losses(lib, kw, code):
+    assert _fwd(**kw) == code
+
+
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     import torch
 
@@ -115,3 +162,7 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     # all arguments valid: the first CUDA call (device query) fails, nothing runs
     assert _fwd() == 5
     assert _bwd() == 5
+    assert _bwd_rows() == 5
+    assert _fb_rows() == 5
+    # 'none' takes loss_out as optional
+    assert _fwd(reduction=vpce.VPCE_NONE, loss_ptr=None, row_loss_ptr=ctypes.c_void_p(FAKE)) == 5

@@ -110,7 +110,13 @@ def test_matches_torch_cross_entropy_fp64(s, V, ignore, reduction):
         g = 0.75
         (ref * g).backward()
         d = O.dlogits(z, y, grad=g, reduction=reduction)
-        np.testing.assert_allclose(d, zt.grad.numpy(), rtol=1e-12, atol=1e-15)
+    else:
+        # one upstream gradient per row, of both signs, some zero
+        g = RNG.normal(0.0, 1.0, size=s)
+        g[::5] = 0.0
+        ref.backward(torch.tensor(g))
+        d = O.dlogits(z, y, grad=g, reduction="none")
+    np.testing.assert_allclose(d, zt.grad.numpy(), rtol=1e-12, atol=1e-15)
 
 
 def test_matches_torch_with_large_logits():
@@ -135,6 +141,27 @@ def test_gradient_by_central_differences():
             zm[r, k] -= h
             fd[r, k] = (O.cross_entropy(zp, y)["loss"] - O.cross_entropy(zm, y)["loss"]) / (2 * h)
     np.testing.assert_allclose(d, fd, rtol=0, atol=1e-8)
+
+
+def test_per_row_gradient_by_central_differences():
+    """'none': d/dz of sum_r g_r * CE_r, differentiated numerically."""
+    s, V = 4, 5
+    z, y = _rand_case(s, V, scale=1.5, ignore=(2,))
+    g = np.array([0.5, -1.25, 7.0, 2.0])
+    d = O.dlogits(z, y, grad=g, reduction="none")
+    h = 1e-6
+    fd = np.zeros_like(z)
+    for r in range(s):
+        for k in range(V):
+            zp = z.copy()
+            zm = z.copy()
+            zp[r, k] += h
+            zm[r, k] -= h
+            lp = O.cross_entropy(zp, y, reduction="none")["loss"]
+            lm = O.cross_entropy(zm, y, reduction="none")["loss"]
+            fd[r, k] = float(np.dot(g, lp - lm)) / (2 * h)
+    np.testing.assert_allclose(d, fd, rtol=0, atol=5e-8)
+    assert np.all(d[2] == 0.0)
 
 
 def test_gradient_rows_sum_to_zero_and_ignored_rows_zero():

@@ -15,8 +15,8 @@ bool fused_supported(const ShardSet& sh, int t, int elem);
 void launch_prep(const long long* targets, long long s, long long V, long long ignore_index, Header* hdr,
                  int reduction, float* loss_out, cudaStream_t st);
 void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long long V, const long long* targets,
-                         long long ignore_index, int reduction, float grad, float* lse, float* rowl,
-                         float* row_loss, float* loss_out, Header* hdr, int sms, cudaStream_t st);
+                         long long ignore_index, int reduction, float grad, const float* grad_rows, float* lse,
+                         float* rowl, float* row_loss, float* loss_out, Header* hdr, int sms, cudaStream_t st);
 
 }  // namespace vpce
 
@@ -123,6 +123,67 @@ vpce_status launch_status() {
   return e == cudaSuccess ? VPCE_OK : VPCE_ERR_CUDA;
 }
 
+// The reduction and the two loss outputs: VPCE_NONE makes the per-row losses
+// the result (row_loss_out required unless s = 0, loss_out optional).
+vpce_status check_outputs(vpce_reduction reduction, int64_t s, const float* loss_out, const float* row_loss_out) {
+  if (reduction != VPCE_MEAN && reduction != VPCE_SUM && reduction != VPCE_NONE) return VPCE_ERR_INVALID_ARG;
+  if (reduction == VPCE_NONE ? (row_loss_out == nullptr && s > 0) : loss_out == nullptr)
+    return VPCE_ERR_INVALID_ARG;
+  if ((loss_out != nullptr && !aligned(loss_out, 4)) || (row_loss_out != nullptr && !aligned(row_loss_out, 4)))
+    return VPCE_ERR_ALIGNMENT;
+  return VPCE_OK;
+}
+
+// Per-row upstream gradients: null means "use the scalar"; otherwise a
+// 4-byte aligned device vector with one entry per row.
+vpce_status check_grad_rows(const float* grad_rows, int64_t s, bool required) {
+  if (grad_rows == nullptr) return (required && s > 0) ? VPCE_ERR_INVALID_ARG : VPCE_OK;
+  return aligned(grad_rows, 4) ? VPCE_OK : VPCE_ERR_ALIGNMENT;
+}
+
+vpce_status backward_impl(void* const* shards, vpce_dtype dtype, int t, int64_t s, const int64_t* vocab_start,
+                          int64_t ld, const int64_t* targets, int64_t ignore_index, float grad_output,
+                          const float* grad_rows, const void* workspace, size_t workspace_bytes,
+                          vpce_stream_t stream) {
+  ShardSet sh;
+  long long V = 0;
+  vpce_status st = check_logits(reinterpret_cast<const void* const*>(shards), dtype, t, s, vocab_start, ld,
+                                targets, &sh, &V);
+  if (st != VPCE_OK) return st;
+  if (!std::isfinite(grad_output)) return VPCE_ERR_INVALID_ARG;
+  st = check_workspace(workspace, workspace_bytes, t, s);
+  if (st != VPCE_OK) return st;
+  int sms = 0;
+  st = device_setup(&sms);
+  if (st != VPCE_OK) return st;
+  if (s == 0) return VPCE_OK;
+
+  const WsLayout L(t, s);
+  const unsigned char* ws = static_cast<const unsigned char*>(workspace);
+  BackwardParams p;
+  p.sh = sh;
+  p.s = s;
+  p.units = (long long)t * s;
+  p.targets = reinterpret_cast<const long long*>(targets);
+  p.ignore_index = ignore_index;
+  p.lse = reinterpret_cast<const float*>(ws + L.lse);
+  p.hdr = reinterpret_cast<const Header*>(ws);
+  p.hdr_flags = reinterpret_cast<Header*>(const_cast<unsigned char*>(ws));
+  p.grad = grad_output;
+  p.grad_rows = grad_rows;
+  const int grid = stream_grid(sms, p.units);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == VPCE_BF16) launch_backward<__nv_bfloat16>(p, grid, cs);
+  else launch_backward<float>(p, grid, cs);
+  return launch_status();
+}
+
+vpce_status forward_backward_impl(void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                                  const int64_t* vocab_start, int64_t ld, const int64_t* targets,
+                                  int64_t ignore_index, vpce_reduction reduction, float grad_output,
+                                  const float* grad_rows, float* loss_out, float* row_loss_out, void* workspace,
+                                  size_t workspace_bytes, vpce_stream_t stream);
+
 }  // namespace
 
 extern "C" {
@@ -140,9 +201,7 @@ vpce_status vpce_forward(const void* const* shards, vpce_dtype dtype, int t, int
   long long V = 0;
   vpce_status st = check_logits(shards, dtype, t, s, vocab_start, ld, targets, &sh, &V);
   if (st != VPCE_OK) return st;
-  if (reduction != VPCE_MEAN && reduction != VPCE_SUM) return VPCE_ERR_INVALID_ARG;
-  if (loss_out == nullptr) return VPCE_ERR_INVALID_ARG;
-  if (!aligned(loss_out, 4) || (row_loss_out != nullptr && !aligned(row_loss_out, 4))) return VPCE_ERR_ALIGNMENT;
+  if ((st = check_outputs(reduction, s, loss_out, row_loss_out)) != VPCE_OK) return st;
   st = check_workspace(workspace, workspace_bytes, t, s);
   if (st != VPCE_OK) return st;
   int sms = 0;
@@ -192,36 +251,17 @@ vpce_status vpce_forward(const void* const* shards, vpce_dtype dtype, int t, int
 vpce_status vpce_backward(void* const* shards, vpce_dtype dtype, int t, int64_t s, const int64_t* vocab_start,
                           int64_t ld, const int64_t* targets, int64_t ignore_index, float grad_output,
                           const void* workspace, size_t workspace_bytes, vpce_stream_t stream) {
-  ShardSet sh;
-  long long V = 0;
-  vpce_status st = check_logits(reinterpret_cast<const void* const*>(shards), dtype, t, s, vocab_start, ld,
-                                targets, &sh, &V);
-  if (st != VPCE_OK) return st;
-  if (!std::isfinite(grad_output)) return VPCE_ERR_INVALID_ARG;
-  st = check_workspace(workspace, workspace_bytes, t, s);
-  if (st != VPCE_OK) return st;
-  int sms = 0;
-  st = device_setup(&sms);
-  if (st != VPCE_OK) return st;
-  if (s == 0) return VPCE_OK;
+  return backward_impl(shards, dtype, t, s, vocab_start, ld, targets, ignore_index, grad_output, nullptr, workspace,
+                       workspace_bytes, stream);
+}
 
-  const WsLayout L(t, s);
-  const unsigned char* ws = static_cast<const unsigned char*>(workspace);
-  BackwardParams p;
-  p.sh = sh;
-  p.s = s;
-  p.units = (long long)t * s;
-  p.targets = reinterpret_cast<const long long*>(targets);
-  p.ignore_index = ignore_index;
-  p.lse = reinterpret_cast<const float*>(ws + L.lse);
-  p.hdr = reinterpret_cast<const Header*>(ws);
-  p.hdr_flags = reinterpret_cast<Header*>(const_cast<unsigned char*>(ws));
-  p.grad = grad_output;
-  const int grid = stream_grid(sms, p.units);
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (dtype == VPCE_BF16) launch_backward<__nv_bfloat16>(p, grid, cs);
-  else launch_backward<float>(p, grid, cs);
-  return launch_status();
+vpce_status vpce_backward_rows(void* const* shards, vpce_dtype dtype, int t, int64_t s, const int64_t* vocab_start,
+                               int64_t ld, const int64_t* targets, int64_t ignore_index, const float* grad_rows,
+                               const void* workspace, size_t workspace_bytes, vpce_stream_t stream) {
+  const vpce_status st = check_grad_rows(grad_rows, s, true);
+  if (st != VPCE_OK) return st;
+  return backward_impl(shards, dtype, t, s, vocab_start, ld, targets, ignore_index, 1.f, grad_rows, workspace,
+                       workspace_bytes, stream);
 }
 
 vpce_status vpce_forward_backward(void* const* shards, vpce_dtype dtype, int t, int64_t s,
@@ -229,15 +269,37 @@ vpce_status vpce_forward_backward(void* const* shards, vpce_dtype dtype, int t, 
                                   int64_t ignore_index, vpce_reduction reduction, float grad_output,
                                   float* loss_out, float* row_loss_out, void* workspace, size_t workspace_bytes,
                                   vpce_stream_t stream) {
+  return forward_backward_impl(shards, dtype, t, s, vocab_start, ld, targets, ignore_index, reduction, grad_output,
+                               nullptr, loss_out, row_loss_out, workspace, workspace_bytes, stream);
+}
+
+vpce_status vpce_forward_backward_rows(void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                                       const int64_t* vocab_start, int64_t ld, const int64_t* targets,
+                                       int64_t ignore_index, vpce_reduction reduction, const float* grad_rows,
+                                       float* loss_out, float* row_loss_out, void* workspace,
+                                       size_t workspace_bytes, vpce_stream_t stream) {
+  const vpce_status st = check_grad_rows(grad_rows, s, true);
+  if (st != VPCE_OK) return st;
+  return forward_backward_impl(shards, dtype, t, s, vocab_start, ld, targets, ignore_index, reduction, 1.f,
+                               grad_rows, loss_out, row_loss_out, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+vpce_status forward_backward_impl(void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                                  const int64_t* vocab_start, int64_t ld, const int64_t* targets,
+                                  int64_t ignore_index, vpce_reduction reduction, float grad_output,
+                                  const float* grad_rows, float* loss_out, float* row_loss_out, void* workspace,
+                                  size_t workspace_bytes, vpce_stream_t stream) {
   ShardSet sh;
   long long V = 0;
   vpce_status st = check_logits(reinterpret_cast<const void* const*>(shards), dtype, t, s, vocab_start, ld,
                                 targets, &sh, &V);
   if (st != VPCE_OK) return st;
-  if (reduction != VPCE_MEAN && reduction != VPCE_SUM) return VPCE_ERR_INVALID_ARG;
+  if ((st = check_outputs(reduction, s, loss_out, row_loss_out)) != VPCE_OK) return st;
   if (!std::isfinite(grad_output)) return VPCE_ERR_INVALID_ARG;
-  if (loss_out == nullptr) return VPCE_ERR_INVALID_ARG;
-  if (!aligned(loss_out, 4) || (row_loss_out != nullptr && !aligned(row_loss_out, 4))) return VPCE_ERR_ALIGNMENT;
   st = check_workspace(workspace, workspace_bytes, t, s);
   if (st != VPCE_OK) return st;
   int sms = 0;
@@ -249,8 +311,8 @@ vpce_status vpce_forward_backward(void* const* shards, vpce_dtype dtype, int t, 
     st = vpce_forward(reinterpret_cast<const void* const*>(shards), dtype, t, s, vocab_start, ld, targets,
                       ignore_index, reduction, loss_out, row_loss_out, workspace, workspace_bytes, stream);
     if (st != VPCE_OK) return st;
-    return vpce_backward(shards, dtype, t, s, vocab_start, ld, targets, ignore_index, grad_output, workspace,
-                         workspace_bytes, stream);
+    return backward_impl(shards, dtype, t, s, vocab_start, ld, targets, ignore_index, grad_output, grad_rows,
+                         workspace, workspace_bytes, stream);
   }
   const WsLayout L(t, s);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
@@ -261,10 +323,14 @@ vpce_status vpce_forward_backward(void* const* shards, vpce_dtype dtype, int t, 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   launch_prep(tg, s, V, ignore_index, hdr, int(reduction), loss_out, cs);
   if ((st = launch_status()) != VPCE_OK || s == 0) return st;
-  launch_stream_fused(sh, dtype == VPCE_BF16, t, s, V, tg, ignore_index, int(reduction), grad_output, lse, rowl,
-                      row_loss_out, loss_out, hdr, sms, cs);
+  launch_stream_fused(sh, dtype == VPCE_BF16, t, s, V, tg, ignore_index, int(reduction), grad_output, grad_rows,
+                      lse, rowl, row_loss_out, loss_out, hdr, sms, cs);
   return launch_status();
 }
+
+}  // namespace
+
+extern "C" {
 
 vpce_status vpce_fused_plan(vpce_dtype dtype, int t, const int64_t* vocab_start, int64_t s, int* kernel,
                            int* cluster, int* grid) {

@@ -2,7 +2,8 @@
 //
 // The pages define the forward only; the gradient of the reduced loss is the
 // standard one, dlogits_rk = g * (exp(z_rk - lse_r) - [k == y_r]) / n_valid
-// for 'mean' (no division for 'sum'), zero on ignored rows.  Each (shard, row)
+// for 'mean' (no division for 'sum'; 'none' scales row r by its own g_r),
+// zero on ignored rows.  Each (shard, row)
 // segment is streamed through shared memory once: the bulk-copy engine loads a
 // chunk, the warp turns it into dlogits in place, and the bulk-copy engine
 // writes it back over the logits -- one read and one write of the shards.
@@ -54,8 +55,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) backward_kernel(const __grid_c
   const long long u1 = p.units * (gw + 1) / nw;
 
   const int n_valid = p.hdr->n_valid;
-  const float scale =
-      p.hdr->reduction == VPCE_SUM ? p.grad : (n_valid > 0 ? p.grad / float(n_valid) : 0.f);
+  const float scale_all =
+      p.hdr->reduction != VPCE_MEAN ? p.grad : (n_valid > 0 ? p.grad / float(n_valid) : 0.f);
 
   if (lane == 0) {
 #pragma unroll
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) backward_kernel(const __grid_c
     }
     const long long lo = p.sh.start[g.shard], hi = p.sh.start[g.shard + 1];
     const long long tcol = (y >= lo && y < hi) ? (y - lo) : -1;  // target column inside this shard
+    const float scale = p.grad_rows != nullptr ? __ldg(p.grad_rows + g.row) : scale_all;
     const float c = -__ldg(p.lse + g.row) * kLog2e;
     const float cb = folded_offset(c, scale);
 

@@ -239,9 +239,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     p.hdr->reduction = p.reduction;
     p.hdr->ticket = 0u;
     float loss;
-    if (p.reduction == VPCE_SUM) loss = float(v);
+    if (p.reduction != VPCE_MEAN) loss = float(v);  // sum ('none' reports the sum when asked)
     else loss = c > 0 ? float(v / double(c)) : __int_as_float(0x7fc00000);
-    *p.loss_out = loss;
+    if (p.loss_out != nullptr) *p.loss_out = loss;
   }
 }
 

@@ -39,6 +39,15 @@ constexpr int kFThreads = (kSW + kDW) * 32;
 constexpr int kFChunk = 4096;  // bytes per pipeline chunk
 constexpr int kSSlots = 4;     // ring slots per stats warp (HBM latency)
 constexpr int kDSlots = 3;     // ring slots per grad warp (L2 latency)
+// L2 bytes per CTA the two passes may keep live between them: one row is
+// the least (a row's statistics precede its gradient); rows shorter than
+// this let the stats warps run further ahead.  Measured on GB300: 320 KB per
+// SM (49 MB over 152 SMs) is where the re-reads still hit L2; more slack
+// turns them into HBM reads.
+constexpr unsigned kLiveBytesPerCta = 320u * 1024u;
+// stats warp w and grad warp w walk the same chunks: the credit between them
+// counts those chunks
+static_assert(kSW == kDW, "stats and grad warps pair up");
 constexpr int kFVPL = kFChunk / 512;
 
 struct FusedParams {
@@ -50,11 +59,23 @@ struct FusedParams {
   long long ignore_index;
   int reduction;
   float grad;
+  unsigned credit_slack;   // chunks a stats warp may run past one row ahead of its grad partner
+  const float* grad_rows;  // [s] per-row upstream gradient, or null (use grad)
   float* lse;       // [s]
   float* rowl;      // [s]: per-row loss (0 ignored, NaN bad target)
   float* row_loss;  // optional user copy of rowl
-  float* loss_out;
+  float* loss_out;  // may be null ('none')
   Header* hdr;
+};
+
+// The shard geometry, copied from the kernel parameters into shared memory
+// once per CTA: the chunk walk looks a segment up several times per chunk,
+// and a run-time index into the parameter block costs a dependent
+// constant-cache load each time.
+struct Geo {
+  const unsigned char* ptr[VPCE_MAX_SHARDS];
+  long long ld[VPCE_MAX_SHARDS];
+  int start[VPCE_MAX_SHARDS + 1];  // V < 2^31
 };
 
 struct FusedSmem {
@@ -66,7 +87,13 @@ struct FusedSmem {
   uint64_t rowfree[2];  // grad warps -> stats warps: the grad warps have begun that row
   float2 part[2][kSW];
   float tz[2];
+  unsigned sdone[kSW];  // chunks stats warp w has received (its grad partner may re-read them)
+  unsigned gdone[kDW];  // chunks grad warp w has received (credit back to its stats partner)
+  Geo geo;
 };
+// Within the 227 KB a CTA may use, with room for a 1 KB granule of static
+// shared memory should the compiler reserve one.
+static_assert(sizeof(FusedSmem) + 1024 <= 232448, "fused kernel shared memory");
 
 // Prologue: clear the header, count the valid rows, flag bad targets.
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const long long* targets, long long s,
@@ -102,7 +129,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const long long* tar
     hdr->ticket = 0u;
     hdr->reduction = reduction;
     hdr->loss_sum = 0.0;
-    if (s == 0) *loss_out = reduction == VPCE_SUM ? 0.f : __int_as_float(0x7fc00000);
+    if (s == 0 && loss_out != nullptr) *loss_out = reduction != VPCE_MEAN ? 0.f : __int_as_float(0x7fc00000);
   }
 }
 
@@ -114,49 +141,112 @@ __device__ __forceinline__ void sub_range(unsigned seg_bytes, int w, unsigned& l
   hi = w == NW - 1 ? seg_bytes : unsigned((unsigned long long)seg_bytes * unsigned(w + 1) / NW) & ~15u;
 }
 
-// Walks the chunks of one row that belong to warp w of NW: segment by
-// segment, each sub-range cut into near-equal 16-byte aligned chunks of at
-// most kFChunk.
+// Walks the chunks of row r that belong to warp w of NW: segment by segment,
+// each sub-range cut into kFChunk-byte chunks and a shorter last one.  No
+// division on the way: the walk runs once per chunk on the critical path of
+// both roles, where a 64-bit division by a variable chunk count cost as much
+// as the chunk's arithmetic.
 template <int EB, int NW>
 struct RowWalk {
   int seg;
-  unsigned k, n, lo, hi;
+  unsigned pos, hi;     // the next chunk starts at pos; the warp's share ends at hi
+  unsigned char* base;  // the row's first byte in shard seg
   bool ok;
 
-  __device__ __forceinline__ bool seek(const FusedParams& p, int w, int from) {
-    for (seg = from; seg < p.t; ++seg) {
-      sub_range<NW>(unsigned(p.sh.start[seg + 1] - p.sh.start[seg]) * EB, w, lo, hi);
-      n = (hi - lo + kFChunk - 1) / kFChunk;
-      if (n > 0) {
-        k = 0;
+  __device__ __forceinline__ bool seek(const Geo& g, int t, long long r, int w, int from) {
+    for (seg = from; seg < t; ++seg) {
+      unsigned lo;
+      sub_range<NW>(unsigned(g.start[seg + 1] - g.start[seg]) * EB, w, lo, hi);
+      if (hi > lo) {
+        pos = lo;
+        base = const_cast<unsigned char*>(g.ptr[seg]) + r * g.ld[seg];
         return ok = true;
       }
     }
     return ok = false;
   }
-  __device__ __forceinline__ void next(const FusedParams& p, int w) {
-    if (++k < n) return;
-    seek(p, w, seg + 1);
+  __device__ __forceinline__ void next(const Geo& g, int t, long long r, int w) {
+    pos += kFChunk;
+    if (pos >= hi) seek(g, t, r, w, seg + 1);
   }
   __device__ __forceinline__ void bounds(unsigned& a, unsigned& b) const {
-    const unsigned len = hi - lo;
-    a = lo + (unsigned((unsigned long long)len * k / n) & ~15u);
-    b = k + 1 == n ? hi : lo + (unsigned((unsigned long long)len * (k + 1) / n) & ~15u);
+    a = pos;
+    b = min(pos + unsigned(kFChunk), hi);
   }
-  __device__ __forceinline__ unsigned char* addr(const FusedParams& p, long long r, unsigned a) const {
-    return const_cast<unsigned char*>(p.sh.ptr[seg]) + r * p.sh.ld_bytes[seg] + a;
+  __device__ __forceinline__ unsigned char* addr(unsigned a) const { return base + a; }
+};
+
+// Chunks of one row that warp w of NW owns (the same for every row).
+template <int EB, int NW>
+__device__ __forceinline__ unsigned row_chunks(const Geo& g, int t, int w) {
+  unsigned c = 0;
+  for (int i = 0; i < t; ++i) {
+    unsigned lo, hi;
+    sub_range<NW>(unsigned(g.start[i + 1] - g.start[i]) * EB, w, lo, hi);
+    c += (hi - lo + kFChunk - 1) / kFChunk;
+  }
+  return c;
+}
+
+// The load side of a warp's walk: the chunks of its share of every row the
+// CTA owns (rows r0, r0 + step, ...), ignored rows skipped, in the order the
+// arithmetic consumes them.
+template <int EB, int NW>
+struct RowCursor {
+  long long r, step;
+  RowWalk<EB, NW> wk;
+  bool ok;
+
+  __device__ __forceinline__ void start(const FusedParams& p, const Geo& g, int t, int w, long long r0,
+                                        long long st) {
+    step = st;
+    r = r0 - st;
+    next_row(p, g, t, w);
+  }
+  __device__ __forceinline__ void next_row(const FusedParams& p, const Geo& g, int t, int w) {
+    for (;;) {
+      r += step;
+      if (r >= p.s) {
+        ok = false;
+        return;
+      }
+      if (__ldg(p.targets + r) == p.ignore_index) continue;
+      if (wk.seek(g, t, r, w, 0)) {
+        ok = true;
+        return;
+      }
+    }
+  }
+  __device__ __forceinline__ void advance(const FusedParams& p, const Geo& g, int t, int w) {
+    wk.next(g, t, r, w);
+    if (!wk.ok) next_row(p, g, t, w);
   }
 };
 
+__device__ __forceinline__ unsigned ld_volatile(const unsigned* a) { return *const_cast<const volatile unsigned*>(a); }
+__device__ __forceinline__ void st_volatile(unsigned* a, unsigned v) { *const_cast<volatile unsigned*>(a) = v; }
+
+// Bounded, warp-uniform wait until the shared counter *c (raised by another
+// warp of the CTA) exceeds `floor`.
+__device__ __forceinline__ bool wait_counter_above(const unsigned* c, unsigned floor) {
+  if (__all_sync(kFull, ld_volatile(c) > floor)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    __nanosleep(64);
+    if (__all_sync(kFull, ld_volatile(c) > floor)) return true;
+    if (__any_sync(kFull, clock64() - t0 > kWaitLimitCycles)) return false;
+  }
+}
+
 // segment and byte offset of target y (segment -1 when out of range)
 template <int EB>
-__device__ __forceinline__ void target_of(const FusedParams& p, long long y, int& ty, unsigned& toff) {
+__device__ __forceinline__ void target_of(const Geo& g, int t, long long y, int& ty, unsigned& toff) {
   ty = -1;
   toff = 0;
-  if (y >= 0 && y < p.V) {
+  if (y >= 0 && y < g.start[t]) {
     ty = 0;
-    while (p.sh.start[ty + 1] <= y) ++ty;
-    toff = unsigned(y - p.sh.start[ty]) * EB;
+    while (g.start[ty + 1] <= y) ++ty;
+    toff = unsigned(y - g.start[ty]) * EB;
   }
 }
 
@@ -165,8 +255,6 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
   constexpr int EB = Elem<T>::kBytes;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   FusedSmem& sm = *reinterpret_cast<FusedSmem*>(smem_raw);
-  __shared__ bool last;
-  __shared__ double sv[kFThreads / 32];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const bool stats = warp < kSW;
@@ -178,6 +266,8 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     } else {
       for (int k = 0; k < kDSlots; ++k) mbar_init(&sm.dfull[w][k], 1);
     }
+    if (stats) sm.sdone[w] = 0u;
+    else sm.gdone[w] = 0u;
     if (warp == 0) {
       mbar_init(&sm.rowdone[0], kSW);
       mbar_init(&sm.rowdone[1], kSW);
@@ -186,49 +276,68 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     }
     fence_mbar_init();
   }
+  for (int i = threadIdx.x; i <= p.t; i += kFThreads) {
+    sm.geo.start[i] = int(p.sh.start[i]);
+    if (i < p.t) {
+      sm.geo.ptr[i] = p.sh.ptr[i];
+      sm.geo.ld[i] = p.sh.ld_bytes[i];
+    }
+  }
   __syncthreads();
+  const Geo& geo = sm.geo;
+  const int nt = p.t;
 
   const long long r_step = gridDim.x;
   const long long r0 = blockIdx.x;
   bool alive = true;
 
   if (stats) {
-    // ---------------- stats warps: pass 1 from HBM over the CTA's rows.
-    // A row's loads start only once the grad warps have begun the previous
-    // row, so at most two rows per CTA are live in L2 (the one the grad warps
-    // re-read and the one streaming in).
+    // ---------------- stats warps: pass 1 from HBM.  The loads run ahead of
+    // the arithmetic across row boundaries, limited by the ring and by the
+    // credit from the grad partner: chunk i is loaded only once grad warp w
+    // has received chunk i - budget, which keeps about one row per CTA (plus
+    // the slack) live in L2 between the two passes.
     unsigned char(*ring)[kFChunk] = sm.sring[w];
     uint64_t* full = sm.sfull[w];
     const uint64_t pol = policy_evict_last();  // the grad warps re-read these bytes
-    unsigned issued = 0;
-    unsigned kc = 0, n = 0;
+    const unsigned budget = row_chunks<EB, kSW>(geo, nt, w) + p.credit_slack;
+    RowCursor<EB, kSW> prod;
+    prod.start(p, geo, nt, w, r0, r_step);
+    unsigned issued = 0, kc = 0, n = 0;
+    auto top_up = [&]() {
+      const unsigned credit = __shfl_sync(kFull, ld_volatile(&sm.gdone[w]), 0) + budget;
+      while (prod.ok && issued < kc + kSSlots && issued < credit) {
+        unsigned a, b;
+        prod.wk.bounds(a, b);
+        const int slot = int(issued % kSSlots);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[slot], b - a);
+          bulk_load(ring[slot], prod.wk.addr(a), b - a, &full[slot], pol);
+        }
+        ++issued;
+        prod.advance(p, geo, nt, w);
+      }
+    };
 #pragma unroll 1
     for (long long r = r0; r < p.s && alive; r += r_step) {
       const long long y = __ldg(p.targets + r);
       if (y == p.ignore_index) continue;
-      if (n > 0 && !mbar_wait_warp(&sm.rowfree[(n - 1) & 1u], ((n - 1) >> 1) & 1u)) {
-        alive = false;
-        break;
-      }
       int ty;
       unsigned toff;
-      target_of<EB>(p, y, ty, toff);
-      RowWalk<EB, kSW> iw, cw;
-      iw.seek(p, w, 0);
-      for (int k = 0; k < kSSlots && iw.ok; ++k, iw.next(p, w)) {
-        unsigned a, b;
-        iw.bounds(a, b);
-        const int slot = int(issued % kSSlots);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[slot], b - a);
-          bulk_load(ring[slot], iw.addr(p, r, a), b - a, &full[slot], pol);
-        }
-        ++issued;
-      }
+      target_of<EB>(geo, nt, y, ty, toff);
       float m = -INFINITY, se = 0.f, zt = 0.f;
       bool has_t = false;
+      RowWalk<EB, kSW> cw;
 #pragma unroll 1
-      for (cw.seek(p, w, 0); cw.ok; cw.next(p, w)) {
+      for (cw.seek(geo, nt, r, w, 0); cw.ok; cw.next(geo, nt, r, w)) {
+        top_up();
+        if (issued == kc && prod.ok) {  // out of credit for the chunk needed now
+          if (!wait_counter_above(&sm.gdone[w], kc - budget)) {
+            alive = false;
+            break;
+          }
+          top_up();
+        }
         unsigned a, b;
         cw.bounds(a, b);
         const int slot = int(kc % kSSlots);
@@ -236,27 +345,24 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
           alive = false;
           break;
         }
+        if (lane == 0) st_volatile(&sm.sdone[w], kc + 1);  // these bytes are in L2 now
         stats_chunk<kFVPL>(ring[slot], b - a, lane, m, se, T());
         if (cw.seg == ty && toff >= a && toff < b) {
           has_t = true;
           zt = Elem<T>::load(ring[slot] + (toff - a));
         }
         __syncwarp();
-        if (iw.ok) {  // refill this slot with the row's next chunk
-          unsigned ia, ib;
-          iw.bounds(ia, ib);
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&full[slot], ib - ia);
-            bulk_load(ring[slot], iw.addr(p, r, ia), ib - ia, &full[slot], pol);
-          }
-          ++issued;
-          iw.next(p, w);
-        }
         ++kc;
       }
       if (!alive) break;
       warp_merge_ms(m, se);
+      // the mailbox slot of this row last held row n - 2: the grad warps
+      // must have taken it (with the credit above this never waits)
       const int buf = int(n & 1u);
+      if (n >= 2 && !mbar_wait_warp(&sm.rowfree[buf], ((n - 2) >> 1) & 1u)) {
+        alive = false;
+        break;
+      }
       if (lane == 0) {
         sm.part[buf][w] = make_float2(m, se);
         if (has_t) sm.tz[buf] = zt;
@@ -270,22 +376,44 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
         if (!mbar_wait_warp(&full[i % kSSlots], (i / kSSlots) & 1u)) break;
     }
   } else {
-    // ---------------- grad warps: logsumexp from the mailbox, pass 2 from L2
+    // ---------------- grad warps: logsumexp from the mailbox, pass 2 from L2.
+    // A chunk is loaded as soon as the stats partner has received it (so it
+    // is in L2), before the row's logsumexp is known; the arithmetic waits
+    // for the row's partials.  Loads stay kDSlots - 1 ahead, and a slot is
+    // refilled once the store that last used it has read it.
     unsigned char(*ring)[kFChunk] = sm.dring[w];
     uint64_t* full = sm.dfull[w];
     const uint64_t pol = policy_evict_first();
     const int n_valid = p.hdr->n_valid;
-    const float scale = p.reduction == VPCE_SUM ? p.grad : (n_valid > 0 ? p.grad / float(n_valid) : 0.f);
+    const float scale_all = p.reduction != VPCE_MEAN ? p.grad : (n_valid > 0 ? p.grad / float(n_valid) : 0.f);
+    RowCursor<EB, kDW> prod;
+    prod.start(p, geo, nt, w, r0, r_step);
     unsigned kc = 0, issued = 0, n = 0;
+    auto issue = [&]() {
+      unsigned a, b;
+      prod.wk.bounds(a, b);
+      const int slot = int(issued % kDSlots);
+      if (lane == 0) {
+        bulk_wait_read<1>();  // the store of chunk issued - kDSlots has left this slot
+        mbar_arrive_expect_tx(&full[slot], b - a);
+        bulk_load(ring[slot], prod.wk.addr(a), b - a, &full[slot], pol);
+      }
+      ++issued;
+      prod.advance(p, geo, nt, w);
+    };
+    auto top_up = [&]() {
+      const unsigned avail = __shfl_sync(kFull, ld_volatile(&sm.sdone[w]), 0);
+      while (prod.ok && issued <= kc + kDSlots - 2 && issued < avail) issue();
+    };
 #pragma unroll 1
     for (long long r = r0; r < p.s && alive; r += r_step) {
       const long long y = __ldg(p.targets + r);
       if (y == p.ignore_index) {
         // ignored row: zeros over this warp's share, nothing read
-        for (int i = 0; i < p.t; ++i) {
+        for (int i = 0; i < nt; ++i) {
           unsigned lo, hi;
-          sub_range<kDW>(unsigned(p.sh.start[i + 1] - p.sh.start[i]) * EB, w, lo, hi);
-          uint4* d = reinterpret_cast<uint4*>(const_cast<unsigned char*>(p.sh.ptr[i]) + r * p.sh.ld_bytes[i] + lo);
+          sub_range<kDW>(unsigned(geo.start[i + 1] - geo.start[i]) * EB, w, lo, hi);
+          uint4* d = reinterpret_cast<uint4*>(const_cast<unsigned char*>(geo.ptr[i]) + r * geo.ld[i] + lo);
           for (unsigned v = lane; v < (hi - lo) >> 4; v += 32) d[v] = make_uint4(0u, 0u, 0u, 0u);
         }
         if (w == 0 && lane == 0) {
@@ -297,9 +425,10 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
       }
       int ty;
       unsigned toff;
-      target_of<EB>(p, y, ty, toff);
+      target_of<EB>(geo, nt, y, ty, toff);
       const bool in_range = ty >= 0;
       const int buf = int(n & 1u);
+      top_up();
       if (!mbar_wait_warp(&sm.rowdone[buf], (n >> 1) & 1u)) {
         alive = false;
         break;
@@ -319,27 +448,15 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
         p.rowl[r] = rl;
         if (p.row_loss) p.row_loss[r] = rl;
       }
+      const float scale = p.grad_rows != nullptr ? __ldg(p.grad_rows + r) : scale_all;
       const float c = -lse * kLog2e;
       const float cb = folded_offset(c, scale);
 
-      // this row's chunks, kDSlots - 1 loads ahead; a slot is refilled once
-      // its store has read it
-      RowWalk<EB, kDW> iw, cw;
-      iw.seek(p, w, 0);
-      if (lane == 0) bulk_wait_read<0>();
-      __syncwarp();
-      for (int k = 0; k < kDSlots - 1 && iw.ok; ++k, iw.next(p, w)) {
-        unsigned a, b;
-        iw.bounds(a, b);
-        const int slot = int(issued % kDSlots);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[slot], b - a);
-          bulk_load(ring[slot], iw.addr(p, r, a), b - a, &full[slot], pol);
-        }
-        ++issued;
-      }
+      RowWalk<EB, kDW> cw;
 #pragma unroll 1
-      for (cw.seek(p, w, 0); cw.ok; cw.next(p, w)) {
+      for (cw.seek(geo, nt, r, w, 0); cw.ok; cw.next(geo, nt, r, w)) {
+        top_up();
+        if (issued == kc && prod.ok) issue();  // the stats partner has finished this row: the bytes are in L2
         unsigned a, b;
         cw.bounds(a, b);
         const int slot = int(kc % kDSlots);
@@ -347,6 +464,7 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
           alive = false;
           break;
         }
+        if (lane == 0) st_volatile(&sm.gdone[w], kc + 1);  // credit back to the stats partner
         unsigned char* sbuf = ring[slot];
         const bool has_t = cw.seg == ty && toff >= a && toff < b;
         float dt = 0.f;
@@ -360,20 +478,8 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
             Elem<T>::store(sbuf + (toff - a), dt);
             fence_proxy_async_smem();
           }
-          bulk_store(cw.addr(p, r, a), sbuf, b - a, pol);
+          bulk_store(cw.addr(a), sbuf, b - a, pol);
           bulk_commit();
-        }
-        if (iw.ok) {
-          unsigned ia, ib;
-          iw.bounds(ia, ib);
-          const int ps = int(issued % kDSlots);  // the slot of the previous chunk
-          if (lane == 0) {
-            bulk_wait_read<1>();
-            mbar_arrive_expect_tx(&full[ps], ib - ia);
-            bulk_load(ring[ps], iw.addr(p, r, ia), ib - ia, &full[ps], pol);
-          }
-          ++issued;
-          iw.next(p, w);
         }
         ++kc;
       }
@@ -389,9 +495,12 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
   // ---- batch loss: the last block sums the per-row losses in a fixed order
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(&p.hdr->ticket, 1u) == gridDim.x - 1;
+  // every copy of this CTA has completed: the stats ring is free scratch
+  double* sv = reinterpret_cast<double*>(sm.sring[0][0]);
+  int* last = reinterpret_cast<int*>(sm.sring[0][0] + 1024);
+  if (threadIdx.x == 0) *last = atomicAdd(&p.hdr->ticket, 1u) == gridDim.x - 1;
   __syncthreads();
-  if (!last) return;
+  if (!*last) return;
   __threadfence();
   double v = 0.0;
   const long long nb = (p.s + 255) / 256;
@@ -411,8 +520,9 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     const int cnt = p.hdr->n_valid;
     p.hdr->loss_sum = tot;
     p.hdr->ticket = 0u;
-    *p.loss_out =
-        p.reduction == VPCE_SUM ? float(tot) : (cnt > 0 ? float(tot / double(cnt)) : __int_as_float(0x7fc00000));
+    if (p.loss_out != nullptr)
+      *p.loss_out = p.reduction != VPCE_MEAN ? float(tot)
+                                             : (cnt > 0 ? float(tot / double(cnt)) : __int_as_float(0x7fc00000));
   }
 }
 
@@ -441,10 +551,17 @@ void launch_prep(const long long* targets, long long s, long long V, long long i
   prep_kernel<<<1, kPrepThreads, 0, st>>>(targets, s, V, ignore_index, hdr, reduction, loss_out);
 }
 
+// Chunks of slack per stats warp for rows of row_bytes: whatever of
+// kLiveBytesPerCta one row leaves, shared by the kSW stats warps.
+unsigned credit_slack(long long row_bytes) {
+  const long long spare = (long long)kLiveBytesPerCta - row_bytes;
+  return spare > 0 ? unsigned(spare / (long long)(kSW * kFChunk)) : 0u;
+}
+
 // The streaming fused kernel (expects launch_prep before it): one CTA per SM.
 void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long long V, const long long* targets,
-                         long long ignore_index, int reduction, float grad, float* lse, float* rowl,
-                         float* row_loss, float* loss_out, Header* hdr, int sms, cudaStream_t st) {
+                         long long ignore_index, int reduction, float grad, const float* grad_rows, float* lse,
+                         float* rowl, float* row_loss, float* loss_out, Header* hdr, int sms, cudaStream_t st) {
   FusedParams p;
   p.sh = sh;
   p.t = t;
@@ -454,6 +571,8 @@ void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long
   p.ignore_index = ignore_index;
   p.reduction = reduction;
   p.grad = grad;
+  p.grad_rows = grad_rows;
+  p.credit_slack = credit_slack(V * (bf16 ? 2 : 4));
   p.lse = lse;
   p.rowl = rowl;
   p.row_loss = row_loss;

@@ -55,6 +55,7 @@ struct BackwardParams {
   const Header* hdr;
   Header* hdr_flags;    // same header, for the timeout flag
   float grad;
+  const float* grad_rows;  // [s] per-row upstream gradient, or null (use grad)
 };
 
 template <typename T>

@@ -25,7 +25,8 @@ STATUS_NAMES = {
     6: "VPCE_ERR_UNSUPPORTED_DEVICE",
 }
 VPCE_FP32, VPCE_BF16 = 0, 1
-VPCE_MEAN, VPCE_SUM = 0, 1
+VPCE_MEAN, VPCE_SUM, VPCE_NONE = 0, 1, 2
+REDUCTIONS = {"mean": VPCE_MEAN, "sum": VPCE_SUM, "none": VPCE_NONE}
 VPCE_MAX_SHARDS = 64
 VPCE_FLAG_BAD_TARGET = 1
 VPCE_FLAG_WAIT_TIMEOUT = 2
@@ -63,9 +64,15 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.vpce_backward.restype = ctypes.c_int
         lib.vpce_backward.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
                                       ctypes.c_float, _P, ctypes.c_size_t, _P]
+        lib.vpce_backward_rows.restype = ctypes.c_int
+        lib.vpce_backward_rows.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
+                                           _P, _P, ctypes.c_size_t, _P]
         lib.vpce_forward_backward.restype = ctypes.c_int
         lib.vpce_forward_backward.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
                                               ctypes.c_int, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+        lib.vpce_forward_backward_rows.restype = ctypes.c_int
+        lib.vpce_forward_backward_rows.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
+                                                   ctypes.c_int, _P, _P, _P, _P, ctypes.c_size_t, _P]
         lib.vpce_fused_plan.restype = ctypes.c_int
         lib.vpce_fused_plan.argtypes = [ctypes.c_int, ctypes.c_int, _I64P, _I64, ctypes.POINTER(ctypes.c_int),
                                         ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
@@ -124,6 +131,16 @@ def backward_raw(shard_ptrs, dtype, t, s, vocab_start, ld, targets_ptr, ignore_i
                                  ws_ptr, int(ws_bytes), stream))
 
 
+def backward_rows_raw(shard_ptrs, dtype, t, s, vocab_start, ld, targets_ptr, ignore_index, grad_rows_ptr,
+                      ws_ptr, ws_bytes, stream) -> int:
+    lib = load_library()
+    ptrs = _ptr_array(shard_ptrs) if shard_ptrs is not None else None
+    vs = _i64_array(vocab_start) if vocab_start is not None else None
+    return int(lib.vpce_backward_rows(ctypes.cast(ptrs, _P) if ptrs is not None else None, int(dtype), int(t),
+                                      int(s), vs, int(ld), targets_ptr, int(ignore_index), grad_rows_ptr,
+                                      ws_ptr, int(ws_bytes), stream))
+
+
 # ----------------------------------------------------------------------------
 # torch-tensor forms
 # ----------------------------------------------------------------------------
@@ -179,10 +196,38 @@ def new_workspace(t: int, s: int, device=None):
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
+def _ptr(x):
+    return ctypes.c_void_p(x.data_ptr()) if x is not None else None
+
+
+def _outputs(reduction, loss_out, row_loss_out, s, dev):
+    """The reduction code and the loss buffers: 'none' returns the per-row
+    vector (allocated if not given); the others a scalar."""
+    import torch
+
+    red = REDUCTIONS[reduction]
+    if red == VPCE_NONE:
+        if row_loss_out is None:
+            row_loss_out = torch.empty(s, dtype=torch.float32, device=dev)
+        return red, loss_out, row_loss_out, row_loss_out
+    if loss_out is None:
+        loss_out = torch.empty((), dtype=torch.float32, device=dev)
+    return red, loss_out, row_loss_out, loss_out
+
+
+def _check_grad_rows(grad_rows, s):
+    import torch
+
+    if grad_rows.dtype != torch.float32 or not grad_rows.is_cuda or grad_rows.numel() != s \
+            or (s > 1 and grad_rows.stride(0) != 1):
+        raise ValueError("grad_rows must be a contiguous CUDA float32 tensor with one entry per row")
+
+
 def vpce_forward(shards, targets, vocab_start=None, *, ignore_index: int = -100, reduction: str = "mean",
                  loss_out=None, row_loss_out=None, workspace=None, stream=None):
     """Loss of vocab-sharded logits.  Returns ``(loss, workspace)``; pass the
-    workspace unchanged to :func:`vpce_backward`."""
+    workspace unchanged to :func:`vpce_backward`.  With ``reduction='none'``
+    the loss returned is the per-row vector."""
     import torch
 
     dtype, s, vs, ld = _describe(shards, vocab_start)
@@ -192,28 +237,36 @@ def vpce_forward(shards, targets, vocab_start=None, *, ignore_index: int = -100,
         raise ValueError("targets must be a CUDA int64 tensor with one entry per row")
     if workspace is None:
         workspace = new_workspace(t, s, dev)
-    if loss_out is None:
-        loss_out = torch.empty((), dtype=torch.float32, device=dev)
-    red = {"mean": VPCE_MEAN, "sum": VPCE_SUM}[reduction]
+    red, loss_out, row_loss_out, result = _outputs(reduction, loss_out, row_loss_out, s, dev)
     code = forward_raw([sh.data_ptr() for sh in shards], dtype, t, s, vs, ld,
-                       ctypes.c_void_p(targets.data_ptr()), ignore_index, red,
-                       ctypes.c_void_p(loss_out.data_ptr()),
-                       ctypes.c_void_p(row_loss_out.data_ptr()) if row_loss_out is not None else None,
-                       ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+                       ctypes.c_void_p(targets.data_ptr()), ignore_index, red, _ptr(loss_out),
+                       _ptr(row_loss_out), ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                       _stream_ptr(stream))
     if code != VPCE_OK:
         raise VPCEError(code, "vpce_forward")
-    return loss_out, workspace
+    return result, workspace
 
 
 def vpce_backward(shards, targets, workspace, vocab_start=None, *, ignore_index: int = -100,
-                  grad_output: float = 1.0, stream=None):
-    """Overwrite ``shards`` in place with dlogits of the preceding forward."""
+                  grad_output: float = 1.0, grad_rows=None, stream=None):
+    """Overwrite ``shards`` in place with dlogits of the preceding forward.
+    ``grad_rows`` (a float32 vector, one entry per row) selects the per-row
+    backward (vpce_backward_rows) instead of the scalar ``grad_output``."""
     dtype, s, vs, ld = _describe(shards, vocab_start)
-    code = backward_raw([sh.data_ptr() for sh in shards], dtype, len(shards), s, vs, ld,
-                        ctypes.c_void_p(targets.data_ptr()), ignore_index, grad_output,
-                        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+    ptrs = [sh.data_ptr() for sh in shards]
+    if grad_rows is not None:
+        _check_grad_rows(grad_rows, s)
+        code = backward_rows_raw(ptrs, dtype, len(shards), s, vs, ld, ctypes.c_void_p(targets.data_ptr()),
+                                 ignore_index, _ptr(grad_rows), ctypes.c_void_p(workspace.data_ptr()),
+                                 workspace.numel(), _stream_ptr(stream))
+        where = "vpce_backward_rows"
+    else:
+        code = backward_raw(ptrs, dtype, len(shards), s, vs, ld, ctypes.c_void_p(targets.data_ptr()),
+                            ignore_index, grad_output, ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                            _stream_ptr(stream))
+        where = "vpce_backward"
     if code != VPCE_OK:
-        raise VPCEError(code, "vpce_backward")
+        raise VPCEError(code, where)
     return shards
 
 
@@ -228,11 +281,24 @@ def forward_backward_raw(shard_ptrs, dtype, t, s, vocab_start, ld, targets_ptr, 
                                          int(ws_bytes), stream))
 
 
+def forward_backward_rows_raw(shard_ptrs, dtype, t, s, vocab_start, ld, targets_ptr, ignore_index, reduction,
+                              grad_rows_ptr, loss_ptr, row_loss_ptr, ws_ptr, ws_bytes, stream) -> int:
+    lib = load_library()
+    ptrs = _ptr_array(shard_ptrs) if shard_ptrs is not None else None
+    vs = _i64_array(vocab_start) if vocab_start is not None else None
+    return int(lib.vpce_forward_backward_rows(ctypes.cast(ptrs, _P) if ptrs is not None else None, int(dtype),
+                                              int(t), int(s), vs, int(ld), targets_ptr, int(ignore_index),
+                                              int(reduction), grad_rows_ptr, loss_ptr, row_loss_ptr, ws_ptr,
+                                              int(ws_bytes), stream))
+
+
 def vpce_forward_backward(shards, targets, vocab_start=None, *, ignore_index: int = -100,
-                          reduction: str = "mean", grad_output: float = 1.0, loss_out=None, row_loss_out=None,
-                          workspace=None, stream=None):
+                          reduction: str = "mean", grad_output: float = 1.0, grad_rows=None, loss_out=None,
+                          row_loss_out=None, workspace=None, stream=None):
     """Loss and in-place dlogits in one call (the logits cross HBM once each
-    way).  Returns ``(loss, workspace)``; ``shards`` now hold dlogits."""
+    way).  Returns ``(loss, workspace)`` (the per-row vector for
+    ``reduction='none'``); ``shards`` now hold dlogits.  ``grad_rows`` (one
+    float32 per row) replaces the scalar ``grad_output``."""
     import torch
 
     dtype, s, vs, ld = _describe(shards, vocab_start)
@@ -242,17 +308,23 @@ def vpce_forward_backward(shards, targets, vocab_start=None, *, ignore_index: in
         raise ValueError("targets must be a CUDA int64 tensor with one entry per row")
     if workspace is None:
         workspace = new_workspace(t, s, dev)
-    if loss_out is None:
-        loss_out = torch.empty((), dtype=torch.float32, device=dev)
-    red = {"mean": VPCE_MEAN, "sum": VPCE_SUM}[reduction]
-    code = forward_backward_raw([sh.data_ptr() for sh in shards], dtype, t, s, vs, ld,
-                                ctypes.c_void_p(targets.data_ptr()), ignore_index, red, grad_output,
-                                ctypes.c_void_p(loss_out.data_ptr()),
-                                ctypes.c_void_p(row_loss_out.data_ptr()) if row_loss_out is not None else None,
-                                ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+    red, loss_out, row_loss_out, result = _outputs(reduction, loss_out, row_loss_out, s, dev)
+    ptrs = [sh.data_ptr() for sh in shards]
+    if grad_rows is not None:
+        _check_grad_rows(grad_rows, s)
+        code = forward_backward_rows_raw(ptrs, dtype, t, s, vs, ld, ctypes.c_void_p(targets.data_ptr()),
+                                         ignore_index, red, _ptr(grad_rows), _ptr(loss_out), _ptr(row_loss_out),
+                                         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                         _stream_ptr(stream))
+        where = "vpce_forward_backward_rows"
+    else:
+        code = forward_backward_raw(ptrs, dtype, t, s, vs, ld, ctypes.c_void_p(targets.data_ptr()), ignore_index,
+                                    red, grad_output, _ptr(loss_out), _ptr(row_loss_out),
+                                    ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+        where = "vpce_forward_backward"
     if code != VPCE_OK:
-        raise VPCEError(code, "vpce_forward_backward")
-    return loss_out, workspace
+        raise VPCEError(code, where)
+    return result, workspace
 
 
 def vpce_fused_plan(dtype: int, vocab_start, s: int) -> dict:
@@ -296,12 +368,10 @@ def vpce_forward_static(shards, targets, loss_out, vocab_start=None, *, ignore_i
     """Loss of vocab-sharded logits into the caller's ``loss_out`` (and
     ``row_loss_out``), using no workspace from the caller."""
     dtype, s, vs, ld = _describe(shards, vocab_start)
-    red = {"mean": VPCE_MEAN, "sum": VPCE_SUM}[reduction]
+    red = REDUCTIONS[reduction]
     code = forward_static_raw([sh.data_ptr() for sh in shards], dtype, len(shards), s, vs, ld,
-                              ctypes.c_void_p(targets.data_ptr()), ignore_index, red,
-                              ctypes.c_void_p(loss_out.data_ptr()),
-                              ctypes.c_void_p(row_loss_out.data_ptr()) if row_loss_out is not None else None,
-                              _stream_ptr(stream))
+                              ctypes.c_void_p(targets.data_ptr()), ignore_index, red, _ptr(loss_out),
+                              _ptr(row_loss_out), _stream_ptr(stream))
     if code != VPCE_OK:
         raise VPCEError(code, "vpce_forward_static")
     return loss_out
