@@ -163,6 +163,26 @@ def _bind_to_gpu_cpus(dev) -> None:
         pass
 
 
+def _max_over_ranks(x: float, device=None) -> float:
+    """The largest x over the ranks of the default process group (x itself
+    without one).  `device` holds the collective's tensor: a CUDA device for
+    NCCL, None (host) for gloo."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _weak_scaling_value(units_per_rank: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time."""
+    return world * units_per_rank / (max_ms * 1e-3)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -251,10 +271,7 @@ def run_ours(args):
     total_ms = t0.elapsed_time(t1)
     fwd_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
     bwd_ms = [ev[1].elapsed_time(ev[2]) for ev in evs]
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = _max_over_ranks(total_ms, dev)
 
     # ---------------- end to end through the public API: every step copies its
     # logits and targets from pinned host memory and reads its loss back.
@@ -301,7 +318,7 @@ def run_ours(args):
         used[b].record(stream)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
     h2d = buf_bytes + w.s * 8
     d2h = 4
 
@@ -312,7 +329,7 @@ def run_ours(args):
 
     peak, peak_kind = _peaks()
     ms_step = total_ms / args.steps
-    tokens_s = world * w.s * args.steps / (total_ms * 1e-3)
+    tokens_s = _weak_scaling_value(w.s * args.steps, world, total_ms)
     n_valid = int(np.sum(meta.targets != w.ignore_index))
     three_pass = 3 * w.s * w.V * e
     gbs_3pass = three_pass / (ms_step * 1e-3) / 1e9
@@ -377,7 +394,7 @@ def run_ours(args):
             "algorithmic_bytes_per_launch": dom_bytes,
         },
         "e2e": {
-            "value": round(w.s * world / (e2e_ms * 1e-3), 1),
+            "value": round(_weak_scaling_value(w.s, world, e2e_ms), 1),
             "unit": "tokens/s",
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
