@@ -48,6 +48,21 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
+def _tensor_peaks():
+    """(burst, sustained, kind) dense bf16 TFLOP/s."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
+
+
 def _env_rank():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -508,6 +523,188 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+# ----------------------------------------------------------------------------
+# the LM-head GEMM fused with the forward loss (vpce_lmhead_forward)
+# ----------------------------------------------------------------------------
+LMHEAD_METRIC = "LM-head GEMM + VPCE forward tokens/s & TFLOP/s (% of peak), s=8192 h=8192 V=128256 bf16, 1 GB300"
+
+
+def run_lmhead(args):
+    import torch
+
+    from vocab_sharded_lm_gb300 import _build, vpce
+    from oracle import vpce_oracle as O
+
+    rank, world, local = _env_rank()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    vpce.load_library()
+    m = synth.LMHEADS[synth.LMHEAD_BENCH]
+    if args.rows:
+        m = m.replace(s=args.rows)
+    vs = synth.even_vocab_start(m.V, m.t)
+    meta = synth.lmhead_meta(m)
+    x, ws = synth.lmhead_device(m, vs, device=dev)
+    y = torch.from_numpy(meta.targets).to(dev)
+    wk = torch.empty(vpce.vpce_lmhead_workspace_bytes(m.s), dtype=torch.uint8, device=dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        vpce.vpce_lmhead_forward(x, ws, y, vs, ignore_index=m.ignore_index, loss_out=loss, workspace=wk)
+
+    for _ in range(args.warmup):
+        step()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        evs[k][0].record(stream)
+        step()
+        evs[k][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = _max_over_ranks(t0.elapsed_time(t1), dev)
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    # end to end: the step's hidden states (and targets) copied in from pinned
+    # host memory, the loss read back; the head's weights stay on the device
+    hx = x.cpu().pin_memory()
+    hy = torch.from_numpy(meta.targets).pin_memory()
+    xb = [x, torch.empty_like(x)]
+    yb = [y, torch.empty_like(y)]
+    lb = [torch.empty((), dtype=torch.float32, device=dev) for _ in range(2)]
+    wkb = [wk, torch.empty_like(wk)]
+    host_loss = torch.empty(max(1, args.e2e_steps), dtype=torch.float32).pin_memory()
+    cs = torch.cuda.Stream(dev)
+    done = [torch.cuda.Event() for _ in range(2)]
+    used = [torch.cuda.Event() for _ in range(2)]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n_e2e = max(1, args.e2e_steps)
+    warm = 2
+    for k in range(-warm, n_e2e):
+        if k == 0:
+            stream.synchronize()
+            cs.synchronize()
+            e0.record(cs)
+        b = k % 2
+        with torch.cuda.stream(cs):
+            if k >= 2 - warm:
+                cs.wait_event(used[b])
+            xb[b].copy_(hx, non_blocking=True)
+            yb[b].copy_(hy, non_blocking=True)
+            done[b].record(cs)
+        stream.wait_event(done[b])
+        vpce.vpce_lmhead_forward(xb[b], ws, yb[b], vs, ignore_index=m.ignore_index, loss_out=lb[b],
+                                 workspace=wkb[b])
+        host_loss[max(k, 0)].copy_(lb[b], non_blocking=True)
+        used[b].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    flops = 2.0 * m.s * m.h * m.V
+    burst, sustained, kind = _tensor_peaks()
+    achieved = flops / (call_ms * 1e-3) / 1e12
+    ms_step = total_ms / args.steps
+    out = {
+        "metric": LMHEAD_METRIC,
+        "value": round(_weak_scaling_value(m.s * args.steps, world, total_ms), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; no dataset or trained weights)",
+        "config": {
+            "workload": (f"{m.name}: X [{m.s}, {m.h}] ~N(0,{m.sigma_x:g}^2), head [{m.V}, {m.h}] in t={m.t} "
+                         f"vocabulary shards ~N(0,({m.logit_sigma:g}/sqrt(h))^2) (logits ~N(0,{m.logit_sigma:g}^2)), "
+                         f"bf16, targets uniform"),
+            "global_batch": m.s * world,
+            "seq_len": m.s,
+            "parallelism": f"vocab shards t={m.t} on one GPU; {world} independent replica(s)",
+            "l2": f"inputs larger than L2: the head is {sum(w.numel() for w in ws) * 2 / 1e9:.2f} GB",
+            "path": "vpce_lmhead_forward (tcgen05 GEMM, fp32 accumulators in TMEM, loss statistics in the "
+                    "epilogue; the logits are never written), then the shard combine",
+        },
+        "tflops": round(achieved, 1),
+        "roofline": {
+            "kernel": "gemm_stats_kernel",
+            "bound": "tensor",
+            "achieved": round(achieved, 1),
+            "peak": burst,
+            "peak_kind": f"{kind} burst (cuBLAS bf16)",
+            "unit": "TFLOP/s",
+            "frac": round(achieved / burst, 4),
+            "frac_of_sustained": round(achieved / sustained, 4),
+            "traffic": None,
+            "algorithmic_flops_per_launch": flops,
+            "note": "achieved = 2 s h V / mean CUDA-event time of one call (the GEMM launch plus the few-us combine)",
+        },
+        "e2e": {
+            "value": round(_weak_scaling_value(m.s, world, e2e_ms), 1),
+            "unit": "tokens/s",
+            "h2d_bytes_per_step": int(x.numel() * 2 + m.s * 8),
+            "d2h_bytes_per_step": 4,
+            "steps": n_e2e,
+            "ms_per_step": round(e2e_ms, 4),
+            "note": "pinned host hidden states + targets copied in every step (copy stream, double-buffered), "
+                    "loss read back; the head's weights stay on the device",
+        },
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        # the oracle on a bounded sample: a few rows against the first vocabulary
+        # rows of the head (read back from the device generator), scaled to the
+        # full vocabulary (the oracle's cost is linear in V)
+        nv = min(8192, m.V)
+        w_sample = ws[0][:nv].view(torch.int16).cpu().numpy().view(np.uint16)
+        rows = np.arange(4)
+        x_sample = x[:4].view(torch.int16).cpu().numpy().view(np.uint16)
+        t_start = time.perf_counter()
+        done_rows = 0
+        while time.perf_counter() - t_start < args.cpu_seconds:
+            z = O.lmhead_logits(x_sample, [w_sample], [0, nv])
+            O.cross_entropy(z, np.minimum(meta.targets[rows], nv - 1))
+            done_rows += len(rows)
+        dt = time.perf_counter() - t_start
+        out["cpu_baseline"] = {
+            "value": round(done_rows / dt * nv / m.V, 3),
+            "unit": "tokens/s",
+            "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{done_rows} rows x {nv} of {m.V} vocabulary rows (fp64 numpy matmul on up to {os.cpu_count()} BLAS threads + loss), "
+                      f"{dt:.1f} s, scaled by {nv}/{m.V}",
+        }
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -520,8 +717,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=["fused", "split"], default="fused",
-                    help="fused: vpce_forward_backward; split: vpce_forward then vpce_backward")
+    ap.add_argument("--path", choices=["fused", "split", "lmhead"], default="fused",
+                    help="fused: vpce_forward_backward; split: vpce_forward then vpce_backward; "
+                         "lmhead: the LM-head GEMM fused with the forward loss (its own metric)")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the workload's row count (small profiling captures only)")
     args = ap.parse_args()
@@ -529,6 +727,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.path == "lmhead":
+        run_lmhead(args)
     else:
         run_ours(args)
 

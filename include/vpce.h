@@ -229,6 +229,38 @@ vpce_status vpce_forward_static(const void* const* shards, vpce_dtype dtype, int
                                 vpce_stream_t stream);
 
 /*
+ * LM-head GEMM fused with the forward loss: the logits of shard i are
+ * z_i = X W_i^T, computed tile by tile on the tensor cores (bf16 in, fp32
+ * accumulate) and reduced in the tile's epilogue to the per-row maximum, sum
+ * of exponentials and target logit, so the [s, V] logits are never written
+ * ("Distributed Training III: Model Parallelism", CMU 11-868 Lecture 16
+ * notes, §5.5: do not assemble the big tensor, move the later computation to
+ * the data; "LLM Internals" §7.3.4: the LM head [128256, 8192] split by
+ * vocabulary, 16032 rows per card at t = 8).  The combine and the batch sum
+ * are vpce_forward's, so loss_out, row_loss_out, the reduction and the
+ * workspace's logsumexp / n_valid / error flag mean the same.
+ *   hidden         device bf16 [s, h], row stride ld_hidden elements (0 = h);
+ *                  16-byte aligned base, ld_hidden * 2 a multiple of 16.
+ *   weight_shards  host array of t device pointers; shard i is bf16
+ *                  [w_i, h] (one row per vocabulary entry, K contiguous),
+ *                  row stride ld_weight elements (0 = h); 16-byte aligned,
+ *                  ld_weight * 2 a multiple of 16.
+ *   t              1..32 shards; vocab_start as vpce_forward (t+1 offsets).
+ *   h              hidden size, a positive multiple of 64.
+ *   workspace      vpce_lmhead_workspace_bytes(s) bytes, 256-byte aligned.
+ * Other arguments and errors as vpce_forward.  No backward is provided (it
+ * would recompute the logits tile by tile).
+ */
+#define VPCE_LMHEAD_MAX_GROUPS 256
+size_t vpce_lmhead_workspace_bytes(int64_t s);
+vpce_status vpce_lmhead_forward(const void* hidden, int64_t ld_hidden,
+                                const void* const* weight_shards, int64_t ld_weight,
+                                int t, int64_t s, int64_t h, const int64_t* vocab_start,
+                                const int64_t* targets, int64_t ignore_index,
+                                vpce_reduction reduction, float* loss_out, float* row_loss_out,
+                                void* workspace, size_t workspace_bytes, vpce_stream_t stream);
+
+/*
  * Synchronise `stream`, then copy the workspace error flag to *flag (bit 0:
  * bad target seen by the last forward; bit 1: a device wait timed out).
  */

@@ -54,6 +54,7 @@ __all__ = [
     "split_columns",
     "shard_partials",
     "combine_sharded",
+    "lmhead_logits",
 ]
 
 
@@ -203,6 +204,33 @@ def dlogits(z: np.ndarray, y: np.ndarray, ignore_index: int = -100,
         d[rows] = scale[rows][:, None] * p
     d[bad] = np.nan
     return d
+
+
+# --------------------------------------------------------------------------
+# the LM head in front of the loss
+# --------------------------------------------------------------------------
+def lmhead_logits(x, w_shards, vocab_start, dtype: str = "bf16") -> np.ndarray:
+    """Full fp64 logits of a vocabulary-split LM head, ``z = X W^T``.
+
+    "LLM Internals" §7.3.4 splits the LM head ``[V, h]`` (``[128256, 8192]``
+    for Llama-3-70B) along the vocabulary, ``[16032, h]`` per card at t = 8;
+    card i's logits are the columns ``vocab_start[i] .. vocab_start[i+1]-1``
+    of ``z``.  ``x`` is ``[s, h]``, ``w_shards[i]`` is ``[w_i, h]`` (one row
+    per vocabulary entry), both in the stored form of ``dtype`` (bf16 bit
+    patterns or float32), widened exactly; the product is a plain fp64 matrix
+    multiply, so z is the exact dot product up to fp64 rounding.
+    """
+    X = widen(x, dtype)
+    vs = [int(v) for v in vocab_start]
+    if len(vs) != len(w_shards) + 1 or vs[0] != 0:
+        raise ValueError("vocab_start must have t+1 entries starting at 0")
+    z = np.empty((X.shape[0], vs[-1]), dtype=np.float64)
+    for i, w in enumerate(w_shards):
+        W = widen(w, dtype)
+        if W.shape != (vs[i + 1] - vs[i], X.shape[1]):
+            raise ValueError(f"shard {i} has shape {W.shape}")
+        z[:, vs[i]:vs[i + 1]] = X @ W.T
+    return z
 
 
 # --------------------------------------------------------------------------

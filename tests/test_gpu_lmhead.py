@@ -1,0 +1,166 @@
+"""GPU parity of vpce_lmhead_forward (LM-head GEMM on the tensor cores fused
+with the sharded loss) against the fp64 oracle: z = X W^T, then the
+cross-entropy of z, every row of small cases with ragged M and N tiles,
+uneven and one-column shards, padded row strides, ignored and bad targets,
+the reductions, and sampled rows of the full-size head.
+
+Tolerances.  The tensor cores multiply bf16 exactly and accumulate in fp32,
+h / 16 accumulator updates per logit (16 products per tcgen05.mma step).  A
+logit's error is then at most gamma * S_rk, gamma = (h / 16) * 2^-24 and S_rk
+= sum_k |x_rk w_jk| (the classic bound for that many rounded additions), and
+a row's loss lse - z_y moves by at most twice the largest logit error.  The
+test bounds each row by 2 * gamma * max_j S_rj.  The batch loss carries the
+loss tolerance of the sharded path, 1e-5 relative."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import vpce_oracle as O
+from vocab_sharded_lm_gb300 import synth, vpce
+
+pytestmark = pytest.mark.gpu
+
+LOSS_RTOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from vocab_sharded_lm_gb300 import _build
+
+    _build.build()
+    vpce.load_library()
+
+
+def _host(m, vs, rows=None):
+    rows = np.arange(m.s) if rows is None else np.asarray(rows)
+    xh = synth.dense_host(m.seed, synth.STREAM_HIDDEN, rows, m.h, m.sigma_x)
+    wh = [synth.dense_host(m.seed, synth.STREAM_WEIGHT, np.arange(vs[i], vs[i + 1]), m.h, m.sigma_w)
+          for i in range(len(vs) - 1)]
+    return xh, wh
+
+
+def _row_bound(xh, wh, h):
+    """2 * gamma * max_j sum_k |x_rk w_jk| per row."""
+    X = np.abs(O.widen(xh, "bf16"))
+    S = np.max(np.concatenate([X @ np.abs(O.widen(w, "bf16")).T for w in wh], axis=1), axis=1)
+    return 2.0 * (h / 16) * 2.0 ** -24 * S
+
+
+def _check(m, vs=None, *, targets=None, reduction="mean", pad_x=0, pad_w=0):
+    vs = synth.even_vocab_start(m.V, m.t) if vs is None else list(vs)
+    meta = synth.lmhead_meta(m)
+    y_host = meta.targets if targets is None else np.asarray(targets, dtype=np.int64)
+    x, ws = synth.lmhead_device(m, vs)
+    if pad_x:
+        xp = torch.zeros((m.s, m.h + pad_x), dtype=torch.bfloat16, device="cuda")
+        xp[:, :m.h] = x
+        x = xp[:, :m.h]
+    if pad_w:
+        wp = []
+        for w in ws:
+            b = torch.zeros((w.shape[0], m.h + pad_w), dtype=torch.bfloat16, device="cuda")
+            b[:, :m.h] = w
+            wp.append(b[:, :m.h])
+        ws = wp
+    y = torch.from_numpy(y_host).cuda()
+    rl = torch.full((m.s,), -7.0, dtype=torch.float32, device="cuda")
+    loss_t = torch.full((), -7.0, dtype=torch.float32, device="cuda")
+    out, wk = vpce.vpce_lmhead_forward(x, ws, y, vs, ignore_index=m.ignore_index, reduction=reduction,
+                                       loss_out=loss_t, row_loss_out=rl)
+    flag = vpce.vpce_read_error_flag(wk)
+    got_rows = rl.cpu().numpy().astype(np.float64)
+    got_loss = float(loss_t.item())
+
+    xh, wh = _host(m, vs)
+    z = O.lmhead_logits(xh, wh, vs)
+    ref = O.cross_entropy(z, y_host, m.ignore_index, reduction=reduction)
+    valid = ref["valid"]
+    bound = _row_bound(xh, wh, m.h)
+    err = np.abs(got_rows - ref["row_loss"])
+    assert np.all(err[valid] <= bound[valid]), (err[valid].max(), bound[valid].min())
+    assert np.all(got_rows[y_host == m.ignore_index] == 0.0)
+    bad = (~valid) & (y_host != m.ignore_index)
+    assert np.all(np.isnan(got_rows[bad]))
+    assert flag == ref["error_flag"]
+    exp_loss = ref["loss"] if np.ndim(ref["loss"]) == 0 else float(ref["row_loss"].sum())
+    if np.isnan(exp_loss):
+        assert np.isnan(got_loss)
+    else:
+        assert abs(got_loss - exp_loss) <= LOSS_RTOL * abs(exp_loss), (got_loss, exp_loss)
+    return got_rows, got_loss
+
+
+@pytest.mark.parametrize("m,vs", [
+    (synth.LMHEADS["lmhead_s300_h512_v5000"], None),          # ragged M and N tiles, 3 shards, ignored rows
+    (synth.LmHead("one_tile", 8, 128, 64, 256, 1), None),      # one tile, one K step
+    (synth.LmHead("one_row", 9, 1, 128, 17, 1), None),         # one row, 17 columns
+    (synth.LmHead("uneven", 10, 513, 192, 3000, 5), [0, 1, 300, 301, 2000, 3000]),  # one-column shards
+    (synth.LmHead("deep", 11, 256, 8192, 2000, 2), None),      # the pages' hidden size
+    (synth.LmHead("many_waves", 12, 1200, 128, 700, 7, ignore_frac=0.1), None),  # more M tiles than one wave
+])
+def test_lmhead_parity(m, vs):
+    _check(m, vs)
+
+
+def test_lmhead_padded_row_strides():
+    _check(synth.LmHead("padded", 13, 200, 256, 1500, 3), pad_x=64, pad_w=128)
+
+
+@pytest.mark.parametrize("reduction", ["sum", "none"])
+def test_lmhead_reductions(reduction):
+    _check(synth.LmHead("red", 14, 160, 128, 900, 2, ignore_frac=0.1), reduction=reduction)
+
+
+def test_lmhead_bad_and_ignored_targets():
+    m = synth.LmHead("bad", 15, 140, 64, 600, 3)
+    y = synth.lmhead_meta(m).targets.copy()
+    y[[0, 77]] = -100
+    y[5] = 600          # one past the vocabulary
+    y[6] = -3
+    rows, loss = _check(m, targets=y)
+    assert np.isnan(loss)
+
+
+def test_lmhead_deterministic():
+    m = synth.LmHead("det", 16, 300, 256, 3000, 4)
+    a = _check(m)
+    b = _check(m)
+    np.testing.assert_array_equal(a[0], b[0])
+    assert a[1] == b[1]
+
+
+def test_lmhead_full_size_sampled_rows():
+    """The pages' head (s = 8192, h = 8192, V = 128256, t = 8) in the launch
+    configuration bench.py times, checked on sampled rows.  The 1.05e9
+    weights come from the generator's device twin: a random sample of them is
+    first checked against the host generator, then the sampled rows' logits
+    are formed in fp64 from the read-back weights."""
+    m = synth.LMHEADS["lmhead_s8192_h8192_v128256"]
+    vs = synth.even_vocab_start(m.V, m.t)
+    meta = synth.lmhead_meta(m)
+    x, ws = synth.lmhead_device(m, vs)
+    y = torch.from_numpy(meta.targets).cuda()
+    rl = torch.empty(m.s, dtype=torch.float32, device="cuda")
+    loss, wk = vpce.vpce_lmhead_forward(x, ws, y, vs, row_loss_out=rl)
+    assert vpce.vpce_read_error_flag(wk) == 0
+    got = rl.cpu().numpy().astype(np.float64)
+    assert abs(float(loss) - got.mean()) <= 1e-6 * abs(got.mean())
+
+    rng = np.random.default_rng(7)
+    w_host = [w.view(torch.int16).cpu().numpy().view(np.uint16) for w in ws]
+    for i in range(m.t):
+        pick = rng.integers(0, vs[i + 1] - vs[i], size=64)
+        ref = synth.dense_host(m.seed, synth.STREAM_WEIGHT, vs[i] + pick, m.h, m.sigma_w)
+        # the device generator's float64 log/cos may differ from the host's in
+        # the last bit, which moves a stored value by at most one bf16 ulp
+        diff = np.abs(w_host[i][pick].astype(np.int64) - ref.astype(np.int64))
+        assert diff.max() <= 1 and np.count_nonzero(diff) <= 2
+    rows = np.concatenate([[0, m.s - 1], rng.integers(1, m.s - 1, size=6)])
+    xh = synth.dense_host(m.seed, synth.STREAM_HIDDEN, rows, m.h, m.sigma_x)
+    z = O.lmhead_logits(xh, w_host, vs)
+    ref = O.cross_entropy(z, meta.targets[rows], m.ignore_index, n_valid=int(np.sum(meta.targets != m.ignore_index)))
+    bound = _row_bound(xh, w_host, m.h)
+    err = np.abs(got[rows] - ref["row_loss"])
+    assert np.all(err <= bound), (err, bound)

@@ -218,6 +218,44 @@ def test_sampled_rows_use_batch_n_valid():
 
 
 # ---------------------------------------------------------------- bf16 widening
+# ---------------------------------------------------------------- LM head
+def _bf16(a):
+    return torch.tensor(a, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_lmhead_one_hot_rows_select_weight_columns():
+    """X rows that are unit vectors e_k pick column k of the head exactly."""
+    rng = np.random.default_rng(3)
+    h, V, s = 64, 37, 5
+    W = _bf16(rng.normal(size=(V, h)))
+    ks = np.array([0, 5, 63, 17, 5])
+    x = np.zeros((s, h), dtype=np.float32)
+    x[np.arange(s), ks] = 1.0
+    vs = [0, 10, 37]
+    z = O.lmhead_logits(_bf16(x), [W[:10], W[10:]], vs)
+    np.testing.assert_array_equal(z, O.widen(W, "bf16")[:, ks].T)
+
+
+def test_lmhead_matches_torch_linear_and_cross_entropy():
+    rng = np.random.default_rng(4)
+    s, h, V = 40, 128, 300
+    x = _bf16(rng.normal(size=(s, h)))
+    W = _bf16(rng.normal(0.0, 3.0 / np.sqrt(h), size=(V, h)))
+    y = rng.integers(0, V, size=s)
+    y[[3, 11]] = -100
+    vs = [0, 100, 256, 300]
+    z = O.lmhead_logits(x, [W[vs[i]:vs[i + 1]] for i in range(3)], vs)
+    xt = torch.tensor(O.widen(x, "bf16"))
+    wt = torch.tensor(O.widen(W, "bf16"))
+    zt = torch.nn.functional.linear(xt, wt)
+    np.testing.assert_allclose(z, zt.numpy(), rtol=1e-13, atol=1e-13)
+    ref = torch.nn.functional.cross_entropy(zt, torch.tensor(y), ignore_index=-100)
+    assert O.cross_entropy(z, y)["loss"] == pytest.approx(float(ref), rel=1e-12)
+    # the split does not change the logits
+    z1 = O.lmhead_logits(x, [W], [0, V])
+    np.testing.assert_allclose(z, z1, rtol=1e-14, atol=1e-14)
+
+
 def test_bf16_widening_exact():
     bits = np.array([0x3F80, 0xC000, 0x4049, 0x0000, 0x8000, 0x7F7F, 0x0001, 0xBF00], dtype=np.uint16)
     got = O.widen(bits, "bf16")

@@ -25,7 +25,8 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas"
               "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
 
 LIBS = {
-    "libvpce.so": ["vpce_api.cu", "vpce_forward.cu", "vpce_backward.cu", "vpce_fused.cu", "vpce_static.cu"],
+    "libvpce.so": ["vpce_api.cu", "vpce_forward.cu", "vpce_backward.cu", "vpce_fused.cu", "vpce_static.cu",
+                   "vpce_gemm.cu"],
     "libvpce_synth.so": ["synth_gen.cu"],
 }
 HEADERS = ["vpce_device.cuh", "vpce_kernels.cuh", "vpce_chunk.cuh"]

@@ -17,6 +17,11 @@ void launch_prep(const long long* targets, long long s, long long V, long long i
 void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long long V, const long long* targets,
                          long long ignore_index, int reduction, float grad, const float* grad_rows, float* lse,
                          float* rowl, float* row_loss, float* loss_out, Header* hdr, int sms, cudaStream_t st);
+cudaError_t set_gemm_smem();
+int gemm_max_shards();
+bool launch_gemm_stats(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
+                       long long h, const long long* vocab_start, const long long* targets, long long ignore_index,
+                       float2* part, float* tgt, Header* hdr, int sms, int* groups, cudaStream_t st);
 
 }  // namespace vpce
 
@@ -57,7 +62,7 @@ vpce_status device_setup(int* sms) {
     if (major != 10 || minor != 3) {
       d.status = VPCE_ERR_UNSUPPORTED_DEVICE;
     } else if (set_stats_smem() != cudaSuccess || set_backward_smem() != cudaSuccess ||
-               set_fused_smem() != cudaSuccess) {
+               set_fused_smem() != cudaSuccess || set_gemm_smem() != cudaSuccess) {
       cudaGetLastError();
       return VPCE_ERR_CUDA;
     } else {
@@ -368,6 +373,81 @@ vpce_status vpce_read_error_flag(const void* workspace, int* flag, vpce_stream_t
   }
   *flag = v;
   return VPCE_OK;
+}
+
+size_t vpce_lmhead_workspace_bytes(int64_t s) {
+  if (s < 0 || s > (int64_t(1) << 31)) return 0;
+  return WsLayout(VPCE_LMHEAD_MAX_GROUPS, s).total;
+}
+
+vpce_status vpce_lmhead_forward(const void* hidden, int64_t ld_hidden, const void* const* weight_shards,
+                                int64_t ld_weight, int t, int64_t s, int64_t h, const int64_t* vocab_start,
+                                const int64_t* targets, int64_t ignore_index, vpce_reduction reduction,
+                                float* loss_out, float* row_loss_out, void* workspace, size_t workspace_bytes,
+                                vpce_stream_t stream) {
+  if (t < 1 || t > gemm_max_shards() || s < 0 || s >= (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  if (h < 64 || h % 64 != 0 || h >= (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  if (weight_shards == nullptr || vocab_start == nullptr || vocab_start[0] != 0) return VPCE_ERR_INVALID_ARG;
+  for (int i = 0; i < t; ++i)
+    if (vocab_start[i + 1] <= vocab_start[i]) return VPCE_ERR_INVALID_ARG;
+  if (vocab_start[t] >= (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  const int64_t ldx = ld_hidden == 0 ? h : ld_hidden;
+  const int64_t ldw = ld_weight == 0 ? h : ld_weight;
+  if (ldx < h || ldw < h) return VPCE_ERR_INVALID_ARG;
+  if (s > 0) {
+    if (hidden == nullptr || targets == nullptr) return VPCE_ERR_INVALID_ARG;
+    for (int i = 0; i < t; ++i)
+      if (weight_shards[i] == nullptr) return VPCE_ERR_INVALID_ARG;
+  }
+  // the tensor-memory-access engine: 16-byte aligned bases and row strides
+  if ((hidden != nullptr && !aligned(hidden, 16)) || (ldx * 2) % 16 != 0 || (ldw * 2) % 16 != 0)
+    return VPCE_ERR_ALIGNMENT;
+  for (int i = 0; i < t; ++i)
+    if (weight_shards[i] != nullptr && !aligned(weight_shards[i], 16)) return VPCE_ERR_ALIGNMENT;
+  if (targets != nullptr && !aligned(targets, 8)) return VPCE_ERR_ALIGNMENT;
+  vpce_status st = check_outputs(reduction, s, loss_out, row_loss_out);
+  if (st != VPCE_OK) return st;
+  if (workspace == nullptr) return VPCE_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return VPCE_ERR_ALIGNMENT;
+  if (workspace_bytes < WsLayout(VPCE_LMHEAD_MAX_GROUPS, s).total) return VPCE_ERR_WORKSPACE;
+  int sms = 0;
+  st = device_setup(&sms);
+  if (st != VPCE_OK) return st;
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  Header* hdr = reinterpret_cast<Header*>(ws);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int groups = 1;
+  // partials go where the sharded loss keeps them, [groups][s] (the layout of
+  // WsLayout(VPCE_LMHEAD_MAX_GROUPS, s) holds up to that many groups)
+  const WsLayout L(VPCE_LMHEAD_MAX_GROUPS, s);
+  if (s > 0) {
+    const int g_sms = sms < VPCE_LMHEAD_MAX_GROUPS ? sms : VPCE_LMHEAD_MAX_GROUPS;
+    if (!launch_gemm_stats(hidden, ldx, weight_shards, ldw, t, s, h, reinterpret_cast<const long long*>(vocab_start),
+                           reinterpret_cast<const long long*>(targets), ignore_index,
+                           reinterpret_cast<float2*>(ws + L.part), reinterpret_cast<float*>(ws + L.tgt), hdr, g_sms,
+                           &groups, cs))
+      return VPCE_ERR_CUDA;
+    if ((st = launch_status()) != VPCE_OK) return st;
+  }
+  CombineParams c;
+  c.s = s;
+  c.t = groups;
+  c.V = vocab_start[t];
+  c.targets = reinterpret_cast<const long long*>(targets);
+  c.ignore_index = ignore_index;
+  c.reduction = int(reduction);
+  c.part = reinterpret_cast<const float2*>(ws + L.part);
+  c.tgt = reinterpret_cast<const float*>(ws + L.tgt);
+  c.lse = reinterpret_cast<float*>(ws + L.lse);
+  c.bsum = reinterpret_cast<double*>(ws + L.bsum);
+  c.bcnt = reinterpret_cast<int*>(ws + L.bcnt);
+  c.loss_out = loss_out;
+  c.row_loss = row_loss_out;
+  c.hdr = hdr;
+  const long long blocks = s > 0 ? (s + kCombineThreads - 1) / kCombineThreads : 1;
+  launch_combine(c, int(blocks), cs);
+  return launch_status();
 }
 
 const char* vpce_status_string(vpce_status status) {

@@ -1,0 +1,483 @@
+// LM-head GEMM fused with the vocab-parallel cross-entropy statistics: the
+// logits z = X W_i^T of every vocabulary shard are formed tile by tile on the
+// tensor cores and reduced to per-row (max, sum of exponentials) partials and
+// the target logit in the tile's epilogue, so the [s, V] logits are never
+// written.  This is the pages' "do not assemble the big tensor, move the
+// later computation to where the data is" ("Distributed Training III: Model
+// Parallelism", CMU 11-868 Lecture 16 notes, §5.5), applied one step earlier
+// than the sharded loss: the LM head is [V, h] split along V ("LLM Internals"
+// §7.3.4: [128256, 8192], 16032 rows per card at t = 8).
+//
+// Kernel shape (sm_100 family, one CTA per SM, persistent):
+//   warp 0      one lane issues the TMA loads: a 128 x 64 tile of X and a
+//               256 x 64 tile of W_i per K step, 128-byte swizzled, into a
+//               4-stage shared-memory ring (mbarrier full / empty);
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32
+//               accumulators); one lane issues tcgen05.mma (kind::f16, bf16
+//               in, fp32 accumulate, M = 128, N = 256, K = 16 per
+//               instruction) and commits each stage back to the loader and
+//               each finished accumulator to the epilogue;
+//   warps 2..5  the epilogue: each thread owns one row (one TMEM lane),
+//               reads the row's 256 fp32 values with tcgen05.ld, masks the
+//               columns past the shard's end, folds them into a running
+//               (max, sum exp) and picks up the target logit when the
+//               row's target column falls in the tile.
+// CTA c takes M tile (wave * gm + c % gm) and the N tiles of group c / gm, for
+// every wave: the gm CTAs of a group read the same W tile at the same time
+// (L2 hits), and the gn CTAs of an M tile read the same X tile.  Each CTA
+// writes one partial per row and group; the combine kernel of the sharded
+// loss folds them in group order.
+#include <cuda.h>
+
+#include <cstring>
+
+#include "vpce_kernels.cuh"
+
+namespace vpce {
+
+namespace {
+
+constexpr int kBM = 128;   // rows (tokens) per tile
+constexpr int kBN = 256;   // vocabulary columns per tile
+constexpr int kBK = 64;    // K elements per stage (one 128-byte swizzle atom of bf16)
+constexpr int kUK = 16;    // K per tcgen05.mma for 16-bit inputs
+constexpr int kGStages = 4;
+constexpr int kATile = kBM * kBK * 2;  // 16 KB
+constexpr int kBTile = kBN * kBK * 2;  // 32 KB
+constexpr int kGStage = kATile + kBTile;
+constexpr int kGThreads = 192;  // 6 warps
+constexpr int kTmemCols = 512;  // two accumulators of kBN fp32 columns
+constexpr int kMaxGemmShards = 32;
+constexpr int kMaxGroupsPerWave = 8;  // M tiles that share a W tile
+
+struct GemmSmem {
+  unsigned char stage[kGStages][kGStage];  // 1024-byte aligned (swizzle atoms)
+  uint64_t full[kGStages];
+  uint64_t empty[kGStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct GemmParams {
+  CUtensorMap tmx;                  // X [s, h] bf16, box 64 x 128
+  CUtensorMap tmw[kMaxGemmShards];  // W_i [w_i, h] bf16, box 64 x 256
+  int t;
+  int s;
+  int k_steps;                      // h / 64
+  int m_tiles, n_tiles, gm, gn;
+  int vstart[kMaxGemmShards + 1];   // global column of each shard's first row
+  int nstart[kMaxGemmShards + 1];   // first N tile of each shard
+  const long long* targets;
+  long long ignore_index;
+  float2* part;                     // [gn][s]: (max, sum exp) of the group's columns
+  float* tgt;                       // [s]: target logit
+  Header* hdr;
+};
+
+// ---------------------------------------------------------------------------
+// inline PTX: TMA tiles, tcgen05
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile stored as 128-byte rows
+// with the 128-byte swizzle: start address, stride of 8-row groups 1024 B,
+// descriptor version 1, layout type 2 (128B swizzle).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t(1u) << 16;             // leading byte offset (unused for swizzled K-major)
+  d |= uint64_t(1024u >> 4) << 32;     // stride byte offset
+  d |= uint64_t(1u) << 46;             // version
+  d |= uint64_t(2u) << 61;             // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = kBN, M = kBM.
+constexpr uint32_t kIdesc = (1u << 4)                       // D format f32
+                            | (1u << 7)                     // A bf16
+                            | (1u << 10)                    // B bf16
+                            | (uint32_t(kBN >> 3) << 17)    // N / 8
+                            | (uint32_t(kBM >> 4) << 24);   // M / 16
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.  The load and its
+// wait sit in one asm statement, so no use of the registers can be scheduled
+// before the data has arrived.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ int ld_abort(const int* f) { return *const_cast<const volatile int*>(f); }
+
+// Single-thread bounded wait that also gives up once another role aborted.
+__device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t parity, const int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (ld_abort(abort_flag) || clock64() - t0 > kWaitLimitCycles) return false;
+  }
+}
+
+// Warp-uniform bounded wait with the same abort check.
+__device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t parity, const int* abort_flag) {
+  if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+    if (__any_sync(kFull, ld_abort(abort_flag) != 0 || clock64() - t0 > kWaitLimitCycles)) return false;
+  }
+}
+
+__device__ __forceinline__ int shard_of_tile(const GemmParams& p, int nt) {
+  int i = 0;
+  while (p.nstart[i + 1] <= nt) ++i;
+  return i;
+}
+
+__global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  GemmSmem& sm = *reinterpret_cast<GemmSmem*>(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kGStages; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_empty[b], 4);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+    if (blockIdx.x == 0) {
+      p.hdr->ticket = 0u;
+      p.hdr->error_flag = 0;
+    }
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  const int m_slot = int(blockIdx.x) % p.gm;
+  const int grp = int(blockIdx.x) / p.gm;
+  const int nt0 = int((long long)grp * p.n_tiles / p.gn);
+  const int nt1 = int((long long)(grp + 1) * p.n_tiles / p.gn);
+  const int waves = (p.m_tiles + p.gm - 1) / p.gm;
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      unsigned issued = 0;
+      bool ok = true;
+      for (int wv = 0; wv < waves && ok; ++wv) {
+        const int mt = wv * p.gm + m_slot;
+        if (mt >= p.m_tiles) break;
+        for (int nt = nt0; nt < nt1 && ok; ++nt) {
+          const int sh = shard_of_tile(p, nt);
+          const int n_off = (nt - p.nstart[sh]) * kBN;
+          for (int kb = 0; kb < p.k_steps; ++kb) {
+            const int st = int(issued % kGStages);
+            if (!wait1(&sm.empty[st], ((issued / kGStages) & 1u) ^ 1u, &sm.abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.full[st], kGStage);
+            tma_load_2d(sm.stage[st], &p.tmx, kb * kBK, mt * kBM, &sm.full[st]);
+            tma_load_2d(sm.stage[st] + kATile, &p.tmw[sh], kb * kBK, n_off, &sm.full[st]);
+            ++issued;
+          }
+        }
+      }
+      if (!ok) {
+        sm.abort_flag = 1;
+        atomicOr(&p.hdr->error_flag, VPCE_FLAG_WAIT_TIMEOUT);
+        // the copies still in flight land in shared memory before the CTA exits
+        const unsigned first = issued > unsigned(kGStages) ? issued - kGStages : 0u;
+        for (unsigned j = first; j < issued; ++j) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(&sm.full[j % kGStages], (j / kGStages) & 1u) && clock64() - t0 < kWaitLimitCycles) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      unsigned consumed = 0, tiles = 0, issued_any = 0;
+      bool ok = true;
+      for (int wv = 0; wv < waves && ok; ++wv) {
+        const int mt = wv * p.gm + m_slot;
+        if (mt >= p.m_tiles) break;
+        for (int nt = nt0; nt < nt1 && ok; ++nt) {
+          const int b = int(tiles & 1u);
+          if (!wait1(&sm.acc_empty[b], ((tiles >> 1) & 1u) ^ 1u, &sm.abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + uint32_t(b * kBN);
+          for (int kb = 0; kb < p.k_steps; ++kb) {
+            const int st = int(consumed % kGStages);
+            if (!wait1(&sm.full[st], (consumed / kGStages) & 1u, &sm.abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_addr(sm.stage[st]);
+            const uint32_t b0 = a0 + kATile;
+#pragma unroll
+            for (int kk = 0; kk < kBK / kUK; ++kk)
+              umma_bf16(d, sw128_desc(a0 + kk * kUK * 2), sw128_desc(b0 + kk * kUK * 2), (kb | kk) != 0);
+            issued_any = 1;
+            umma_commit(&sm.empty[st]);  // the stage is free once these MMAs have read it
+            ++consumed;
+          }
+          if (!ok) break;
+          umma_commit(&sm.acc_full[b]);  // the accumulator is complete
+          ++tiles;
+        }
+      }
+      if (!ok) {
+        sm.abort_flag = 1;
+        atomicOr(&p.hdr->error_flag, VPCE_FLAG_WAIT_TIMEOUT);
+      }
+      if (issued_any) {  // every MMA has finished before the TMEM is released
+        umma_commit(&sm.drain);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&sm.drain, 0u) && clock64() - t0 < kWaitLimitCycles) {
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue: one row per thread
+    const int q = warp & 3;  // the TMEM lane quarter this warp may access
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t lane_addr = tmem + (uint32_t(q * 32) << 16);
+    unsigned tiles = 0;
+    bool ok = true;
+    for (int wv = 0; wv < waves && ok; ++wv) {
+      const int mt = wv * p.gm + m_slot;
+      if (mt >= p.m_tiles) break;
+      const int r = mt * kBM + row_in_tile;
+      const bool live = r < p.s;
+      long long y = live ? __ldg(p.targets + r) : -1;
+      float m = -INFINITY, se = 0.f, zt = 0.f;
+      bool has_t = false;
+      for (int nt = nt0; nt < nt1; ++nt) {
+        const int b = int(tiles & 1u);
+        if (!waitw(&sm.acc_full[b], (tiles >> 1) & 1u, &sm.abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int sh = shard_of_tile(p, nt);
+        const int col0 = (nt - p.nstart[sh]) * kBN;
+        const int width = p.vstart[sh + 1] - p.vstart[sh];
+        const int valid = min(kBN, width - col0);
+        const long long tc = y - (long long)p.vstart[sh] - col0;  // target column inside this tile
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          if (c * 32 >= valid) break;  // warp-uniform
+          float v[32];
+          tmem_ld32(lane_addr + uint32_t(b * kBN + c * 32), v);
+          const int lim = valid - c * 32;
+          const long long rel = tc - c * 32;
+          if (rel >= 0 && rel < 32 && rel < lim) {
+            // the target logit: a sum of products with 0/1 weights picks it
+            // without a run-time index into the registers (exact: one term
+            // is 1 * z, the rest are 0 * finite)
+            float pick = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) pick = fmaf(j == int(rel) ? 1.f : 0.f, v[j], pick);
+            zt = pick;
+            has_t = true;
+          }
+          float cm = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j >= lim) v[j] = -INFINITY;
+            cm = fmaxf(cm, v[j]);
+          }
+          if (cm > m) {
+            se *= ex2((m - cm) * kLog2e);
+            m = cm;
+          }
+          const float nb = -m * kLog2e;
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            a0 += ex2(fmaf(v[j], kLog2e, nb));
+            a1 += ex2(fmaf(v[j + 1], kLog2e, nb));
+          }
+          se += a0 + a1;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_local(&sm.acc_empty[b]);
+        ++tiles;
+      }
+      if (!ok) break;
+      if (live) {
+        p.part[(long long)grp * p.s + r] = make_float2(m, se);
+        if (has_t) p.tgt[r] = zt;
+      }
+    }
+    if (!ok && lane == 0) {
+      sm.abort_flag = 1;
+      atomicOr(&p.hdr->error_flag, VPCE_FLAG_WAIT_TIMEOUT);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library; resolved once).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      f = nullptr;
+    }
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// A [rows, h] bf16 row-major matrix (row stride ld elements) as a 2-D tensor
+// map with a box of 64 columns x box_rows rows and the 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long h, long long ld, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(h), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(ld) * 2u};
+  const cuuint32_t box[2] = {cuuint32_t(kBK), cuuint32_t(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int gemm_max_shards() { return kMaxGemmShards; }
+int gemm_max_groups(int sms) { return sms > 0 ? sms : 1; }
+
+cudaError_t set_gemm_smem() {
+  return cudaFuncSetAttribute(gemm_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(sizeof(GemmSmem)));
+}
+
+// The grid of the fused LM-head kernel for s rows and n_tiles N tiles on sms
+// SMs: gm M tiles per wave share each W tile, gn groups split the N tiles.
+void gemm_grid(long long s, int n_tiles, int sms, int* gm, int* gn) {
+  const int m_tiles = int((s + kBM - 1) / kBM);
+  int a = m_tiles < kMaxGroupsPerWave ? m_tiles : kMaxGroupsPerWave;
+  if (a < 1) a = 1;
+  int b = sms / a;
+  if (b > n_tiles) b = n_tiles;
+  if (b < 1) b = 1;
+  *gm = a;
+  *gn = b;
+}
+
+int gemm_n_tiles(const long long* vocab_start, int t) {
+  int n = 0;
+  for (int i = 0; i < t; ++i) n += int((vocab_start[i + 1] - vocab_start[i] + kBN - 1) / kBN);
+  return n;
+}
+
+// Encodes the tensor maps and launches the kernel; returns false when a
+// tensor map cannot be encoded (the launch status is the caller's to read).
+bool launch_gemm_stats(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
+                       long long h, const long long* vocab_start, const long long* targets, long long ignore_index,
+                       float2* part, float* tgt, Header* hdr, int sms, int* groups, cudaStream_t st) {
+  static_assert(sizeof(GemmParams) < 32000, "kernel parameter block");
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!make_map(&p.tmx, x, s, h, ld_x, kBM)) return false;
+  p.nstart[0] = 0;
+  for (int i = 0; i < t; ++i) {
+    const long long wi = vocab_start[i + 1] - vocab_start[i];
+    if (!make_map(&p.tmw[i], w[i], wi, h, ld_w, kBN)) return false;
+    p.vstart[i] = int(vocab_start[i]);
+    p.nstart[i + 1] = p.nstart[i] + int((wi + kBN - 1) / kBN);
+  }
+  p.vstart[t] = int(vocab_start[t]);
+  p.t = t;
+  p.s = int(s);
+  p.k_steps = int(h / kBK);
+  p.m_tiles = int((s + kBM - 1) / kBM);
+  p.n_tiles = p.nstart[t];
+  gemm_grid(s, p.n_tiles, sms, &p.gm, &p.gn);
+  p.targets = targets;
+  p.ignore_index = ignore_index;
+  p.part = part;
+  p.tgt = tgt;
+  p.hdr = hdr;
+  *groups = p.gn;
+  gemm_stats_kernel<<<p.gm * p.gn, kGThreads, sizeof(GemmSmem), st>>>(p);
+  return true;
+}
+
+}  // namespace vpce

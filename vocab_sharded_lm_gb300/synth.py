@@ -295,3 +295,96 @@ def device_shards(w: Workload, meta: RowMeta, vocab_start=None, ld=None, device=
     torch.cuda.current_stream(device).synchronize()
     del boost
     return out
+
+
+# --------------------------------------------------------------------------
+# LM-head inputs: hidden states X [s, h] and the vocabulary-sharded head
+# W [V, h] (one row per vocabulary entry), both bf16, drawn element by
+# element from their own streams of the same generator.
+# --------------------------------------------------------------------------
+STREAM_HIDDEN = 5
+STREAM_WEIGHT = 6
+
+
+@dataclasses.dataclass(frozen=True)
+class LmHead:
+    name: str
+    index: int              # seed = 20261202 + index
+    s: int                  # rows (tokens)
+    h: int                  # hidden size (K of the contraction)
+    V: int                  # vocabulary
+    t: int                  # shards
+    sigma_x: float = 1.0    # X ~ N(0, sigma_x^2)
+    logit_sigma: float = 3.0  # W ~ N(0, (logit_sigma / sqrt(h))^2): logits ~ N(0, logit_sigma^2)
+    ignore_frac: float = 0.0
+    ignore_index: int = -100
+
+    @property
+    def seed(self) -> int:
+        return 20261202 + self.index
+
+    @property
+    def sigma_w(self) -> float:
+        return self.logit_sigma / float(np.sqrt(self.h))
+
+    def replace(self, **kw) -> "LmHead":
+        return dataclasses.replace(self, **kw)
+
+    def as_workload(self) -> Workload:
+        """The loss-side recipe with the same rows, vocabulary and targets."""
+        return Workload(self.name, self.index, self.s, self.V, self.t, "bf16", self.logit_sigma, "uniform",
+                        ignore_frac=self.ignore_frac, ignore_index=self.ignore_index)
+
+
+LMHEADS = {
+    m.name: m for m in [
+        # the pages' Llama-3-70B LM head: [128256, 8192], t = 8, s = 8192
+        LmHead("lmhead_s8192_h8192_v128256", 6, 8192, 8192, 128256, 8),
+        LmHead("lmhead_s300_h512_v5000", 7, 300, 512, 5000, 3, ignore_frac=0.05),
+    ]
+}
+LMHEAD_BENCH = "lmhead_s8192_h8192_v128256"
+
+
+def dense_host(seed: int, stream: int, rows, cols: int, sigma: float) -> np.ndarray:
+    """bf16 patterns (uint16) of rows ``rows`` of a [*, cols] matrix whose
+    element (r, c) is the generator's normal number r * cols + c of the
+    stream, times sigma, rounded to binary32 and then to bfloat16."""
+    rows = np.asarray(rows, dtype=np.int64)
+    key = stream_key(seed, stream)
+    g = rows[:, None].astype(np.uint64) * np.uint64(cols) + np.arange(cols, dtype=np.uint64)[None, :]
+    v = (_normals_from_index(key, g) * sigma).astype(np.float32)
+    return f32_to_bf16_bits(v)
+
+
+def lmhead_meta(m: LmHead) -> RowMeta:
+    return row_meta(m.as_workload())
+
+
+def _dense_device(buf, seed: int, stream: int, row0: int, cols: int, sigma: float) -> None:
+    import ctypes
+    import torch
+
+    key = int(stream_key(seed, stream))
+    st = torch.cuda.current_stream(buf.device).cuda_stream
+    err = _synth_lib().vpce_synth_fill(ctypes.c_void_p(buf.data_ptr()), 1, buf.shape[0], row0, 0, cols,
+                                       buf.stride(0), cols, key, float(sigma), None, 0.0, ctypes.c_void_p(st))
+    if err != 0:
+        raise RuntimeError(f"vpce_synth_fill failed with CUDA error {err}")
+
+
+def lmhead_device(m: LmHead, vocab_start=None, device="cuda"):
+    """Device X [s, h] and the t weight shards [w_i, h] (bf16), filled by the
+    device twin of the generator (the values of :func:`dense_host`)."""
+    import torch
+
+    vs = even_vocab_start(m.V, m.t) if vocab_start is None else list(vocab_start)
+    x = torch.empty((m.s, m.h), dtype=torch.bfloat16, device=device)
+    _dense_device(x, m.seed, STREAM_HIDDEN, 0, m.h, m.sigma_x)
+    ws = []
+    for i in range(len(vs) - 1):
+        wi = torch.empty((vs[i + 1] - vs[i], m.h), dtype=torch.bfloat16, device=device)
+        _dense_device(wi, m.seed, STREAM_WEIGHT, vs[i], m.h, m.sigma_w)
+        ws.append(wi)
+    torch.cuda.current_stream(device).synchronize()
+    return x, ws

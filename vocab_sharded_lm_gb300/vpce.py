@@ -31,6 +31,7 @@ VPCE_MAX_SHARDS = 64
 VPCE_FLAG_BAD_TARGET = 1
 VPCE_FLAG_WAIT_TIMEOUT = 2
 VPCE_STATIC_SCRATCH_BYTES = 8 * 1024 * 1024
+VPCE_LMHEAD_MAX_GROUPS = 256
 
 _lib = None
 _lock = threading.Lock()
@@ -79,6 +80,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.vpce_forward_static.restype = ctypes.c_int
         lib.vpce_forward_static.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
                                             ctypes.c_int, _P, _P, _P]
+        lib.vpce_lmhead_workspace_bytes.restype = ctypes.c_size_t
+        lib.vpce_lmhead_workspace_bytes.argtypes = [_I64]
+        lib.vpce_lmhead_forward.restype = ctypes.c_int
+        lib.vpce_lmhead_forward.argtypes = [_P, _I64, _P, _I64, ctypes.c_int, _I64, _I64, _I64P, _P, _I64,
+                                            ctypes.c_int, _P, _P, _P, ctypes.c_size_t, _P]
         lib.vpce_read_error_flag.restype = ctypes.c_int
         lib.vpce_read_error_flag.argtypes = [_P, ctypes.POINTER(ctypes.c_int), _P]
         lib.vpce_status_string.restype = ctypes.c_char_p
@@ -376,3 +382,60 @@ def vpce_forward_static(shards, targets, loss_out, vocab_start=None, *, ignore_i
         raise VPCEError(code, "vpce_forward_static")
     return loss_out
 
+
+
+# ----------------------------------------------------------------------------
+# LM-head GEMM fused with the forward loss (the logits are never written)
+# ----------------------------------------------------------------------------
+def vpce_lmhead_workspace_bytes(s: int) -> int:
+    return int(load_library().vpce_lmhead_workspace_bytes(int(s)))
+
+
+def lmhead_forward_raw(hidden_ptr, ld_hidden, weight_ptrs, ld_weight, t, s, h, vocab_start, targets_ptr,
+                       ignore_index, reduction, loss_ptr, row_loss_ptr, ws_ptr, ws_bytes, stream) -> int:
+    lib = load_library()
+    ptrs = _ptr_array(weight_ptrs) if weight_ptrs is not None else None
+    vs = _i64_array(vocab_start) if vocab_start is not None else None
+    return int(lib.vpce_lmhead_forward(hidden_ptr, int(ld_hidden), ctypes.cast(ptrs, _P) if ptrs is not None else None,
+                                       int(ld_weight), int(t), int(s), int(h), vs, targets_ptr, int(ignore_index),
+                                       int(reduction), loss_ptr, row_loss_ptr, ws_ptr, int(ws_bytes), stream))
+
+
+def vpce_lmhead_forward(hidden, weight_shards, targets, vocab_start=None, *, ignore_index: int = -100,
+                        reduction: str = "mean", loss_out=None, row_loss_out=None, workspace=None, stream=None):
+    """Loss of the logits ``hidden @ W_i^T`` of every vocabulary shard, formed
+    and reduced tile by tile on the tensor cores.  ``hidden``: CUDA bf16
+    ``[s, h]``; ``weight_shards``: CUDA bf16 ``[w_i, h]`` sharing one row
+    stride.  Returns ``(loss, workspace)`` (the per-row vector for 'none')."""
+    import torch
+
+    if hidden.dtype != torch.bfloat16 or hidden.dim() != 2 or not hidden.is_cuda or hidden.stride(1) != 1:
+        raise ValueError("hidden must be a CUDA bf16 [s, h] tensor with contiguous columns")
+    s, h = hidden.shape
+    if not weight_shards:
+        raise ValueError("need at least one weight shard")
+    for w in weight_shards:
+        if w.dtype != torch.bfloat16 or w.dim() != 2 or not w.is_cuda or w.shape[1] != h or w.stride(1) != 1:
+            raise ValueError("weight shards must be CUDA bf16 [w_i, h] tensors with contiguous columns")
+    strides = {w.stride(0) for w in weight_shards if w.shape[0] > 1}
+    if len(strides) > 1:
+        raise ValueError("weight shards must share one row stride")
+    ld_w = strides.pop() if strides else h
+    ld_x = hidden.stride(0) if s > 1 else h
+    if vocab_start is None:
+        vocab_start = [0]
+        for w in weight_shards:
+            vocab_start.append(vocab_start[-1] + w.shape[0])
+    if targets.dtype != torch.int64 or not targets.is_cuda or targets.numel() != s:
+        raise ValueError("targets must be a CUDA int64 tensor with one entry per row")
+    dev = hidden.device
+    if workspace is None:
+        workspace = torch.empty(vpce_lmhead_workspace_bytes(s), dtype=torch.uint8, device=dev)
+    red, loss_out, row_loss_out, result = _outputs(reduction, loss_out, row_loss_out, s, dev)
+    code = lmhead_forward_raw(ctypes.c_void_p(hidden.data_ptr()), ld_x, [w.data_ptr() for w in weight_shards],
+                              ld_w, len(weight_shards), s, h, vocab_start, ctypes.c_void_p(targets.data_ptr()),
+                              ignore_index, red, _ptr(loss_out), _ptr(row_loss_out),
+                              ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+    if code != VPCE_OK:
+        raise VPCEError(code, "vpce_lmhead_forward")
+    return result, workspace
