@@ -55,6 +55,8 @@ __all__ = [
     "shard_partials",
     "combine_sharded",
     "lmhead_logits",
+    "embedding_forward",
+    "embedding_backward",
 ]
 
 
@@ -231,6 +233,57 @@ def lmhead_logits(x, w_shards, vocab_start, dtype: str = "bf16") -> np.ndarray:
             raise ValueError(f"shard {i} has shape {W.shape}")
         z[:, vs[i]:vs[i + 1]] = X @ W.T
     return z
+
+
+# --------------------------------------------------------------------------
+# the vocabulary-parallel input embedding
+# --------------------------------------------------------------------------
+def embedding_forward(table_shards, vocab_start, ids, dtype: str = "bf16"):
+    """Output rows of a vocabulary-split embedding table, in fp64.
+
+    "Distributed Training III: Model Parallelism" (CMU 11-868 Lecture 16
+    notes), §5.5: card i holds only the embeddings of the ids in its range,
+    fills every other position with zeros, and an all-reduce sums the cards.
+    "LLM Internals" §7.3.4: the table [128256, 8192] is split into [16032,
+    8192] per card, ids outside a card's range give zero vectors there.
+    Written out in that order: card i's masked lookup, then the sum over
+    cards.  An id outside [0, V) is in no card's range, so its row is zero;
+    ``bad`` reports whether any id was.  Returns ``(out [s, h], bad)``.
+    """
+    vs = [int(v) for v in vocab_start]
+    ids = np.asarray(ids, dtype=np.int64)
+    shards = [widen(e, dtype) for e in table_shards]
+    h = shards[0].shape[1]
+    out = np.zeros((ids.size, h))
+    for i, e in enumerate(shards):
+        mine = (ids >= vs[i]) & (ids < vs[i + 1])
+        part = np.zeros((ids.size, h))
+        part[mine] = e[ids[mine] - vs[i]]
+        out += part
+    bad = bool(np.any((ids < 0) | (ids >= vs[-1])))
+    return out, bad
+
+
+def embedding_backward(grad_out, ids, vocab_start, h: int):
+    """Gradient of the embedding lookup with respect to each table shard, fp64.
+
+    The pages give no backward.  The standard one is the adjoint of the
+    lookup: row j of shard i receives the sum of the output gradients of the
+    positions whose id is ``vocab_start[i] + j``.  Ids outside [0, V) send
+    their gradient nowhere, matching their zero output rows.  ``grad_out`` is
+    ``[s, h]`` fp64.  Returns the list of shard gradients ``[w_i, h]``.
+    """
+    vs = [int(v) for v in vocab_start]
+    ids = np.asarray(ids, dtype=np.int64)
+    g = np.asarray(grad_out, dtype=np.float64)
+    out = []
+    for i in range(len(vs) - 1):
+        d = np.zeros((vs[i + 1] - vs[i], h))
+        mine = np.nonzero((ids >= vs[i]) & (ids < vs[i + 1]))[0]
+        for r in mine:
+            d[ids[r] - vs[i]] += g[r]
+        out.append(d)
+    return out
 
 
 # --------------------------------------------------------------------------

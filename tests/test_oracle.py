@@ -256,6 +256,48 @@ def test_lmhead_matches_torch_linear_and_cross_entropy():
     np.testing.assert_allclose(z, z1, rtol=1e-14, atol=1e-14)
 
 
+# ---------------------------------------------------------------- embedding
+def test_embedding_forward_matches_torch_embedding():
+    rng = np.random.default_rng(5)
+    V, h, s = 300, 24, 50
+    E = _bf16(rng.normal(size=(V, h)))
+    vs = [0, 7, 150, 300]
+    ids = rng.integers(0, V, size=s)
+    ids[:4] = [0, 6, 7, 299]           # shard edges
+    out, bad = O.embedding_forward([E[vs[i]:vs[i + 1]] for i in range(3)], vs, ids)
+    ref = torch.nn.functional.embedding(torch.tensor(ids), torch.tensor(O.widen(E, "bf16")))
+    np.testing.assert_array_equal(out, ref.numpy())
+    assert not bad
+
+
+def test_embedding_forward_out_of_range_ids_give_zero_rows():
+    E = _bf16(np.arange(40, dtype=np.float32).reshape(10, 4) + 1.0)
+    out, bad = O.embedding_forward([E[:3], E[3:]], [0, 3, 10], np.array([2, -1, 10, 3, 1000]))
+    assert bad
+    np.testing.assert_array_equal(out[[1, 2, 4]], 0.0)
+    np.testing.assert_array_equal(out[0], O.widen(E, "bf16")[2])
+    np.testing.assert_array_equal(out[3], O.widen(E, "bf16")[3])
+
+
+def test_embedding_backward_matches_torch_autograd():
+    rng = np.random.default_rng(6)
+    V, h, s = 40, 8, 200               # many repeated ids
+    vs = [0, 13, 14, 40]
+    ids = rng.integers(0, V, size=s)
+    g = rng.normal(size=(s, h))
+    E = torch.zeros((V, h), dtype=torch.float64, requires_grad=True)
+    torch.nn.functional.embedding(torch.tensor(ids), E).backward(torch.tensor(g))
+    got = O.embedding_backward(g, ids, vs, h)
+    np.testing.assert_allclose(np.concatenate(got), E.grad.numpy(), rtol=1e-13, atol=1e-13)
+
+
+def test_embedding_backward_drops_out_of_range_ids():
+    g = np.ones((3, 2))
+    got = O.embedding_backward(g, np.array([-5, 1, 4]), [0, 2, 4], 2)
+    np.testing.assert_array_equal(got[0], [[0, 0], [1, 1]])
+    np.testing.assert_array_equal(got[1], [[0, 0], [0, 0]])
+
+
 def test_bf16_widening_exact():
     bits = np.array([0x3F80, 0xC000, 0x4049, 0x0000, 0x8000, 0x7F7F, 0x0001, 0xBF00], dtype=np.uint16)
     got = O.widen(bits, "bf16")
