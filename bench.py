@@ -705,6 +705,172 @@ def run_lmhead(args):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------
+# the vocabulary-parallel input embedding (forward + backward)
+# ----------------------------------------------------------------------------
+EMBED_METRIC = "vocab-parallel embedding fwd+bwd tokens/s & HBM GB/s (% of peak), s=8192 h=8192 V=128256 bf16, 1 GB300"
+
+
+def run_embedding(args):
+    import torch
+
+    from vocab_sharded_lm_gb300 import _build, vpce
+    from oracle import vpce_oracle as O
+
+    rank, world, local = _env_rank()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    vpce.load_library()
+    V, h, t = 128256, 8192, 8
+    s = args.rows or 8192
+    vs = synth.even_vocab_start(V, t)
+    idw = synth.Workload("embedding_ids", 6, s, V, 1, "bf16", 1.0, "zipf1.1")
+    ids_host = synth.row_meta(idw).targets
+    ids = torch.from_numpy(ids_host).to(dev)
+    tab = synth.table_device(idw.seed, vs, h, device=dev)
+    gout = synth.grad_device(idw.seed, s, h, device=dev)
+    grads = [torch.zeros((vs[i + 1] - vs[i], h), dtype=torch.float32, device=dev) for i in range(t)]
+    out = torch.empty((s, h), dtype=torch.bfloat16, device=dev)
+    wk = torch.empty(vpce.vpce_embedding_backward_workspace_bytes(), dtype=torch.uint8, device=dev)
+    flag = torch.zeros((), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        vpce.vpce_embedding_forward(tab, ids, vs, out=out, flag=flag)
+        if ev:
+            ev[1].record(stream)
+        vpce.vpce_embedding_backward(gout, ids, grads, vs, workspace=wk)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = _max_over_ranks(t0.elapsed_time(t1), dev)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+
+    # end to end: ids and the output gradient copied in each step, the flag read back
+    h_ids = torch.from_numpy(ids_host).pin_memory()
+    h_g = gout.cpu().pin_memory()
+    n_e2e = max(1, args.e2e_steps)
+    h_flag = torch.empty(n_e2e, dtype=torch.int32).pin_memory()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(n_e2e):
+        ids.copy_(h_ids, non_blocking=True)
+        gout.copy_(h_g, non_blocking=True)
+        step()
+        h_flag[k].copy_(flag, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    uniq = int(np.unique(ids_host[(ids_host >= 0) & (ids_host < V)]).size)
+    fwd_bytes = 2 * s * h * 2 + 8 * s
+    bwd_bytes = s * h * 2 + 2 * uniq * h * 4 + 8 * s
+    peak, kind = _peaks()
+    ms_step = total_ms / args.steps
+    achieved = (fwd_bytes + bwd_bytes) / ((fwd_ms + bwd_ms) * 1e-3) / 1e9
+    out_line = {
+        "metric": EMBED_METRIC,
+        "value": round(_weak_scaling_value(s * args.steps, world, total_ms), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; no dataset or trained weights)",
+        "config": {
+            "workload": f"table [{V}, {h}] bf16 in t={t} vocabulary shards, {s} ids Zipf(1.1) ({uniq} distinct), "
+                        f"output gradient [{s}, {h}] bf16, fp32 gradient table",
+            "global_batch": s * world,
+            "seq_len": s,
+            "parallelism": f"vocab shards t={t} on one GPU; {world} independent replica(s)",
+            "l2": "the table (2.10 GB) and gradient table (4.20 GB) are larger than L2; the rows one step touches "
+                  "(128 MB out, 128 MB gradient) are re-read by the next step only in part",
+            "path": "vpce_embedding_forward (row gather) + vpce_embedding_backward (sort, per-id sums, fp32 add)",
+        },
+        "fwd_ms": round(fwd_ms, 5),
+        "bwd_ms": round(bwd_ms, 5),
+        "roofline": {
+            "kernel": "embed_forward_kernel + embed_sort_kernel + embed_accum_kernel",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": None,
+            "algorithmic_bytes_per_step": fwd_bytes + bwd_bytes,
+            "note": "forward: the gathered rows read and written; backward: the gradient rows read and the "
+                    "distinct ids' fp32 rows read and written",
+        },
+        "e2e": {
+            "value": round(_weak_scaling_value(s, world, e2e_ms), 1),
+            "unit": "tokens/s",
+            "h2d_bytes_per_step": int(s * 8 + s * h * 2),
+            "d2h_bytes_per_step": 4,
+            "steps": n_e2e,
+            "ms_per_step": round(e2e_ms, 4),
+            "note": "pinned host ids and output gradient copied in every step, the id flag read back; the "
+                    "tables stay on the device",
+        },
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        rows = np.arange(min(s, 512))
+        tab_host = [e.view(torch.int16).cpu().numpy().view(np.uint16) for e in tab]
+        g_host = O.widen(gout[:len(rows)].view(torch.int16).cpu().numpy().view(np.uint16), "bf16")
+        t_start = time.perf_counter()
+        n_done = 0
+        while time.perf_counter() - t_start < args.cpu_seconds:
+            O.embedding_forward(tab_host, vs, ids_host[rows])
+            O.embedding_backward(g_host, ids_host[rows], vs, h)
+            n_done += len(rows)
+        dt = time.perf_counter() - t_start
+        out_line["cpu_baseline"] = {"value": round(n_done / dt, 2), "unit": "tokens/s", "cores": 1,
+                                    "kind": "oracle",
+                                    "sample": f"{n_done} ids (batches of {len(rows)}), fp64 numpy forward + "
+                                              f"backward on one host core, {dt:.1f} s"}
+    print(json.dumps(out_line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -717,9 +883,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=["fused", "split", "lmhead"], default="fused",
+    ap.add_argument("--path", choices=["fused", "split", "lmhead", "embedding"], default="fused",
                     help="fused: vpce_forward_backward; split: vpce_forward then vpce_backward; "
-                         "lmhead: the LM-head GEMM fused with the forward loss (its own metric)")
+                         "lmhead: the LM-head GEMM fused with the forward loss; embedding: the vocabulary-parallel "
+                         "input embedding (each its own metric)")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the workload's row count (small profiling captures only)")
     args = ap.parse_args()
@@ -729,6 +896,8 @@ def main():
         run_reference(args)
     elif args.path == "lmhead":
         run_lmhead(args)
+    elif args.path == "embedding":
+        run_embedding(args)
     else:
         run_ours(args)
 

@@ -261,6 +261,51 @@ vpce_status vpce_lmhead_forward(const void* hidden, int64_t ld_hidden,
                                 void* workspace, size_t workspace_bytes, vpce_stream_t stream);
 
 /*
+ * Vocabulary-parallel input embedding ("Distributed Training III: Model
+ * Parallelism", CMU 11-868 Lecture 16 notes, §5.5; "LLM Internals" §7.3.4):
+ * the table [V, h] is split by vocabulary into t shards; card i looks up only
+ * the ids in its range and writes zeros elsewhere, and an all-reduce sums the
+ * cards.  On one GPU the sum has one non-zero term per row, so
+ *     out[r] = table_shard_i[ids[r] - vocab_start[i]]  for the shard i holding ids[r],
+ *     out[r] = 0                                          for an id outside [0, V).
+ *   table_shards  host array of t device pointers, shard i [w_i, h] of dtype,
+ *                 row stride ld_table elements (0 = h); element-aligned.
+ *   ids           device int64[s].
+ *   out           device [s, h] of dtype, row stride ld_out (0 = h).
+ *   flag_out      device int or NULL: set to 0, then bit 0
+ *                 (VPCE_FLAG_BAD_TARGET) if some id is outside [0, V).
+ * Rows whose source and destination are 16-byte aligned (and h * element
+ * size a multiple of 16) are copied in 16-byte vectors; others by element.
+ */
+vpce_status vpce_embedding_forward(const void* const* table_shards, vpce_dtype dtype, int t,
+                                   const int64_t* vocab_start, int64_t h, int64_t ld_table,
+                                   const int64_t* ids, int64_t s, void* out, int64_t ld_out,
+                                   int* flag_out, vpce_stream_t stream);
+
+/*
+ * Backward of vpce_embedding_forward (not on the pages; the adjoint of the
+ * lookup): adds each output-gradient row into the fp32 gradient-table row of
+ * its id, accumulating into what grad_shards already hold:
+ *     grad_shard_i[j] += sum over r with ids[r] = vocab_start[i] + j of grad_out[r].
+ * Ids outside [0, V) contribute nothing.  Deterministic: the rows of each id
+ * are summed in ascending row order (fp32), then added once; batches longer
+ * than 16384 rows run in 16384-row chunks in order.
+ *   grad_out      device [s, h] of grad_dtype, row stride ld_grad (0 = h);
+ *                 16-byte aligned, ld_grad * element size a multiple of 16.
+ *   grad_shards   host array of t device float pointers, shard i [w_i, h],
+ *                 row stride ld_grad_table (0 = h); 16-byte aligned,
+ *                 ld_grad_table a multiple of 4.
+ *   h             a positive multiple of 4.
+ *   workspace     vpce_embedding_backward_workspace_bytes() bytes, 256-byte
+ *                 aligned, caller owned.
+ */
+size_t vpce_embedding_backward_workspace_bytes(void);
+vpce_status vpce_embedding_backward(const void* grad_out, vpce_dtype grad_dtype, int64_t ld_grad,
+                                    const int64_t* ids, int64_t s, float* const* grad_shards, int t,
+                                    const int64_t* vocab_start, int64_t h, int64_t ld_grad_table,
+                                    void* workspace, size_t workspace_bytes, vpce_stream_t stream);
+
+/*
  * Synchronise `stream`, then copy the workspace error flag to *flag (bit 0:
  * bad target seen by the last forward; bit 1: a device wait timed out).
  */

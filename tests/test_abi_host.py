@@ -166,3 +166,53 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert _fb_rows() == 5
     # 'none' takes loss_out as optional
     assert _fwd(reduction=vpce.VPCE_NONE, loss_ptr=None, row_loss_ptr=ctypes.c_void_p(FAKE)) == 5
+
+
+def _lmhead(**kw):
+    args = dict(hidden_ptr=ctypes.c_void_p(FAKE), ld_hidden=0, weight_ptrs=[FAKE, FAKE + 4096], ld_weight=0, t=2,
+                s=4, h=128, vocab_start=[0, 16, 40], targets_ptr=ctypes.c_void_p(FAKE), ignore_index=-100,
+                reduction=vpce.VPCE_MEAN, loss_ptr=ctypes.c_void_p(FAKE), row_loss_ptr=None,
+                ws_ptr=ctypes.c_void_p(FAKE), ws_bytes=1 << 24, stream=None)
+    args.update(kw)
+    return vpce.lmhead_forward_raw(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h=100), 1),                               # not a multiple of 64
+    (dict(h=0), 1),
+    (dict(t=33, weight_ptrs=[FAKE] * 33, vocab_start=list(range(0, 34 * 8, 8))), 1),
+    (dict(hidden_ptr=ctypes.c_void_p(FAKE + 8)), 2),  # TMA needs 16-byte bases
+    (dict(weight_ptrs=[FAKE, FAKE + 4100]), 2),
+    (dict(ld_hidden=130), 2),                       # 260-byte rows are not 16-byte multiples
+    (dict(ld_weight=100), 1),                       # narrower than h
+    (dict(vocab_start=[0, 16, 16]), 1),
+    (dict(weight_ptrs=[FAKE, 0]), 1),
+    (dict(reduction=vpce.VPCE_NONE), 1),            # 'none' needs row losses
+    (dict(ws_bytes=1024), 4),
+    (dict(ws_ptr=ctypes.c_void_p(FAKE + 64)), 2),
+])
+def test_lmhead_rejects_bad_arguments(lib, kw, code):
+    assert _lmhead(**kw) == code
+
+
+def test_embedding_rejects_bad_arguments(lib):
+    vs = vpce._i64_array([0, 8, 16])
+    two = ctypes.cast(vpce._ptr_array([FAKE, FAKE + 4096]), ctypes.c_void_p)
+    f = lib.vpce_embedding_forward
+    assert f(two, 7, 2, vs, 16, 0, ctypes.c_void_p(FAKE), 4, ctypes.c_void_p(FAKE), 0, None, None) == 3
+    assert f(two, vpce.VPCE_BF16, 0, vs, 16, 0, ctypes.c_void_p(FAKE), 4, ctypes.c_void_p(FAKE), 0, None, None) == 1
+    assert f(two, vpce.VPCE_BF16, 2, vs, 16, 8, ctypes.c_void_p(FAKE), 4, ctypes.c_void_p(FAKE), 0, None, None) == 1
+    assert f(two, vpce.VPCE_BF16, 2, vs, 16, 0, ctypes.c_void_p(FAKE + 4), 4, ctypes.c_void_p(FAKE), 0, None,
+             None) == 2
+    b = lib.vpce_embedding_backward
+    ws = ctypes.c_void_p(FAKE)
+    nbytes = vpce.vpce_embedding_backward_workspace_bytes()
+    assert b(ctypes.c_void_p(FAKE), vpce.VPCE_BF16, 0, ctypes.c_void_p(FAKE), 4, two, 2, vs, 18, 0, ws, nbytes,
+             None) == 1                            # h not a multiple of 4
+    assert b(ctypes.c_void_p(FAKE + 8), vpce.VPCE_BF16, 0, ctypes.c_void_p(FAKE), 4, two, 2, vs, 16, 0, ws, nbytes,
+             None) == 2
+    assert b(ctypes.c_void_p(FAKE), vpce.VPCE_BF16, 0, ctypes.c_void_p(FAKE), 4, two, 2, vs, 16, 0, ws, 16,
+             None) == 4
+    if not __import__("torch").cuda.is_available():
+        assert b(ctypes.c_void_p(FAKE), vpce.VPCE_BF16, 0, ctypes.c_void_p(FAKE), 4, two, 2, vs, 16, 0, ws, nbytes,
+                 None) == 5

@@ -26,7 +26,7 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas"
 
 LIBS = {
     "libvpce.so": ["vpce_api.cu", "vpce_forward.cu", "vpce_backward.cu", "vpce_fused.cu", "vpce_static.cu",
-                   "vpce_gemm.cu"],
+                   "vpce_gemm.cu", "vpce_embed.cu"],
     "libvpce_synth.so": ["synth_gen.cu"],
 }
 HEADERS = ["vpce_device.cuh", "vpce_kernels.cuh", "vpce_chunk.cuh"]

@@ -18,6 +18,13 @@ void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long
                          long long ignore_index, int reduction, float grad, const float* grad_rows, float* lse,
                          float* rowl, float* row_loss, float* loss_out, Header* hdr, int sms, cudaStream_t st);
 cudaError_t set_gemm_smem();
+cudaError_t set_embed_smem();
+size_t embed_bwd_workspace_bytes();
+void launch_embed_forward(const ShardSet& sh, int t, long long V, long long h, int eb, const long long* ids,
+                          long long s, void* out, long long ld_out, int* flag, int sms, cudaStream_t st);
+cudaError_t launch_embed_backward(const void* grad, int grad_bf16, long long ld_grad, const long long* ids,
+                                  long long s, const ShardSet& gsh, int t, long long V, long long h, void* ws,
+                                  int sms, cudaStream_t st);
 int gemm_max_shards();
 bool launch_gemm_stats(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
                        long long h, const long long* vocab_start, const long long* targets, long long ignore_index,
@@ -62,7 +69,8 @@ vpce_status device_setup(int* sms) {
     if (major != 10 || minor != 3) {
       d.status = VPCE_ERR_UNSUPPORTED_DEVICE;
     } else if (set_stats_smem() != cudaSuccess || set_backward_smem() != cudaSuccess ||
-               set_fused_smem() != cudaSuccess || set_gemm_smem() != cudaSuccess) {
+               set_fused_smem() != cudaSuccess || set_gemm_smem() != cudaSuccess ||
+               set_embed_smem() != cudaSuccess) {
       cudaGetLastError();
       return VPCE_ERR_CUDA;
     } else {
@@ -448,6 +456,89 @@ vpce_status vpce_lmhead_forward(const void* hidden, int64_t ld_hidden, const voi
   const long long blocks = s > 0 ? (s + kCombineThreads - 1) / kCombineThreads : 1;
   launch_combine(c, int(blocks), cs);
   return launch_status();
+}
+
+// Shard geometry of a [w_i, h] table split by vocabulary (row stride ld
+// elements of eb bytes); checks the offsets and the pointers.
+static vpce_status split_table(const void* const* shards, int t, const int64_t* vocab_start, int64_t ld, int eb,
+                                bool need_ptrs, ShardSet* sh) {
+  if (shards == nullptr || vocab_start == nullptr || vocab_start[0] != 0) return VPCE_ERR_INVALID_ARG;
+  std::memset(sh, 0, sizeof(*sh));
+  for (int i = 0; i < t; ++i) {
+    if (vocab_start[i + 1] <= vocab_start[i]) return VPCE_ERR_INVALID_ARG;
+    if (need_ptrs && shards[i] == nullptr) return VPCE_ERR_INVALID_ARG;
+    if (!aligned(shards[i], size_t(eb))) return VPCE_ERR_ALIGNMENT;
+    sh->ptr[i] = static_cast<const unsigned char*>(shards[i]);
+    sh->ld_bytes[i] = ld * eb;
+    sh->start[i] = vocab_start[i];
+  }
+  sh->start[t] = vocab_start[t];
+  return VPCE_OK;
+}
+
+vpce_status vpce_embedding_forward(const void* const* table_shards, vpce_dtype dtype, int t,
+                                   const int64_t* vocab_start, int64_t h, int64_t ld_table, const int64_t* ids,
+                                   int64_t s, void* out, int64_t ld_out, int* flag_out, vpce_stream_t stream) {
+  if (dtype != VPCE_FP32 && dtype != VPCE_BF16) return VPCE_ERR_DTYPE;
+  if (t < 1 || t > VPCE_MAX_SHARDS || s < 0 || h < 1) return VPCE_ERR_INVALID_ARG;
+  const int eb = dtype == VPCE_BF16 ? 2 : 4;
+  const int64_t ldt = ld_table == 0 ? h : ld_table;
+  const int64_t ldo = ld_out == 0 ? h : ld_out;
+  if (ldt < h || ldo < h) return VPCE_ERR_INVALID_ARG;
+  ShardSet sh;
+  vpce_status st = split_table(table_shards, t, vocab_start, ldt, eb, s > 0, &sh);
+  if (st != VPCE_OK) return st;
+  if (s > 0 && (ids == nullptr || out == nullptr)) return VPCE_ERR_INVALID_ARG;
+  if ((ids != nullptr && !aligned(ids, 8)) || (out != nullptr && !aligned(out, size_t(eb))) ||
+      (flag_out != nullptr && !aligned(flag_out, 4)))
+    return VPCE_ERR_ALIGNMENT;
+  int sms = 0;
+  st = device_setup(&sms);
+  if (st != VPCE_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (flag_out != nullptr && cudaMemsetAsync(flag_out, 0, sizeof(int), cs) != cudaSuccess) {
+    cudaGetLastError();
+    return VPCE_ERR_CUDA;
+  }
+  if (s == 0) return VPCE_OK;
+  launch_embed_forward(sh, t, vocab_start[t], h, eb, reinterpret_cast<const long long*>(ids), s, out, ldo,
+                       flag_out, sms, cs);
+  return launch_status();
+}
+
+size_t vpce_embedding_backward_workspace_bytes(void) { return embed_bwd_workspace_bytes(); }
+
+vpce_status vpce_embedding_backward(const void* grad_out, vpce_dtype grad_dtype, int64_t ld_grad,
+                                    const int64_t* ids, int64_t s, float* const* grad_shards, int t,
+                                    const int64_t* vocab_start, int64_t h, int64_t ld_grad_table, void* workspace,
+                                    size_t workspace_bytes, vpce_stream_t stream) {
+  if (grad_dtype != VPCE_FP32 && grad_dtype != VPCE_BF16) return VPCE_ERR_DTYPE;
+  if (t < 1 || t > VPCE_MAX_SHARDS || s < 0 || h < 4 || h % 4 != 0) return VPCE_ERR_INVALID_ARG;
+  const int eb = grad_dtype == VPCE_BF16 ? 2 : 4;
+  const int64_t ldg = ld_grad == 0 ? h : ld_grad;
+  const int64_t ldt = ld_grad_table == 0 ? h : ld_grad_table;
+  if (ldg < h || ldt < h) return VPCE_ERR_INVALID_ARG;
+  ShardSet gsh;
+  vpce_status st = split_table(reinterpret_cast<const void* const*>(grad_shards), t, vocab_start, ldt, 4, s > 0,
+                                &gsh);
+  if (st != VPCE_OK) return st;
+  for (int i = 0; i < t; ++i)
+    if (grad_shards[i] != nullptr && !aligned(grad_shards[i], 16)) return VPCE_ERR_ALIGNMENT;
+  if ((ldt * 4) % 16 != 0) return VPCE_ERR_ALIGNMENT;
+  if (s > 0 && (grad_out == nullptr || ids == nullptr)) return VPCE_ERR_INVALID_ARG;
+  if ((grad_out != nullptr && !aligned(grad_out, 16)) || (ldg * eb) % 16 != 0) return VPCE_ERR_ALIGNMENT;
+  if (ids != nullptr && !aligned(ids, 8)) return VPCE_ERR_ALIGNMENT;
+  if (workspace == nullptr) return VPCE_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return VPCE_ERR_ALIGNMENT;
+  if (workspace_bytes < embed_bwd_workspace_bytes()) return VPCE_ERR_WORKSPACE;
+  int sms = 0;
+  st = device_setup(&sms);
+  if (st != VPCE_OK) return st;
+  if (s == 0) return VPCE_OK;
+  const cudaError_t e = launch_embed_backward(grad_out, grad_dtype == VPCE_BF16, ldg,
+                                              reinterpret_cast<const long long*>(ids), s, gsh, t, vocab_start[t],
+                                              h, workspace, sms, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VPCE_OK : VPCE_ERR_CUDA;
 }
 
 const char* vpce_status_string(vpce_status status) {

@@ -388,3 +388,35 @@ def lmhead_device(m: LmHead, vocab_start=None, device="cuda"):
         ws.append(wi)
     torch.cuda.current_stream(device).synchronize()
     return x, ws
+
+
+# --------------------------------------------------------------------------
+# embedding inputs: the table [V, h] (stream 7), output gradients [s, h]
+# (stream 8), ids from the loss workloads' target recipes
+# --------------------------------------------------------------------------
+STREAM_TABLE = 7
+STREAM_GRAD = 8
+
+
+def table_device(seed: int, vocab_start, h: int, sigma: float = 1.0, device="cuda"):
+    """Device bf16 table shards [w_i, h]: element (v, k) is normal number
+    v * h + k of stream 7 (the values of dense_host(seed, STREAM_TABLE, ...))."""
+    import torch
+
+    out = []
+    for i in range(len(vocab_start) - 1):
+        e = torch.empty((vocab_start[i + 1] - vocab_start[i], h), dtype=torch.bfloat16, device=device)
+        _dense_device(e, seed, STREAM_TABLE, vocab_start[i], h, sigma)
+        out.append(e)
+    torch.cuda.current_stream(device).synchronize()
+    return out
+
+
+def grad_device(seed: int, s: int, h: int, sigma: float = 1.0, device="cuda"):
+    """Device bf16 output gradient [s, h] (stream 8)."""
+    import torch
+
+    g = torch.empty((s, h), dtype=torch.bfloat16, device=device)
+    _dense_device(g, seed, STREAM_GRAD, 0, h, sigma)
+    torch.cuda.current_stream(device).synchronize()
+    return g

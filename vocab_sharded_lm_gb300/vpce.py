@@ -85,6 +85,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.vpce_lmhead_forward.restype = ctypes.c_int
         lib.vpce_lmhead_forward.argtypes = [_P, _I64, _P, _I64, ctypes.c_int, _I64, _I64, _I64P, _P, _I64,
                                             ctypes.c_int, _P, _P, _P, ctypes.c_size_t, _P]
+        lib.vpce_embedding_forward.restype = ctypes.c_int
+        lib.vpce_embedding_forward.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64P, _I64, _I64, _P, _I64, _P,
+                                               _I64, _P, _P]
+        lib.vpce_embedding_backward_workspace_bytes.restype = ctypes.c_size_t
+        lib.vpce_embedding_backward_workspace_bytes.argtypes = []
+        lib.vpce_embedding_backward.restype = ctypes.c_int
+        lib.vpce_embedding_backward.argtypes = [_P, ctypes.c_int, _I64, _P, _I64, _P, ctypes.c_int, _I64P, _I64,
+                                                _I64, _P, ctypes.c_size_t, _P]
         lib.vpce_read_error_flag.restype = ctypes.c_int
         lib.vpce_read_error_flag.argtypes = [_P, ctypes.POINTER(ctypes.c_int), _P]
         lib.vpce_status_string.restype = ctypes.c_char_p
@@ -439,3 +447,87 @@ def vpce_lmhead_forward(hidden, weight_shards, targets, vocab_start=None, *, ign
     if code != VPCE_OK:
         raise VPCEError(code, "vpce_lmhead_forward")
     return result, workspace
+
+
+# ----------------------------------------------------------------------------
+# vocabulary-parallel input embedding
+# ----------------------------------------------------------------------------
+def _table_desc(shards, vocab_start):
+    import torch
+
+    if not shards:
+        raise ValueError("need at least one shard")
+    dt = shards[0].dtype
+    h = shards[0].shape[1]
+    for e in shards:
+        if e.dtype != dt or e.dim() != 2 or e.shape[1] != h or not e.is_cuda or e.stride(1) != 1:
+            raise ValueError("table shards must be 2-D CUDA tensors [w_i, h] of one dtype, contiguous columns")
+    strides = {e.stride(0) for e in shards if e.shape[0] > 1}
+    if len(strides) > 1:
+        raise ValueError("table shards must share one row stride")
+    ld = strides.pop() if strides else h
+    if vocab_start is None:
+        vocab_start = [0]
+        for e in shards:
+            vocab_start.append(vocab_start[-1] + e.shape[0])
+    code = {torch.bfloat16: VPCE_BF16, torch.float32: VPCE_FP32}.get(dt)
+    return code, h, ld, [int(v) for v in vocab_start]
+
+
+def vpce_embedding_forward(table_shards, ids, vocab_start=None, *, out=None, flag=None, stream=None):
+    """Rows ``table[ids]`` of a vocabulary-split table (zero rows for ids
+    outside [0, V)).  ``flag`` (CUDA int32 scalar) receives bit 0 if any id
+    was outside."""
+    import torch
+
+    dtype, h, ld, vs = _table_desc(table_shards, vocab_start)
+    if dtype is None:
+        raise TypeError("table dtype must be bf16 or fp32")
+    if ids.dtype != torch.int64 or not ids.is_cuda or ids.dim() != 1:
+        raise ValueError("ids must be a 1-D CUDA int64 tensor")
+    s = ids.numel()
+    if out is None:
+        out = torch.empty((s, h), dtype=table_shards[0].dtype, device=ids.device)
+    ld_out = out.stride(0) if s > 1 else h
+    lib = load_library()
+    code = int(lib.vpce_embedding_forward(ctypes.cast(_ptr_array([e.data_ptr() for e in table_shards]), _P),
+                                          int(dtype), len(table_shards), _i64_array(vs), int(h), int(ld),
+                                          ctypes.c_void_p(ids.data_ptr()), int(s), _ptr(out), int(ld_out),
+                                          _ptr(flag), _stream_ptr(stream)))
+    if code != VPCE_OK:
+        raise VPCEError(code, "vpce_embedding_forward")
+    return out
+
+
+def vpce_embedding_backward_workspace_bytes() -> int:
+    return int(load_library().vpce_embedding_backward_workspace_bytes())
+
+
+def vpce_embedding_backward(grad_out, ids, grad_shards, vocab_start=None, *, workspace=None, stream=None):
+    """Accumulate the lookup's adjoint into the fp32 gradient-table shards
+    (in place): each gradient row is added into its id's row."""
+    import torch
+
+    gdt, h, ld, vs = _table_desc(grad_shards, vocab_start)
+    if gdt != VPCE_FP32:
+        raise TypeError("gradient table shards must be fp32")
+    if grad_out.dim() != 2 or grad_out.shape[1] != h or not grad_out.is_cuda or grad_out.stride(1) != 1:
+        raise ValueError("grad_out must be a CUDA [s, h] tensor with contiguous columns")
+    code_dt = {torch.bfloat16: VPCE_BF16, torch.float32: VPCE_FP32}.get(grad_out.dtype)
+    if code_dt is None:
+        raise TypeError("grad_out dtype must be bf16 or fp32")
+    s = grad_out.shape[0]
+    if ids.dtype != torch.int64 or not ids.is_cuda or ids.numel() != s:
+        raise ValueError("ids must be a CUDA int64 tensor with one entry per row")
+    if workspace is None:
+        workspace = torch.empty(vpce_embedding_backward_workspace_bytes(), dtype=torch.uint8, device=ids.device)
+    lib = load_library()
+    code = int(lib.vpce_embedding_backward(_ptr(grad_out), int(code_dt), int(grad_out.stride(0) if s > 1 else h),
+                                           ctypes.c_void_p(ids.data_ptr()), int(s),
+                                           ctypes.cast(_ptr_array([g.data_ptr() for g in grad_shards]), _P),
+                                           len(grad_shards), _i64_array(vs), int(h), int(ld),
+                                           ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                           _stream_ptr(stream)))
+    if code != VPCE_OK:
+        raise VPCEError(code, "vpce_embedding_backward")
+    return grad_shards
