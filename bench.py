@@ -527,6 +527,8 @@ def run_reference(args):
 # the LM-head GEMM fused with the forward loss (vpce_lmhead_forward)
 # ----------------------------------------------------------------------------
 LMHEAD_METRIC = "LM-head GEMM + VPCE forward tokens/s & TFLOP/s (% of peak), s=8192 h=8192 V=128256 bf16, 1 GB300"
+LMHEAD_TRAIN_METRIC = ("LM-head GEMM + VPCE forward and backward (dX, dW) tokens/s & TFLOP/s (% of peak), "
+                       "s=8192 h=8192 V=128256 bf16, 1 GB300")
 
 
 def run_lmhead(args):
@@ -554,9 +556,17 @@ def run_lmhead(args):
     wk = torch.empty(vpce.vpce_lmhead_workspace_bytes(m.s), dtype=torch.uint8, device=dev)
     loss = torch.empty((), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    train = args.path == "lmhead_train"
+    if train:
+        gx = torch.empty_like(x)
+        gw = [torch.zeros((w.shape[0], m.h), dtype=torch.float32, device=dev) for w in ws]
+        bwk = torch.empty(vpce.vpce_lmhead_backward_workspace_bytes(m.V, m.h), dtype=torch.uint8, device=dev)
 
     def step():
         vpce.vpce_lmhead_forward(x, ws, y, vs, ignore_index=m.ignore_index, loss_out=loss, workspace=wk)
+        if train:
+            vpce.vpce_lmhead_backward(x, ws, y, wk, vs, ignore_index=m.ignore_index, grad_hidden=gx,
+                                      grad_weight_shards=gw, workspace=bwk)
 
     for _ in range(args.warmup):
         step()
@@ -612,6 +622,9 @@ def run_lmhead(args):
         stream.wait_event(done[b])
         vpce.vpce_lmhead_forward(xb[b], ws, yb[b], vs, ignore_index=m.ignore_index, loss_out=lb[b],
                                  workspace=wkb[b])
+        if train:
+            vpce.vpce_lmhead_backward(xb[b], ws, yb[b], wkb[b], vs, ignore_index=m.ignore_index, grad_hidden=gx,
+                                      grad_weight_shards=gw, workspace=bwk)
         host_loss[max(k, 0)].copy_(lb[b], non_blocking=True)
         used[b].record(stream)
     e1.record(stream)
@@ -622,12 +635,13 @@ def run_lmhead(args):
             dist.destroy_process_group()
         return
 
-    flops = 2.0 * m.s * m.h * m.V
+    # forward: one product; backward: the logits again, dX and dW
+    flops = 2.0 * m.s * m.h * m.V * (4 if train else 1)
     burst, sustained, kind = _tensor_peaks()
     achieved = flops / (call_ms * 1e-3) / 1e12
     ms_step = total_ms / args.steps
     out = {
-        "metric": LMHEAD_METRIC,
+        "metric": LMHEAD_TRAIN_METRIC if train else LMHEAD_METRIC,
         "value": round(_weak_scaling_value(m.s * args.steps, world, total_ms), 1),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -648,11 +662,13 @@ def run_lmhead(args):
             "parallelism": f"vocab shards t={m.t} on one GPU; {world} independent replica(s)",
             "l2": f"inputs larger than L2: the head is {sum(w.numel() for w in ws) * 2 / 1e9:.2f} GB",
             "path": "vpce_lmhead_forward (tcgen05 GEMM, fp32 accumulators in TMEM, loss statistics in the "
-                    "epilogue; the logits are never written), then the shard combine",
+                    "epilogue; the logits are never written), then the shard combine"
+                    + ("; vpce_lmhead_backward (per 1024-row chunk: tcgen05 recompute writing bf16 dZ, then "
+                       "cuBLAS dX = dZ W and dW += dZ^T X)" if train else ""),
         },
         "tflops": round(achieved, 1),
         "roofline": {
-            "kernel": "gemm_stats_kernel",
+            "kernel": "gemm_stats_kernel" + (" + recompute + cuBLAS dX, dW (the whole step)" if train else ""),
             "bound": "tensor",
             "achieved": round(achieved, 1),
             "peak": burst,
@@ -662,7 +678,8 @@ def run_lmhead(args):
             "frac_of_sustained": round(achieved / sustained, 4),
             "traffic": None,
             "algorithmic_flops_per_launch": flops,
-            "note": "achieved = 2 s h V / mean CUDA-event time of one call (the GEMM launch plus the few-us combine)",
+            "note": ("achieved = 8 s h V / mean CUDA-event time of one forward + backward step" if train else
+                     "achieved = 2 s h V / mean CUDA-event time of one call (the GEMM launch plus the few-us combine)"),
         },
         "e2e": {
             "value": round(_weak_scaling_value(m.s, world, e2e_ms), 1),
@@ -674,10 +691,13 @@ def run_lmhead(args):
             "note": "pinned host hidden states + targets copied in every step (copy stream, double-buffered), "
                     "loss read back; the head's weights stay on the device",
         },
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (2 + (m.s + 1023) // 1024 * 2 if train else 2) * args.steps,
         "clocks": clk,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if train:
+        out["gpu_launches_note"] = ("forward 2 + per row chunk: the tcgen05 dlogits kernel and the dX conversion; "
+                                    "the 2 t cuBLAS GEMMs per chunk are library launches, not counted")
+    if world == 1 and not args.no_cpu_baseline and not train:
         # the oracle on a bounded sample: a few rows against the first vocabulary
         # rows of the head (read back from the device generator), scaled to the
         # full vocabulary (the oracle's cost is linear in V)
@@ -883,7 +903,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=["fused", "split", "lmhead", "embedding"], default="fused",
+    ap.add_argument("--path", choices=["fused", "split", "lmhead", "lmhead_train", "embedding"], default="fused",
                     help="fused: vpce_forward_backward; split: vpce_forward then vpce_backward; "
                          "lmhead: the LM-head GEMM fused with the forward loss; embedding: the vocabulary-parallel "
                          "input embedding (each its own metric)")
@@ -894,7 +914,7 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
-    elif args.path == "lmhead":
+    elif args.path in ("lmhead", "lmhead_train"):
         run_lmhead(args)
     elif args.path == "embedding":
         run_embedding(args)

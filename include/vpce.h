@@ -248,8 +248,8 @@ vpce_status vpce_forward_static(const void* const* shards, vpce_dtype dtype, int
  *   t              1..32 shards; vocab_start as vpce_forward (t+1 offsets).
  *   h              hidden size, a positive multiple of 64.
  *   workspace      vpce_lmhead_workspace_bytes(s) bytes, 256-byte aligned.
- * Other arguments and errors as vpce_forward.  No backward is provided (it
- * would recompute the logits tile by tile).
+ * Other arguments and errors as vpce_forward.  The backward is
+ * vpce_lmhead_backward.
  */
 #define VPCE_LMHEAD_MAX_GROUPS 256
 size_t vpce_lmhead_workspace_bytes(int64_t s);
@@ -259,6 +259,39 @@ vpce_status vpce_lmhead_forward(const void* hidden, int64_t ld_hidden,
                                 const int64_t* targets, int64_t ignore_index,
                                 vpce_reduction reduction, float* loss_out, float* row_loss_out,
                                 void* workspace, size_t workspace_bytes, vpce_stream_t stream);
+
+/*
+ * Backward of vpce_lmhead_forward (the pages give none; the standard
+ * derivative): with dZ = (softmax(z) - onehot) * g / n_valid ('mean'; g for
+ * 'sum'; g_r = grad_rows[r] when grad_rows is given),
+ *     grad_hidden         = dZ W              bf16 [s, h], overwritten
+ *     grad_weight_shards[i] += dZ_i^T X       fp32 [w_i, h], accumulated
+ * The logits are formed again tile by tile on the tensor cores (the forward
+ * kept none) and written as bf16 dZ for one chunk of 1024 rows at a time into
+ * `workspace`; the two products are plain cuBLAS GEMMs (bf16 in, fp32
+ * accumulate).  Every argument describing X, the head, the targets and
+ * fwd_workspace must be the preceding vpce_lmhead_forward's, unmodified
+ * (it carries logsumexp, n_valid and the reduction).
+ *   grad_output / grad_rows  as vpce_backward / vpce_backward_rows (grad_rows
+ *                   device float[s] or NULL).
+ *   grad_hidden     device bf16 [s, h], row stride ld_grad_hidden (0 = h).
+ *   grad_weight_shards  host array of t device float pointers, [w_i, h],
+ *                   row stride ld_grad_weight (0 = h), 16-byte aligned.
+ *   workspace       vpce_lmhead_backward_workspace_bytes(V, h) bytes,
+ *                   256-byte aligned (dZ of one chunk and an fp32 dX chunk).
+ * The cuBLAS handle is created once per device on first use and owns its
+ * own workspace; calls on one device are serialised on it.
+ */
+size_t vpce_lmhead_backward_workspace_bytes(int64_t V, int64_t h);
+vpce_status vpce_lmhead_backward(const void* hidden, int64_t ld_hidden,
+                                 const void* const* weight_shards, int64_t ld_weight,
+                                 int t, int64_t s, int64_t h, const int64_t* vocab_start,
+                                 const int64_t* targets, int64_t ignore_index,
+                                 float grad_output, const float* grad_rows,
+                                 const void* fwd_workspace, size_t fwd_workspace_bytes,
+                                 void* grad_hidden, int64_t ld_grad_hidden,
+                                 float* const* grad_weight_shards, int64_t ld_grad_weight,
+                                 void* workspace, size_t workspace_bytes, vpce_stream_t stream);
 
 /*
  * Vocabulary-parallel input embedding ("Distributed Training III: Model

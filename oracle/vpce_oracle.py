@@ -55,6 +55,7 @@ __all__ = [
     "shard_partials",
     "combine_sharded",
     "lmhead_logits",
+    "lmhead_backward",
     "embedding_forward",
     "embedding_backward",
 ]
@@ -233,6 +234,30 @@ def lmhead_logits(x, w_shards, vocab_start, dtype: str = "bf16") -> np.ndarray:
             raise ValueError(f"shard {i} has shape {W.shape}")
         z[:, vs[i]:vs[i + 1]] = X @ W.T
     return z
+
+
+def lmhead_backward(x, w_shards, vocab_start, y, ignore_index: int = -100, grad=1.0,
+                    reduction: str = "mean", dtype: str = "bf16"):
+    """Gradients of the reduced cross-entropy of ``z = X W^T`` with respect
+    to X and to each head shard, in fp64.
+
+    The pages give no backward; this is the chain rule through the plain
+    product: with ``dZ = dlogits(z, ...)`` (the loss's own gradient, per-row
+    ``grad`` for 'none'), ``dX = dZ W`` and ``dW_i = dZ_i^T X``.  Returns
+    ``(dX [s, h], [dW_i [w_i, h]], dZ)``.
+    """
+    vs = [int(v) for v in vocab_start]
+    X = widen(x, dtype)
+    z = lmhead_logits(x, w_shards, vs, dtype)
+    dz = dlogits(z, y, ignore_index, grad=grad, reduction=reduction)
+    dX = np.zeros_like(X)
+    dW = []
+    for i, w in enumerate(w_shards):
+        W = widen(w, dtype)
+        dzi = dz[:, vs[i]:vs[i + 1]]
+        dX += dzi @ W
+        dW.append(dzi.T @ X)
+    return dX, dW, dz
 
 
 # --------------------------------------------------------------------------

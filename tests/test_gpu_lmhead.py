@@ -164,3 +164,65 @@ def test_lmhead_full_size_sampled_rows():
     bound = _row_bound(xh, w_host, m.h)
     err = np.abs(got[rows] - ref["row_loss"])
     assert np.all(err <= bound), (err, bound)
+
+
+# ---------------------------------------------------------------- backward
+def _bwd_bound(dz, mat, ref, K):
+    """dZ rounded to bf16 (8 significant bits: unit roundoff 2^-8), the
+    recomputed logits' error carried through exp (under 2^-11 for h <= 8192,
+    from the bound above), fp32 accumulation over K terms in 16-term MMA
+    steps, and, for bf16 outputs, the final rounding (2^-8 of the result)."""
+    eps = 2.0 ** -8 + 2.0 ** -11 + (K / 16) * 2.0 ** -24
+    a = eps * (np.abs(dz) @ np.abs(mat))
+    return a + 2.0 ** -8 * (np.abs(ref) + a) + 1e-30
+
+
+def _check_backward(m, vs=None, *, reduction="mean", grad=1.0, grad_rows=None):
+    vs = synth.even_vocab_start(m.V, m.t) if vs is None else list(vs)
+    meta = synth.lmhead_meta(m)
+    x, ws = synth.lmhead_device(m, vs)
+    y = torch.from_numpy(meta.targets).cuda()
+    rl = torch.empty(m.s, dtype=torch.float32, device="cuda")
+    _, fwk = vpce.vpce_lmhead_forward(x, ws, y, vs, ignore_index=m.ignore_index, reduction=reduction,
+                                      row_loss_out=rl)
+    gw0 = [torch.full((w.shape[0], m.h), 0.5, dtype=torch.float32, device="cuda") for w in ws]
+    gr = torch.from_numpy(np.asarray(grad_rows, dtype=np.float32)).cuda() if grad_rows is not None else None
+    dx, dw = vpce.vpce_lmhead_backward(x, ws, y, fwk, vs, ignore_index=m.ignore_index, grad_output=grad,
+                                       grad_rows=gr, grad_weight_shards=gw0)
+    torch.cuda.synchronize()
+    xh, wh = _host(m, vs)
+    if grad_rows is not None:
+        ref_x, ref_w, dz = O.lmhead_backward(xh, wh, vs, meta.targets, m.ignore_index,
+                                             grad=np.asarray(grad_rows, dtype=np.float64), reduction="none")
+    else:
+        ref_x, ref_w, dz = O.lmhead_backward(xh, wh, vs, meta.targets, m.ignore_index, grad=grad,
+                                             reduction=reduction)
+    got_x = O.widen(dx.view(torch.int16).cpu().numpy().view(np.uint16), "bf16")
+    W = np.concatenate([O.widen(w, "bf16") for w in wh])
+    bx = _bwd_bound(dz, W, ref_x, m.V)
+    assert np.all(np.abs(got_x - ref_x) <= bx), np.max(np.abs(got_x - ref_x) / bx)
+    X = O.widen(xh, "bf16")
+    for i in range(len(vs) - 1):
+        got_w = dw[i].cpu().numpy().astype(np.float64) - 0.5
+        dzi = dz[:, vs[i]:vs[i + 1]]
+        # plus one fp32 rounding of the accumulation onto 0.5 per row chunk
+        chunks = (m.s + 1023) // 1024
+        bw = _bwd_bound(dzi.T, X, np.zeros_like(ref_w[i]), min(m.s, 1024)) + chunks * 2.0 ** -24 * (0.5 + np.abs(ref_w[i]))
+        assert np.all(np.abs(got_w - ref_w[i]) <= bw), (i, np.max(np.abs(got_w - ref_w[i]) / bw))
+
+
+@pytest.mark.parametrize("m,vs", [
+    (synth.LMHEADS["lmhead_s300_h512_v5000"], None),                    # ragged tiles, ignored rows
+    (synth.LmHead("bwd_chunks", 17, 1200, 128, 700, 7, ignore_frac=0.1), None),  # two row chunks
+    (synth.LmHead("bwd_uneven", 18, 130, 64, 600, 3), [0, 1, 300, 600]),  # one-column shard
+])
+def test_lmhead_backward_parity(m, vs):
+    _check_backward(m, vs)
+
+
+def test_lmhead_backward_sum_and_per_row_gradients():
+    m = synth.LmHead("bwd_red", 19, 200, 128, 900, 2, ignore_frac=0.1)
+    _check_backward(m, reduction="sum", grad=0.75)
+    g = np.random.default_rng(2).normal(size=m.s).astype(np.float32)
+    g[::9] = 0.0
+    _check_backward(m, reduction="none", grad_rows=g)

@@ -256,6 +256,26 @@ def test_lmhead_matches_torch_linear_and_cross_entropy():
     np.testing.assert_allclose(z, z1, rtol=1e-14, atol=1e-14)
 
 
+def test_lmhead_backward_matches_torch_autograd():
+    rng = np.random.default_rng(8)
+    s, h, V = 30, 64, 200
+    x = _bf16(rng.normal(size=(s, h)))
+    W = _bf16(rng.normal(0.0, 3.0 / np.sqrt(h), size=(V, h)))
+    y = rng.integers(0, V, size=s)
+    y[[2, 9]] = -100
+    vs = [0, 64, 65, 200]
+    shards = [W[vs[i]:vs[i + 1]] for i in range(3)]
+    for red, g in (("mean", 1.5), ("sum", 0.5)):
+        xt = torch.tensor(O.widen(x, "bf16"), requires_grad=True)
+        wt = torch.tensor(O.widen(W, "bf16"), requires_grad=True)
+        loss = torch.nn.functional.cross_entropy(torch.nn.functional.linear(xt, wt), torch.tensor(y),
+                                                 ignore_index=-100, reduction=red)
+        (loss * g).backward()
+        dX, dW, _ = O.lmhead_backward(x, shards, vs, y, grad=g, reduction=red)
+        np.testing.assert_allclose(dX, xt.grad.numpy(), rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(np.concatenate(dW), wt.grad.numpy(), rtol=1e-12, atol=1e-14)
+
+
 # ---------------------------------------------------------------- embedding
 def test_embedding_forward_matches_torch_embedding():
     rng = np.random.default_rng(5)

@@ -26,10 +26,12 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas"
 
 LIBS = {
     "libvpce.so": ["vpce_api.cu", "vpce_forward.cu", "vpce_backward.cu", "vpce_fused.cu", "vpce_static.cu",
-                   "vpce_gemm.cu", "vpce_embed.cu"],
+                   "vpce_gemm.cu", "vpce_embed.cu", "vpce_lmhead_bwd.cu"],
     "libvpce_synth.so": ["synth_gen.cu"],
 }
 HEADERS = ["vpce_device.cuh", "vpce_kernels.cuh", "vpce_chunk.cuh"]
+# the LM-head backward's two plain GEMMs (dX, dW) go through cuBLAS
+LINK = {"libvpce.so": ["-lcublas"]}
 
 
 def _nvcc() -> str:
@@ -82,7 +84,7 @@ def build(verbose: bool = False) -> dict:
         if not (os.path.exists(target) and os.path.getmtime(target) >= _mtime(objs)):
             tmp = target + ".tmp"
             cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-                   "-Xlinker", f"-rpath,{cudalib}"]
+                   "-Xlinker", f"-rpath,{cudalib}"] + LINK.get(lib, [])
             r = subprocess.run(cmd, capture_output=True, text=True)
             if r.returncode != 0:
                 raise RuntimeError(f"link failed for {lib}:\n{r.stdout}\n{r.stderr}")

@@ -19,6 +19,12 @@ void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long
                          float* rowl, float* row_loss, float* loss_out, Header* hdr, int sms, cudaStream_t st);
 cudaError_t set_gemm_smem();
 cudaError_t set_embed_smem();
+size_t lmhead_bwd_workspace_bytes(long long V, long long h);
+vpce_status lmhead_backward_run(const void* x, long long ld_x, const void* const* w, long long ld_w, int t,
+                                long long s, long long h, const long long* vs, const long long* targets,
+                                long long ignore_index, float grad, const float* grad_rows, const float* lse,
+                                Header* hdr, void* dx, long long ld_dx, float* const* dw, long long ld_dw, void* ws,
+                                int sms, cudaStream_t st);
 size_t embed_bwd_workspace_bytes();
 void launch_embed_forward(const ShardSet& sh, int t, long long V, long long h, int eb, const long long* ids,
                           long long s, void* out, long long ld_out, int* flag, int sms, cudaStream_t st);
@@ -456,6 +462,64 @@ vpce_status vpce_lmhead_forward(const void* hidden, int64_t ld_hidden, const voi
   const long long blocks = s > 0 ? (s + kCombineThreads - 1) / kCombineThreads : 1;
   launch_combine(c, int(blocks), cs);
   return launch_status();
+}
+
+size_t vpce_lmhead_backward_workspace_bytes(int64_t V, int64_t h) {
+  if (V < 1 || h < 1) return 0;
+  return lmhead_bwd_workspace_bytes(V, h);
+}
+
+vpce_status vpce_lmhead_backward(const void* hidden, int64_t ld_hidden, const void* const* weight_shards,
+                                 int64_t ld_weight, int t, int64_t s, int64_t h, const int64_t* vocab_start,
+                                 const int64_t* targets, int64_t ignore_index, float grad_output,
+                                 const float* grad_rows, const void* fwd_workspace, size_t fwd_workspace_bytes,
+                                 void* grad_hidden, int64_t ld_grad_hidden, float* const* grad_weight_shards,
+                                 int64_t ld_grad_weight, void* workspace, size_t workspace_bytes,
+                                 vpce_stream_t stream) {
+  if (t < 1 || t > gemm_max_shards() || s < 0 || s >= (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  if (h < 64 || h % 64 != 0 || h >= (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  if (weight_shards == nullptr || grad_weight_shards == nullptr || vocab_start == nullptr || vocab_start[0] != 0)
+    return VPCE_ERR_INVALID_ARG;
+  for (int i = 0; i < t; ++i)
+    if (vocab_start[i + 1] <= vocab_start[i]) return VPCE_ERR_INVALID_ARG;
+  if (vocab_start[t] >= (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  if (!std::isfinite(grad_output)) return VPCE_ERR_INVALID_ARG;
+  const int64_t ldx = ld_hidden == 0 ? h : ld_hidden;
+  const int64_t ldw = ld_weight == 0 ? h : ld_weight;
+  const int64_t ldgx = ld_grad_hidden == 0 ? h : ld_grad_hidden;
+  const int64_t ldgw = ld_grad_weight == 0 ? h : ld_grad_weight;
+  if (ldx < h || ldw < h || ldgx < h || ldgw < h) return VPCE_ERR_INVALID_ARG;
+  if (s > 0) {
+    if (hidden == nullptr || targets == nullptr || grad_hidden == nullptr) return VPCE_ERR_INVALID_ARG;
+    for (int i = 0; i < t; ++i)
+      if (weight_shards[i] == nullptr || grad_weight_shards[i] == nullptr) return VPCE_ERR_INVALID_ARG;
+  }
+  if ((hidden != nullptr && !aligned(hidden, 16)) || (ldx * 2) % 16 != 0 || (ldw * 2) % 16 != 0)
+    return VPCE_ERR_ALIGNMENT;
+  for (int i = 0; i < t; ++i) {
+    if (weight_shards[i] != nullptr && !aligned(weight_shards[i], 16)) return VPCE_ERR_ALIGNMENT;
+    if (grad_weight_shards[i] != nullptr && !aligned(grad_weight_shards[i], 16)) return VPCE_ERR_ALIGNMENT;
+  }
+  if ((grad_hidden != nullptr && !aligned(grad_hidden, 2)) || (targets != nullptr && !aligned(targets, 8)) ||
+      (grad_rows != nullptr && !aligned(grad_rows, 4)))
+    return VPCE_ERR_ALIGNMENT;
+  if (fwd_workspace == nullptr || workspace == nullptr) return VPCE_ERR_INVALID_ARG;
+  if (!aligned(fwd_workspace, 256) || !aligned(workspace, 256)) return VPCE_ERR_ALIGNMENT;
+  if (fwd_workspace_bytes < WsLayout(VPCE_LMHEAD_MAX_GROUPS, s).total ||
+      workspace_bytes < lmhead_bwd_workspace_bytes(vocab_start[t], h))
+    return VPCE_ERR_WORKSPACE;
+  int sms = 0;
+  vpce_status st = device_setup(&sms);
+  if (st != VPCE_OK) return st;
+  if (s == 0) return VPCE_OK;
+  const WsLayout L(VPCE_LMHEAD_MAX_GROUPS, s);
+  const unsigned char* fws = static_cast<const unsigned char*>(fwd_workspace);
+  const int g_sms = sms < VPCE_LMHEAD_MAX_GROUPS ? sms : VPCE_LMHEAD_MAX_GROUPS;
+  return lmhead_backward_run(hidden, ldx, weight_shards, ldw, t, s, h, reinterpret_cast<const long long*>(vocab_start),
+                             reinterpret_cast<const long long*>(targets), ignore_index, grad_output, grad_rows,
+                             reinterpret_cast<const float*>(fws + L.lse),
+                             reinterpret_cast<Header*>(const_cast<unsigned char*>(fws)), grad_hidden, ldgx,
+                             grad_weight_shards, ldgw, workspace, g_sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // Shard geometry of a [w_i, h] table split by vocabulary (row stride ld

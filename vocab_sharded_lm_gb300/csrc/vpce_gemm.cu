@@ -75,7 +75,16 @@ struct GemmParams {
   float2* part;                     // [gn][s]: (max, sum exp) of the group's columns
   float* tgt;                       // [s]: target logit
   Header* hdr;
+  // gradient epilogue only
+  const float* lse;                 // [s] logsumexp of the forward
+  const float* grad_rows;           // [s] per-row upstream gradient, or null
+  float grad;                       // upstream gradient g of the reduced loss (grad_rows null)
+  unsigned short* dz;               // [s, ldz] bf16 dlogits, global column c at dz + c
+  long long ldz;
 };
+
+constexpr int kEpiStats = 0;  // loss statistics of the tile
+constexpr int kEpiGrad = 1;   // dlogits of the tile, from the forward's logsumexp
 
 // ---------------------------------------------------------------------------
 // inline PTX: TMA tiles, tcgen05
@@ -173,6 +182,7 @@ __device__ __forceinline__ int shard_of_tile(const GemmParams& p, int nt) {
   return i;
 }
 
+template <int EPI>
 __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   GemmSmem& sm = *reinterpret_cast<GemmSmem*>(smem_raw);
@@ -191,7 +201,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
-    if (blockIdx.x == 0) {
+    if (EPI == kEpiStats && blockIdx.x == 0) {
       p.hdr->ticket = 0u;
       p.hdr->error_flag = 0;
     }
@@ -312,6 +322,16 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
       long long y = live ? __ldg(p.targets + r) : -1;
       float m = -INFINITY, se = 0.f, zt = 0.f;
       bool has_t = false;
+      // gradient epilogue: the row's exponent offset and scale (0 for rows
+      // outside the batch or ignored)
+      float cb = 0.f, scl = 0.f;
+      if (EPI == kEpiGrad && live && y != p.ignore_index) {
+        // the forward's header: g / n_valid for 'mean', g otherwise
+        const int nv = p.hdr->n_valid;
+        const float sc_all = p.hdr->reduction != VPCE_MEAN ? p.grad : (nv > 0 ? p.grad / float(nv) : 0.f);
+        cb = -__ldg(p.lse + r) * kLog2e;
+        scl = p.grad_rows != nullptr ? __ldg(p.grad_rows + r) : sc_all;
+      }
       for (int nt = nt0; nt < nt1; ++nt) {
         const int b = int(tiles & 1u);
         if (!waitw(&sm.acc_full[b], (tiles >> 1) & 1u, &sm.abort_flag)) {
@@ -324,6 +344,40 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
         const int width = p.vstart[sh + 1] - p.vstart[sh];
         const int valid = min(kBN, width - col0);
         const long long tc = y - (long long)p.vstart[sh] - col0;  // target column inside this tile
+        if constexpr (EPI == kEpiGrad) {
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            if (c * 32 >= valid) break;  // warp-uniform
+            float v[32];
+            tmem_ld32(lane_addr + uint32_t(b * kBN + c * 32), v);
+            const int lim = valid - c * 32;
+            const long long rel = tc - c * 32;
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              // (softmax - onehot) * g, rounded to nearest-even bf16
+              float d0 = ex2(fmaf(v[j], kLog2e, cb)) * scl;
+              float d1 = ex2(fmaf(v[j + 1], kLog2e, cb)) * scl;
+              if (j == rel) d0 -= scl;
+              if (j + 1 == rel) d1 -= scl;
+              if (scl == 0.f) d0 = d1 = 0.f;  // ignored or padding rows (also keeps inf * 0 out)
+              w[j / 2] = pack_bf16x2(d0, d1);
+            }
+            if (live) {
+              const long long col = (long long)p.vstart[sh] + col0 + c * 32;
+              unsigned short* dst = p.dz + (long long)r * p.ldz + col;
+              if (lim == 32 && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+                uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) d4[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j < lim) dst[j] = (unsigned short)((j & 1) ? (w[j / 2] >> 16) : (w[j / 2] & 0xffffu));
+              }
+            }
+          }
+        } else {
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           if (c * 32 >= valid) break;  // warp-uniform
@@ -360,13 +414,14 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
           }
           se += a0 + a1;
         }
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_local(&sm.acc_empty[b]);
         ++tiles;
       }
       if (!ok) break;
-      if (live) {
+      if (EPI == kEpiStats && live) {
         p.part[(long long)grp * p.s + r] = make_float2(m, se);
         if (has_t) p.tgt[r] = zt;
       }
@@ -424,7 +479,10 @@ int gemm_max_shards() { return kMaxGemmShards; }
 int gemm_max_groups(int sms) { return sms > 0 ? sms : 1; }
 
 cudaError_t set_gemm_smem() {
-  return cudaFuncSetAttribute(gemm_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const cudaError_t e = cudaFuncSetAttribute(gemm_stats_kernel<kEpiStats>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(GemmSmem)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemm_stats_kernel<kEpiGrad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(sizeof(GemmSmem)));
 }
 
@@ -476,7 +534,42 @@ bool launch_gemm_stats(const void* x, long long ld_x, const void* const* w, long
   p.tgt = tgt;
   p.hdr = hdr;
   *groups = p.gn;
-  gemm_stats_kernel<<<p.gm * p.gn, kGThreads, sizeof(GemmSmem), st>>>(p);
+  gemm_stats_kernel<kEpiStats><<<p.gm * p.gn, kGThreads, sizeof(GemmSmem), st>>>(p);
+  return true;
+}
+
+// dlogits of rows [0, s) of X (the caller offsets X, targets, lse and
+// grad_rows to a chunk), written as bf16 into dz (row stride ldz elements;
+// global vocabulary column c of a row at dz + c).
+bool launch_gemm_grad(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
+                      long long h, const long long* vocab_start, const long long* targets, long long ignore_index,
+                      const float* lse, const float* grad_rows, float grad, unsigned short* dz, long long ldz,
+                      Header* hdr, int sms, cudaStream_t st) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!make_map(&p.tmx, x, s, h, ld_x, kBM)) return false;
+  for (int i = 0; i < t; ++i) {
+    const long long wi = vocab_start[i + 1] - vocab_start[i];
+    if (!make_map(&p.tmw[i], w[i], wi, h, ld_w, kBN)) return false;
+    p.vstart[i] = int(vocab_start[i]);
+    p.nstart[i + 1] = p.nstart[i] + int((wi + kBN - 1) / kBN);
+  }
+  p.vstart[t] = int(vocab_start[t]);
+  p.t = t;
+  p.s = int(s);
+  p.k_steps = int(h / kBK);
+  p.m_tiles = int((s + kBM - 1) / kBM);
+  p.n_tiles = p.nstart[t];
+  gemm_grid(s, p.n_tiles, sms, &p.gm, &p.gn);
+  p.targets = targets;
+  p.ignore_index = ignore_index;
+  p.hdr = hdr;
+  p.lse = lse;
+  p.grad_rows = grad_rows;
+  p.grad = grad;
+  p.dz = dz;
+  p.ldz = ldz;
+  gemm_stats_kernel<kEpiGrad><<<p.gm * p.gn, kGThreads, sizeof(GemmSmem), st>>>(p);
   return true;
 }
 

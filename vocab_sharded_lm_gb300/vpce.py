@@ -85,6 +85,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.vpce_lmhead_forward.restype = ctypes.c_int
         lib.vpce_lmhead_forward.argtypes = [_P, _I64, _P, _I64, ctypes.c_int, _I64, _I64, _I64P, _P, _I64,
                                             ctypes.c_int, _P, _P, _P, ctypes.c_size_t, _P]
+        lib.vpce_lmhead_backward_workspace_bytes.restype = ctypes.c_size_t
+        lib.vpce_lmhead_backward_workspace_bytes.argtypes = [_I64, _I64]
+        lib.vpce_lmhead_backward.restype = ctypes.c_int
+        lib.vpce_lmhead_backward.argtypes = [_P, _I64, _P, _I64, ctypes.c_int, _I64, _I64, _I64P, _P, _I64,
+                                             ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _I64, _P, _I64, _P,
+                                             ctypes.c_size_t, _P]
         lib.vpce_embedding_forward.restype = ctypes.c_int
         lib.vpce_embedding_forward.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64P, _I64, _I64, _P, _I64, _P,
                                                _I64, _P, _P]
@@ -447,6 +453,51 @@ def vpce_lmhead_forward(hidden, weight_shards, targets, vocab_start=None, *, ign
     if code != VPCE_OK:
         raise VPCEError(code, "vpce_lmhead_forward")
     return result, workspace
+
+
+def vpce_lmhead_backward_workspace_bytes(V: int, h: int) -> int:
+    return int(load_library().vpce_lmhead_backward_workspace_bytes(int(V), int(h)))
+
+
+def vpce_lmhead_backward(hidden, weight_shards, targets, fwd_workspace, vocab_start=None, *,
+                         ignore_index: int = -100, grad_output: float = 1.0, grad_rows=None, grad_hidden=None,
+                         grad_weight_shards=None, workspace=None, stream=None):
+    """dX (bf16, overwritten) and dW_i (fp32, accumulated) of the loss of
+    the preceding :func:`vpce_lmhead_forward` (same inputs, its workspace).
+    Returns ``(grad_hidden, grad_weight_shards)``."""
+    import torch
+
+    s, h = hidden.shape
+    if vocab_start is None:
+        vocab_start = [0]
+        for w in weight_shards:
+            vocab_start.append(vocab_start[-1] + w.shape[0])
+    vocab_start = [int(v) for v in vocab_start]
+    strides = {w.stride(0) for w in weight_shards if w.shape[0] > 1}
+    ld_w = strides.pop() if len(strides) == 1 else h
+    dev = hidden.device
+    if grad_hidden is None:
+        grad_hidden = torch.empty((s, h), dtype=torch.bfloat16, device=dev)
+    if grad_weight_shards is None:
+        grad_weight_shards = [torch.zeros((w.shape[0], h), dtype=torch.float32, device=dev) for w in weight_shards]
+    gstr = {g.stride(0) for g in grad_weight_shards if g.shape[0] > 1}
+    ld_gw = gstr.pop() if len(gstr) == 1 else h
+    if grad_rows is not None:
+        _check_grad_rows(grad_rows, s)
+    if workspace is None:
+        workspace = torch.empty(vpce_lmhead_backward_workspace_bytes(vocab_start[-1], h), dtype=torch.uint8,
+                                device=dev)
+    code = int(load_library().vpce_lmhead_backward(
+        ctypes.c_void_p(hidden.data_ptr()), int(hidden.stride(0) if s > 1 else h),
+        ctypes.cast(_ptr_array([w.data_ptr() for w in weight_shards]), _P), int(ld_w), len(weight_shards), int(s),
+        int(h), _i64_array(vocab_start), ctypes.c_void_p(targets.data_ptr()), int(ignore_index), float(grad_output),
+        _ptr(grad_rows), ctypes.c_void_p(fwd_workspace.data_ptr()), fwd_workspace.numel(),
+        ctypes.c_void_p(grad_hidden.data_ptr()), int(grad_hidden.stride(0) if s > 1 else h),
+        ctypes.cast(_ptr_array([g.data_ptr() for g in grad_weight_shards]), _P), int(ld_gw),
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream)))
+    if code != VPCE_OK:
+        raise VPCEError(code, "vpce_lmhead_backward")
+    return grad_hidden, grad_weight_shards
 
 
 # ----------------------------------------------------------------------------
