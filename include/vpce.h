@@ -128,6 +128,8 @@ vpce_status vpce_forward(const void* const* shards, vpce_dtype dtype, int t, int
  * unmodified (it carries logsumexp, n_valid and the reduction).
  * grad_output is the upstream gradient g of the reduced loss (1.0 normally);
  * after a VPCE_NONE forward it is applied to every row, as VPCE_SUM.
+ * vocab_start[0] may be > 0 when the shards are one process's part of the
+ * vocabulary and the workspace comes from vpce_combine_partials.
  * Padding columns (ld > w_i) are neither read nor written.
  */
 vpce_status vpce_backward(void* const* shards, vpce_dtype dtype, int t, int64_t s,
@@ -150,6 +152,40 @@ vpce_status vpce_backward_rows(void* const* shards, vpce_dtype dtype, int t, int
                                const int64_t* targets, int64_t ignore_index,
                                const float* grad_rows, const void* workspace, size_t workspace_bytes,
                                vpce_stream_t stream);
+
+/*
+ * The two halves of vpce_forward, for shards spread over several processes
+ * (one GPU each), with the exchange in between done by the caller -- the
+ * pages' multi-card method ("Distributed Training III: Model Parallelism",
+ * CMU 11-868 Lecture 16 notes, §5.5; "LLM Internals" §7.3.4): each card
+ * reduces its columns to per-row partials, the cards exchange them, and every
+ * card combines them.
+ *
+ * vpce_partials: this process's shards (vocab_start: t+1 global column
+ * offsets, vocab_start[0] >= 0, the shards' part of the vocabulary) reduced
+ * per (shard, row) to part_out[i * s + r] = (max, sum exp(z - max)) (device
+ * float2 [t][s]) and tgt_out[r] = the target logit when this process holds
+ * the target's column, else 0 (device float [s], cleared here).  workspace
+ * as vpce_forward's (vpce_workspace_bytes(t, s)); other arguments as
+ * vpce_forward.
+ *
+ * vpce_combine_partials: n_part partials [n_part][s] (all processes' part_out
+ * gathered, in a fixed order) and tgt [s] (the sum over processes of tgt_out,
+ * exact since one term per row is non-zero) combined into logsumexp, the row
+ * losses and the reduced loss exactly as vpce_forward's combine (folded in
+ * index order, fp64 batch sum).  V is the whole vocabulary (the bad-target
+ * check).  The workspace is laid out for t_local shards so that
+ * vpce_backward on this process's t_local shards (with their global
+ * vocab_start) reads its logsumexp and n_valid; its header is cleared here.
+ */
+vpce_status vpce_partials(const void* const* shards, vpce_dtype dtype, int t, int64_t s,
+                          const int64_t* vocab_start, int64_t ld, const int64_t* targets,
+                          int64_t ignore_index, float* part_out, float* tgt_out,
+                          void* workspace, size_t workspace_bytes, vpce_stream_t stream);
+vpce_status vpce_combine_partials(const float* part, int n_part, const float* tgt, int64_t s, int64_t V,
+                                  const int64_t* targets, int64_t ignore_index, vpce_reduction reduction,
+                                  float* loss_out, float* row_loss_out, int t_local,
+                                  void* workspace, size_t workspace_bytes, vpce_stream_t stream);
 
 /*
  * Forward and backward in one call: the loss (as vpce_forward) and the shards

@@ -44,10 +44,10 @@ def test_max_over_ranks_gloo_world2():
     procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
     for p in procs:
         p.start()
+    got = dict(q.get(timeout=120) for _ in range(2))
     for p in procs:
-        p.join(120)
+        p.join(60)
         assert p.exitcode == 0
-    got = dict(q.get(timeout=10) for _ in range(2))
     assert got == {0: 15.0, 1: 15.0}
 
 

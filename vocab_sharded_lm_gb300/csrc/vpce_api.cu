@@ -92,16 +92,18 @@ vpce_status device_setup(int* sms) {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Shared validation of the logits description; fills the geometry.
+// from_zero: the shards cover the whole vocabulary (vocab_start[0] = 0);
+// otherwise they may be one rank's part of it (vocab_start[0] >= 0).
 vpce_status check_logits(const void* const* shards, vpce_dtype dtype, int t, int64_t s,
                          const int64_t* vocab_start, int64_t ld, const int64_t* targets, ShardSet* sh,
-                         long long* V) {
+                         long long* V, bool from_zero = true) {
   if (dtype != VPCE_FP32 && dtype != VPCE_BF16) return VPCE_ERR_DTYPE;
   if (t < 1 || t > VPCE_MAX_SHARDS || s < 0 || s > (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
   if (shards == nullptr || vocab_start == nullptr) return VPCE_ERR_INVALID_ARG;
   if (s > 0 && targets == nullptr) return VPCE_ERR_INVALID_ARG;
   if (targets != nullptr && !aligned(targets, 8)) return VPCE_ERR_ALIGNMENT;
   const int eb = dtype == VPCE_BF16 ? 2 : 4;
-  if (vocab_start[0] != 0) return VPCE_ERR_INVALID_ARG;
+  if (from_zero ? vocab_start[0] != 0 : vocab_start[0] < 0) return VPCE_ERR_INVALID_ARG;
   int64_t wmax = 0;
   for (int i = 0; i < t; ++i) {
     const int64_t w = vocab_start[i + 1] - vocab_start[i];
@@ -167,7 +169,7 @@ vpce_status backward_impl(void* const* shards, vpce_dtype dtype, int t, int64_t 
   ShardSet sh;
   long long V = 0;
   vpce_status st = check_logits(reinterpret_cast<const void* const*>(shards), dtype, t, s, vocab_start, ld,
-                                targets, &sh, &V);
+                                targets, &sh, &V, /*from_zero=*/false);
   if (st != VPCE_OK) return st;
   if (!std::isfinite(grad_output)) return VPCE_ERR_INVALID_ARG;
   st = check_workspace(workspace, workspace_bytes, t, s);
@@ -459,6 +461,84 @@ vpce_status vpce_lmhead_forward(const void* hidden, int64_t ld_hidden, const voi
   c.loss_out = loss_out;
   c.row_loss = row_loss_out;
   c.hdr = hdr;
+  const long long blocks = s > 0 ? (s + kCombineThreads - 1) / kCombineThreads : 1;
+  launch_combine(c, int(blocks), cs);
+  return launch_status();
+}
+
+vpce_status vpce_partials(const void* const* shards, vpce_dtype dtype, int t, int64_t s, const int64_t* vocab_start,
+                          int64_t ld, const int64_t* targets, int64_t ignore_index, float* part_out, float* tgt_out,
+                          void* workspace, size_t workspace_bytes, vpce_stream_t stream) {
+  ShardSet sh;
+  long long V = 0;
+  vpce_status st = check_logits(shards, dtype, t, s, vocab_start, ld, targets, &sh, &V, /*from_zero=*/false);
+  if (st != VPCE_OK) return st;
+  if (s > 0 && (part_out == nullptr || tgt_out == nullptr)) return VPCE_ERR_INVALID_ARG;
+  if ((part_out != nullptr && !aligned(part_out, 8)) || (tgt_out != nullptr && !aligned(tgt_out, 4)))
+    return VPCE_ERR_ALIGNMENT;
+  if ((st = check_workspace(workspace, workspace_bytes, t, s)) != VPCE_OK) return st;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != VPCE_OK) return st;
+  if (s == 0) return VPCE_OK;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // rows whose target lies in none of these shards contribute 0 to the sum
+  if (cudaMemsetAsync(tgt_out, 0, sizeof(float) * size_t(s), cs) != cudaSuccess) {
+    cudaGetLastError();
+    return VPCE_ERR_CUDA;
+  }
+  StatsParams p;
+  p.sh = sh;
+  p.s = s;
+  p.units = (long long)t * s;
+  p.targets = reinterpret_cast<const long long*>(targets);
+  p.ignore_index = ignore_index;
+  p.part = reinterpret_cast<float2*>(part_out);
+  p.tgt = tgt_out;
+  p.hdr = reinterpret_cast<Header*>(workspace);
+  const int grid = stream_grid(sms, p.units);
+  if (dtype == VPCE_BF16) launch_stats<__nv_bfloat16>(p, grid, cs);
+  else launch_stats<float>(p, grid, cs);
+  return launch_status();
+}
+
+vpce_status vpce_combine_partials(const float* part, int n_part, const float* tgt, int64_t s, int64_t V,
+                                  const int64_t* targets, int64_t ignore_index, vpce_reduction reduction,
+                                  float* loss_out, float* row_loss_out, int t_local, void* workspace,
+                                  size_t workspace_bytes, vpce_stream_t stream) {
+  if (n_part < 1 || s < 0 || s > (int64_t(1) << 31) || V < 1 || V >= (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  if (t_local < 1 || t_local > VPCE_MAX_SHARDS) return VPCE_ERR_INVALID_ARG;
+  if (s > 0 && (part == nullptr || tgt == nullptr || targets == nullptr)) return VPCE_ERR_INVALID_ARG;
+  if ((part != nullptr && !aligned(part, 8)) || (tgt != nullptr && !aligned(tgt, 4)) ||
+      (targets != nullptr && !aligned(targets, 8)))
+    return VPCE_ERR_ALIGNMENT;
+  vpce_status st = check_outputs(reduction, s, loss_out, row_loss_out);
+  if (st != VPCE_OK) return st;
+  if ((st = check_workspace(workspace, workspace_bytes, t_local, s)) != VPCE_OK) return st;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != VPCE_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // a fresh header: n_valid, error flag and ticket start at zero
+  if (cudaMemsetAsync(workspace, 0, 16, cs) != cudaSuccess) {
+    cudaGetLastError();
+    return VPCE_ERR_CUDA;
+  }
+  const WsLayout L(t_local, s);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  CombineParams c;
+  c.s = s;
+  c.t = n_part;
+  c.V = V;
+  c.targets = reinterpret_cast<const long long*>(targets);
+  c.ignore_index = ignore_index;
+  c.reduction = int(reduction);
+  c.part = reinterpret_cast<const float2*>(part);
+  c.tgt = tgt;
+  c.lse = reinterpret_cast<float*>(ws + L.lse);
+  c.bsum = reinterpret_cast<double*>(ws + L.bsum);
+  c.bcnt = reinterpret_cast<int*>(ws + L.bcnt);
+  c.loss_out = loss_out;
+  c.row_loss = row_loss_out;
+  c.hdr = reinterpret_cast<Header*>(ws);
   const long long blocks = s > 0 ? (s + kCombineThreads - 1) / kCombineThreads : 1;
   launch_combine(c, int(blocks), cs);
   return launch_status();
