@@ -14,16 +14,18 @@ namespace vpce {
 namespace {
 
 struct ChunkCursorB {
-  long long u, u_end;
+  long long u_end;
+  UnitPos pos;
   unsigned off;
   Unit g;
   bool ok;
 
+  // the first unit with chunks at or after the current position
   template <int EB>
-  __device__ __forceinline__ void seek(const BackwardParams& p, long long from) {
+  __device__ __forceinline__ void seek(const BackwardParams& p) {
     ok = false;
-    for (u = from; u < u_end; ++u) {
-      g = make_unit(p.sh, p.s, u, EB);
+    for (; pos.u < u_end; pos.step(p.s)) {
+      g = make_unit_at(p.sh, pos.shard, pos.row, EB);
       if (g.body == 0) continue;
       if (__ldg(p.targets + g.row) == p.ignore_index) continue;
       off = 0;
@@ -34,7 +36,10 @@ struct ChunkCursorB {
   template <int EB>
   __device__ __forceinline__ void next(const BackwardParams& p) {
     off += kChunk;
-    if (off >= g.body) seek<EB>(p, u + 1);
+    if (off >= g.body) {
+      pos.step(p.s);
+      seek<EB>(p);
+    }
   }
   __device__ __forceinline__ unsigned bytes() const { return min(unsigned(kChunk), g.body - off); }
   __device__ __forceinline__ const unsigned char* src() const { return g.addr + g.head + off; }
@@ -71,7 +76,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) backward_kernel(const __grid_c
   // refilled only once its store has finished reading shared memory.
   ChunkCursorB prod;
   prod.u_end = u1;
-  prod.seek<EB>(p, u0);
+  prod.pos.at(u0, p.s);
+  prod.seek<EB>(p);
   unsigned issued = 0;
 #pragma unroll 1
   for (int k = 0; k < kStages - 1 && prod.ok; ++k) {
@@ -85,9 +91,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) backward_kernel(const __grid_c
 
   unsigned kc = 0;
   bool alive = true;
+  UnitPos cur;
+  cur.at(u0, p.s);
 #pragma unroll 1
-  for (long long u = u0; u < u1 && alive; ++u) {
-    const Unit g = make_unit(p.sh, p.s, u, EB);
+  for (; cur.u < u1 && alive; cur.step(p.s)) {
+    const Unit g = make_unit_at(p.sh, cur.shard, cur.row, EB);
     const long long y = __ldg(p.targets + g.row);
     const int hn = int(g.head) / EB, tn = int(g.tail) / EB;
     if (y == p.ignore_index) {

@@ -68,10 +68,12 @@ struct Unit {
   unsigned head, body, tail;
 };
 
-__device__ __forceinline__ Unit make_unit(const ShardSet& sh, long long s, long long u, int elem) {
+// The unit of (shard, row), with no division (streaming kernels walk units
+// in order and carry (shard, row) along: UnitPos).
+__device__ __forceinline__ Unit make_unit_at(const ShardSet& sh, int shard, long long row, int elem) {
   Unit g;
-  g.shard = int(u / s);
-  g.row = u - (long long)g.shard * s;
+  g.shard = shard;
+  g.row = row;
   g.addr = sh.ptr[g.shard] + g.row * sh.ld_bytes[g.shard];
   const unsigned len = unsigned(sh.start[g.shard + 1] - sh.start[g.shard]) * unsigned(elem);
   unsigned head = unsigned((16u - (unsigned(reinterpret_cast<uintptr_t>(g.addr)) & 15u)) & 15u);
@@ -81,6 +83,26 @@ __device__ __forceinline__ Unit make_unit(const ShardSet& sh, long long s, long 
   g.tail = len - head - g.body;
   return g;
 }
+
+// Position u = shard * s + row of a walk over units in order: one division
+// when the walk starts, none per step.
+struct UnitPos {
+  long long u, row;
+  int shard;
+  __device__ __forceinline__ void at(long long u0, long long s) {
+    u = u0;
+    shard = int(u0 / s);
+    row = u0 - (long long)shard * s;
+  }
+  __device__ __forceinline__ void step(long long s) {
+    ++u;
+    if (++row == s) {
+      row = 0;
+      ++shard;
+    }
+  }
+};
+
 
 // ---------------------------------------------------------------------------
 // inline PTX: mbarrier + bulk async copies (sm_90+ forms, valid on sm_103a)

@@ -20,16 +20,18 @@ namespace {
 // Walks the bulk-copy chunks of a warp's units in order: units whose row is
 // ignored or whose aligned body is empty have no chunks.
 struct ChunkCursor {
-  long long u, u_end;
+  long long u_end;
+  UnitPos pos;
   unsigned off;
   Unit g;
   bool ok;
 
+  // the first unit with chunks at or after the current position
   template <int EB>
-  __device__ __forceinline__ void seek(const StatsParams& p, long long from) {
+  __device__ __forceinline__ void seek(const StatsParams& p) {
     ok = false;
-    for (u = from; u < u_end; ++u) {
-      g = make_unit(p.sh, p.s, u, EB);
+    for (; pos.u < u_end; pos.step(p.s)) {
+      g = make_unit_at(p.sh, pos.shard, pos.row, EB);
       if (g.body == 0) continue;
       if (__ldg(p.targets + g.row) == p.ignore_index) continue;
       off = 0;
@@ -40,7 +42,10 @@ struct ChunkCursor {
   template <int EB>
   __device__ __forceinline__ void next(const StatsParams& p) {
     off += kChunk;
-    if (off >= g.body) seek<EB>(p, u + 1);
+    if (off >= g.body) {
+      pos.step(p.s);
+      seek<EB>(p);
+    }
   }
   __device__ __forceinline__ unsigned bytes() const { return min(unsigned(kChunk), g.body - off); }
   __device__ __forceinline__ const unsigned char* src() const { return g.addr + g.head + off; }
@@ -74,7 +79,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) partial_stats_kernel(const __g
 
   ChunkCursor prod;
   prod.u_end = u1;
-  prod.seek<EB>(p, u0);
+  prod.pos.at(u0, p.s);
+  prod.seek<EB>(p);
   unsigned issued = 0;
 #pragma unroll 1
   for (int k = 0; k < kStages && prod.ok; ++k) {
@@ -88,9 +94,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) partial_stats_kernel(const __g
 
   unsigned kc = 0;
   bool alive = true;
+  UnitPos cur;
+  cur.at(u0, p.s);
 #pragma unroll 1
-  for (long long u = u0; u < u1 && alive; ++u) {
-    const Unit g = make_unit(p.sh, p.s, u, EB);
+  for (; cur.u < u1 && alive; cur.step(p.s)) {
+    const Unit g = make_unit_at(p.sh, cur.shard, cur.row, EB);
     const long long y = __ldg(p.targets + g.row);
     if (y == p.ignore_index) continue;
     const long long lo = p.sh.start[g.shard], hi = p.sh.start[g.shard + 1];
