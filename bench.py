@@ -663,7 +663,7 @@ def run_lmhead(args):
             "l2": f"inputs larger than L2: the head is {sum(w.numel() for w in ws) * 2 / 1e9:.2f} GB",
             "path": "vpce_lmhead_forward (tcgen05 GEMM, fp32 accumulators in TMEM, loss statistics in the "
                     "epilogue; the logits are never written), then the shard combine"
-                    + ("; vpce_lmhead_backward (per 1024-row chunk: tcgen05 recompute writing bf16 dZ, then "
+                    + ("; vpce_lmhead_backward (per 4096-row chunk: tcgen05 recompute writing bf16 dZ, then "
                        "cuBLAS dX = dZ W and dW += dZ^T X)" if train else ""),
         },
         "tflops": round(achieved, 1),
@@ -691,7 +691,7 @@ def run_lmhead(args):
             "note": "pinned host hidden states + targets copied in every step (copy stream, double-buffered), "
                     "loss read back; the head's weights stay on the device",
         },
-        "gpu_launches": (2 + (m.s + 1023) // 1024 * 2 if train else 2) * args.steps,
+        "gpu_launches": (2 + (m.s + 4095) // 4096 * 2 if train else 2) * args.steps,
         "clocks": clk,
     }
     if train:

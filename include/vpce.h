@@ -303,7 +303,7 @@ vpce_status vpce_lmhead_forward(const void* hidden, int64_t ld_hidden,
  *     grad_hidden         = dZ W              bf16 [s, h], overwritten
  *     grad_weight_shards[i] += dZ_i^T X       fp32 [w_i, h], accumulated
  * The logits are formed again tile by tile on the tensor cores (the forward
- * kept none) and written as bf16 dZ for one chunk of 1024 rows at a time into
+ * kept none) and written as bf16 dZ for one chunk of rows at a time into
  * `workspace`; the two products are plain cuBLAS GEMMs (bf16 in, fp32
  * accumulate).  Every argument describing X, the head, the targets and
  * fwd_workspace must be the preceding vpce_lmhead_forward's, unmodified
@@ -313,8 +313,11 @@ vpce_status vpce_lmhead_forward(const void* hidden, int64_t ld_hidden,
  *   grad_hidden     device bf16 [s, h], row stride ld_grad_hidden (0 = h).
  *   grad_weight_shards  host array of t device float pointers, [w_i, h],
  *                   row stride ld_grad_weight (0 = h), 16-byte aligned.
- *   workspace       vpce_lmhead_backward_workspace_bytes(V, h) bytes,
- *                   256-byte aligned (dZ of one chunk and an fp32 dX chunk).
+ *   workspace       256-byte aligned; vpce_lmhead_backward_workspace_bytes(V, h)
+ *                   bytes give 4096-row chunks (dZ of one chunk and an fp32
+ *                   dX chunk).  A smaller workspace gives smaller chunks, in
+ *                   steps of 128 rows; less than 128 rows' worth returns
+ *                   VPCE_ERR_WORKSPACE.
  * The cuBLAS handle is created once per device on first use and owns its
  * own workspace; calls on one device are serialised on it.
  */

@@ -177,7 +177,13 @@ def _bwd_bound(dz, mat, ref, K):
     return a + 2.0 ** -8 * (np.abs(ref) + a) + 1e-30
 
 
-def _check_backward(m, vs=None, *, reduction="mean", grad=1.0, grad_rows=None):
+def _bwd_workspace(V, h, rows):
+    """Backward workspace sized for chunks of `rows` rows (forces several chunks)."""
+    r256 = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    return torch.empty(r256(rows * ((V + 7) // 8 * 8) * 2) + r256(rows * h * 4), dtype=torch.uint8, device="cuda")
+
+
+def _check_backward(m, vs=None, *, reduction="mean", grad=1.0, grad_rows=None, chunk_rows=None):
     vs = synth.even_vocab_start(m.V, m.t) if vs is None else list(vs)
     meta = synth.lmhead_meta(m)
     x, ws = synth.lmhead_device(m, vs)
@@ -187,8 +193,9 @@ def _check_backward(m, vs=None, *, reduction="mean", grad=1.0, grad_rows=None):
                                       row_loss_out=rl)
     gw0 = [torch.full((w.shape[0], m.h), 0.5, dtype=torch.float32, device="cuda") for w in ws]
     gr = torch.from_numpy(np.asarray(grad_rows, dtype=np.float32)).cuda() if grad_rows is not None else None
+    bwk = _bwd_workspace(m.V, m.h, chunk_rows) if chunk_rows else None
     dx, dw = vpce.vpce_lmhead_backward(x, ws, y, fwk, vs, ignore_index=m.ignore_index, grad_output=grad,
-                                       grad_rows=gr, grad_weight_shards=gw0)
+                                       grad_rows=gr, grad_weight_shards=gw0, workspace=bwk)
     torch.cuda.synchronize()
     xh, wh = _host(m, vs)
     if grad_rows is not None:
@@ -206,14 +213,15 @@ def _check_backward(m, vs=None, *, reduction="mean", grad=1.0, grad_rows=None):
         got_w = dw[i].cpu().numpy().astype(np.float64) - 0.5
         dzi = dz[:, vs[i]:vs[i + 1]]
         # plus one fp32 rounding of the accumulation onto 0.5 per row chunk
-        chunks = (m.s + 1023) // 1024
-        bw = _bwd_bound(dzi.T, X, np.zeros_like(ref_w[i]), min(m.s, 1024)) + chunks * 2.0 ** -24 * (0.5 + np.abs(ref_w[i]))
+        rows = chunk_rows or 4096
+        chunks = (m.s + rows - 1) // rows
+        bw = _bwd_bound(dzi.T, X, np.zeros_like(ref_w[i]), min(m.s, rows)) + chunks * 2.0 ** -24 * (0.5 + np.abs(ref_w[i]))
         assert np.all(np.abs(got_w - ref_w[i]) <= bw), (i, np.max(np.abs(got_w - ref_w[i]) / bw))
 
 
 @pytest.mark.parametrize("m,vs", [
     (synth.LMHEADS["lmhead_s300_h512_v5000"], None),                    # ragged tiles, ignored rows
-    (synth.LmHead("bwd_chunks", 17, 1200, 128, 700, 7, ignore_frac=0.1), None),  # two row chunks
+    (synth.LmHead("bwd_chunks", 17, 1200, 128, 700, 7, ignore_frac=0.1), None),  # several M tiles, one chunk
     (synth.LmHead("bwd_uneven", 18, 130, 64, 600, 3), [0, 1, 300, 600]),  # one-column shard
 ])
 def test_lmhead_backward_parity(m, vs):
@@ -226,3 +234,8 @@ def test_lmhead_backward_sum_and_per_row_gradients():
     g = np.random.default_rng(2).normal(size=m.s).astype(np.float32)
     g[::9] = 0.0
     _check_backward(m, reduction="none", grad_rows=g)
+
+
+def test_lmhead_backward_small_workspace_chunks():
+    # a workspace for 128-row chunks: 1200 rows run as 10 chunks, dW accumulated across them
+    _check_backward(synth.LmHead("bwd_small_ws", 22, 1200, 128, 700, 7, ignore_frac=0.1), chunk_rows=128)

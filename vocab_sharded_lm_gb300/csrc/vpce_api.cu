@@ -20,11 +20,12 @@ void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long
 cudaError_t set_gemm_smem();
 cudaError_t set_embed_smem();
 size_t lmhead_bwd_workspace_bytes(long long V, long long h);
+size_t lmhead_bwd_min_workspace_bytes(long long V, long long h);
 vpce_status lmhead_backward_run(const void* x, long long ld_x, const void* const* w, long long ld_w, int t,
                                 long long s, long long h, const long long* vs, const long long* targets,
                                 long long ignore_index, float grad, const float* grad_rows, const float* lse,
                                 Header* hdr, void* dx, long long ld_dx, float* const* dw, long long ld_dw, void* ws,
-                                int sms, cudaStream_t st);
+                                size_t ws_bytes, int sms, cudaStream_t st);
 size_t embed_bwd_workspace_bytes();
 void launch_embed_forward(const ShardSet& sh, int t, long long V, long long h, int eb, const long long* ids,
                           long long s, void* out, long long ld_out, int* flag, int sms, cudaStream_t st);
@@ -586,7 +587,7 @@ vpce_status vpce_lmhead_backward(const void* hidden, int64_t ld_hidden, const vo
   if (fwd_workspace == nullptr || workspace == nullptr) return VPCE_ERR_INVALID_ARG;
   if (!aligned(fwd_workspace, 256) || !aligned(workspace, 256)) return VPCE_ERR_ALIGNMENT;
   if (fwd_workspace_bytes < WsLayout(VPCE_LMHEAD_MAX_GROUPS, s).total ||
-      workspace_bytes < lmhead_bwd_workspace_bytes(vocab_start[t], h))
+      workspace_bytes < lmhead_bwd_min_workspace_bytes(vocab_start[t], h))
     return VPCE_ERR_WORKSPACE;
   int sms = 0;
   vpce_status st = device_setup(&sms);
@@ -599,7 +600,8 @@ vpce_status vpce_lmhead_backward(const void* hidden, int64_t ld_hidden, const vo
                              reinterpret_cast<const long long*>(targets), ignore_index, grad_output, grad_rows,
                              reinterpret_cast<const float*>(fws + L.lse),
                              reinterpret_cast<Header*>(const_cast<unsigned char*>(fws)), grad_hidden, ldgx,
-                             grad_weight_shards, ldgw, workspace, g_sms, reinterpret_cast<cudaStream_t>(stream));
+                             grad_weight_shards, ldgw, workspace, workspace_bytes, g_sms,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 // Shard geometry of a [w_i, h] table split by vocabulary (row stride ld

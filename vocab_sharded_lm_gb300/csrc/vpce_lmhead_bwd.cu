@@ -6,9 +6,10 @@
 // forward's logsumexp and n_valid); then two plain GEMMs through cuBLAS give
 //     dX[chunk]  = sum_i dZ_i W_i          (fp32, then rounded to bf16)
 //     dW_i      += dZ_i^T X[chunk]         (fp32, accumulated)
-// The chunk bounds the dZ scratch to kBwdRows x V bf16 (263 MB at
-// V = 128256), the "do not assemble the big tensor" of the CMU notes (§5.5)
-// applied to the gradient.
+// The chunk bounds the dZ scratch to rows x V bf16 (1.05 GB for the default
+// 4096 rows at V = 128256; a smaller workspace gives smaller chunks, down to
+// 128 rows), the "do not assemble the big tensor" of the CMU notes (§5.5)
+// applied to the gradient.  Larger chunks give cuBLAS larger products.
 #include <cublas_v2.h>
 
 #include <mutex>
@@ -24,7 +25,8 @@ bool launch_gemm_grad(const void* x, long long ld_x, const void* const* w, long 
 
 namespace {
 
-constexpr long long kBwdRows = 1024;
+constexpr long long kBwdRows = 4096;  // rows per chunk with the suggested workspace
+constexpr long long kMinBwdRows = 128;
 
 __global__ void f32_to_bf16_rows(const float* src, long long lds, __nv_bfloat16* dst, long long ldd, long long rows,
                                  long long cols) {
@@ -50,12 +52,21 @@ cublasHandle_t blas_handle(int dev) {
 
 }  // namespace
 
-long long lmhead_bwd_rows() { return kBwdRows; }
-
 long long lmhead_bwd_ldz(long long V) { return (V + 7) / 8 * 8; }
 
-size_t lmhead_bwd_workspace_bytes(long long V, long long h) {
-  return round256(size_t(kBwdRows) * size_t(lmhead_bwd_ldz(V)) * 2u) + round256(size_t(kBwdRows) * size_t(h) * 4u);
+size_t lmhead_bwd_bytes_for(long long rows, long long V, long long h) {
+  return round256(size_t(rows) * size_t(lmhead_bwd_ldz(V)) * 2u) + round256(size_t(rows) * size_t(h) * 4u);
+}
+
+size_t lmhead_bwd_workspace_bytes(long long V, long long h) { return lmhead_bwd_bytes_for(kBwdRows, V, h); }
+size_t lmhead_bwd_min_workspace_bytes(long long V, long long h) { return lmhead_bwd_bytes_for(kMinBwdRows, V, h); }
+
+// The largest chunk (a multiple of kMinBwdRows, at most kBwdRows) whose
+// scratch fits in `bytes`.
+long long lmhead_bwd_rows_for(size_t bytes, long long V, long long h) {
+  long long r = kBwdRows;
+  while (r > kMinBwdRows && lmhead_bwd_bytes_for(r, V, h) > bytes) r -= kMinBwdRows;
+  return r;
 }
 
 // Returns VPCE_OK, VPCE_ERR_CUDA (a launch or a cuBLAS call failed).
@@ -63,7 +74,7 @@ vpce_status lmhead_backward_run(const void* x, long long ld_x, const void* const
                                 long long s, long long h, const long long* vs, const long long* targets,
                                 long long ignore_index, float grad, const float* grad_rows, const float* lse,
                                 Header* hdr, void* dx, long long ld_dx, float* const* dw, long long ld_dw, void* ws,
-                                int sms, cudaStream_t st) {
+                                size_t ws_bytes, int sms, cudaStream_t st) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
@@ -74,12 +85,13 @@ vpce_status lmhead_backward_run(const void* x, long long ld_x, const void* const
   if (hb == nullptr || cublasSetStream(hb, st) != CUBLAS_STATUS_SUCCESS) return VPCE_ERR_CUDA;
   const long long V = vs[t];
   const long long ldz = lmhead_bwd_ldz(V);
+  const long long rows = lmhead_bwd_rows_for(ws_bytes, V, h);
   unsigned short* dz = static_cast<unsigned short*>(ws);
   float* dx32 = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) +
-                                         round256(size_t(kBwdRows) * size_t(ldz) * 2u));
+                                         round256(size_t(rows) * size_t(ldz) * 2u));
   const float one = 1.f, zero = 0.f;
-  for (long long r0 = 0; r0 < s; r0 += kBwdRows) {
-    const long long R = s - r0 < kBwdRows ? s - r0 : kBwdRows;
+  for (long long r0 = 0; r0 < s; r0 += rows) {
+    const long long R = s - r0 < rows ? s - r0 : rows;
     const unsigned char* xr = static_cast<const unsigned char*>(x) + r0 * ld_x * 2;
     if (!launch_gemm_grad(xr, ld_x, w, ld_w, t, R, h, vs, targets + r0, ignore_index, lse + r0,
                           grad_rows != nullptr ? grad_rows + r0 : nullptr, grad, dz, ldz, hdr, sms, st))
