@@ -132,10 +132,15 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # traffic recorded by ncu for the dominant kernel (per launch), if still current
 # ----------------------------------------------------------------------------
-def _kernel_source_hash():
+# the source file of each kernel whose ncu traffic is recorded; the shared
+# device headers count for all of them
+_KERNEL_FILES = {"stream_fused_kernel": "vpce_fused.cu", "backward_kernel": "vpce_backward.cu",
+                 "partial_stats_kernel": "vpce_forward.cu"}
+
+
+def _kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in ("vpce_device.cuh", "vpce_kernels.cuh", "vpce_chunk.cuh", "vpce_forward.cu", "vpce_backward.cu",
-              "vpce_fused.cu"):
+    for f in ("vpce_device.cuh", "vpce_kernels.cuh", "vpce_chunk.cuh", _KERNEL_FILES[kernel]):
         with open(os.path.join(ROOT, "vocab_sharded_lm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -149,7 +154,7 @@ def _ncu_traffic(kernel: str, workload: str):
     except Exception:
         return None
     ent = d.get(kernel, {}).get(workload)
-    if not ent or ent.get("source_hash") != _kernel_source_hash():
+    if not ent or ent.get("source_hash") != _kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
