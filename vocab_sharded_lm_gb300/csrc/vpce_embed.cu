@@ -11,8 +11,9 @@
 //
 // The backward (not on the pages; the adjoint of the lookup) adds each
 // output-gradient row into the table row of its id.  It is deterministic:
-// a single CTA sorts the (id, row) pairs of up to kEmbChunk rows in shared
-// memory (bitonic), marks where each id's run starts, and one warp per
+// the (id, row) pairs of up to kEmbChunk rows are sorted (each CTA sorts 1024
+// of them in shared memory, bitonic, then merge-path rounds double the sorted
+// width), one CTA marks where each id's run starts, and one warp per
 // (distinct id, 128 columns) then sums the id's rows in ascending row order
 // and adds the sum into the fp32 gradient table.  Longer batches run chunk after chunk on
 // the stream, so the accumulation order is fixed.
@@ -119,49 +120,81 @@ __global__ void __launch_bounds__(kEmbThreads) embed_forward_kernel(const __grid
 // ---------------------------------------------------------------------------
 // backward
 // ---------------------------------------------------------------------------
-struct EmbedSortParams {
-  const long long* ids;  // this chunk's ids
-  int n;                 // rows in this chunk (<= kEmbChunk)
-  int n_pow2;            // n rounded up to a power of two (>= 2)
-  long long V;
-  unsigned long long* keys;  // [kEmbChunk] sorted (id << 32 | row), kNoKey past the valid ones
-  int* seg;                  // [kEmbChunk + 1] start of each distinct id's run; seg[n_seg] = end
-  int* n_seg;
-  int* heavy;                // [kEmbChunk / kHeavyRows] runs longer than kHeavyRows (any order)
-  int* n_heavy;
-};
+constexpr int kSortBlock = 1024;  // keys sorted by one CTA before the merge rounds
 
-// One CTA: bitonic sort of the chunk's (id, row) keys in shared memory, then
-// the start of every run of equal ids (ids outside [0, V) sort last and are
-// dropped).
-__global__ void __launch_bounds__(kSortThreads) embed_sort_kernel(const EmbedSortParams p) {
-  extern __shared__ unsigned long long key[];
-  __shared__ int warp_sum[kSortThreads / 32];
-  const int tid = threadIdx.x;
-  for (int k = tid; k < p.n_pow2; k += kSortThreads) {
+// One CTA per kSortBlock keys: this block's (id << 32 | row) keys (kNoKey for
+// padding and for ids outside [0, V)), bitonic-sorted in shared memory.
+__global__ void __launch_bounds__(kSortBlock / 2) embed_block_sort_kernel(const long long* ids, int n, int n_pow2,
+                                                                          long long V, unsigned long long* out) {
+  __shared__ unsigned long long key[kSortBlock];
+  const int len = n_pow2 < kSortBlock ? n_pow2 : kSortBlock;
+  const int base = blockIdx.x * len;
+  for (int k = threadIdx.x; k < len; k += blockDim.x) {
+    const int g = base + k;
     unsigned long long v = kNoKey;
-    if (k < p.n) {
-      const long long id = p.ids[k];
-      if (id >= 0 && id < p.V) v = (static_cast<unsigned long long>(id) << 32) | unsigned(k);
+    if (g < n) {
+      const long long id = ids[g];
+      if (id >= 0 && id < V) v = (static_cast<unsigned long long>(id) << 32) | unsigned(g);
     }
     key[k] = v;
   }
   __syncthreads();
-  for (int size = 2; size <= p.n_pow2; size <<= 1) {
+  for (int size = 2; size <= len; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int k = tid; k < p.n_pow2 / 2; k += kSortThreads) {
+      for (int k = threadIdx.x; k < len / 2; k += blockDim.x) {
         const int lo = 2 * k - (k & (stride - 1));  // first element of this compare pair
         const int hi = lo + stride;
         const bool up = (lo & size) == 0;
-        const unsigned long long a = key[lo], b = key[hi];
-        if ((a > b) == up) {
-          key[lo] = b;
-          key[hi] = a;
+        const unsigned long long x = key[lo], y = key[hi];
+        if ((x > y) == up) {
+          key[lo] = y;
+          key[hi] = x;
         }
       }
       __syncthreads();
     }
   }
+  for (int k = threadIdx.x; k < len; k += blockDim.x) out[base + k] = key[k];
+}
+
+// One merge round: pairs of sorted runs of `width` keys become runs of
+// 2 * width.  Each key's place is its index in its own run plus the number of
+// keys of the partner run before it (a binary search; keys of the first run
+// go before equal keys of the second, so the padding keys stay in order).
+__global__ void embed_merge_kernel(const unsigned long long* in, unsigned long long* out, int width, int total) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  const int pair = i / (2 * width), base = pair * 2 * width;
+  const int j = i - base;
+  const bool first = j < width;
+  const int own = first ? j : j - width;
+  const unsigned long long* other = in + base + (first ? width : 0);
+  const unsigned long long v = in[i];
+  int lo = 0, hi = width;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (first ? (other[mid] < v) : (other[mid] <= v)) lo = mid + 1;
+    else hi = mid;
+  }
+  out[base + own + lo] = v;
+}
+
+struct EmbedRunsParams {
+  const unsigned long long* keys;  // [n_pow2] sorted
+  int n_pow2;
+  int* seg;                        // [kEmbChunk + 1] start of each distinct id's run; seg[n_seg] = end
+  int* n_seg;
+  int* heavy;                      // [kEmbChunk / kHeavyRows] runs longer than kHeavyRows (any order)
+  int* n_heavy;
+};
+
+// One CTA: the start of every run of equal ids in the sorted keys (ids outside
+// [0, V) sorted last as kNoKey and are dropped), and the list of long runs.
+__global__ void __launch_bounds__(kSortThreads) embed_runs_kernel(const EmbedRunsParams p) {
+  __shared__ int warp_sum[kSortThreads / 32];
+  __shared__ int nh;
+  const int tid = threadIdx.x;
+  const unsigned long long* key = p.keys;
   // run heads: a valid key whose id differs from its predecessor's
   const int per = (p.n_pow2 + kSortThreads - 1) / kSortThreads;
   const int k0 = tid * per;
@@ -179,6 +212,7 @@ __global__ void __launch_bounds__(kSortThreads) embed_sort_kernel(const EmbedSor
     if (lane >= o) incl += x;
   }
   if (lane == 31) warp_sum[warp] = incl;
+  if (tid == 0) nh = 0;
   __syncthreads();
   if (warp == 0) {
     int w = warp_sum[lane];
@@ -195,9 +229,8 @@ __global__ void __launch_bounds__(kSortThreads) embed_sort_kernel(const EmbedSor
     const unsigned long long v = key[k];
     if (v != kNoKey && (k == 0 || (key[k - 1] >> 32) != (v >> 32))) p.seg[pos++] = k;
   }
-  for (int k = tid; k < p.n_pow2 && k < kEmbChunk; k += kSortThreads) p.keys[k] = key[k];
+  const int total = warp_sum[kSortThreads / 32 - 1];
   if (tid == kSortThreads - 1) {
-    const int total = warp_sum[kSortThreads / 32 - 1];
     *p.n_seg = total;
     // end of the last run: the number of valid keys, i.e. the first kNoKey
     // of the sorted array (binary search)
@@ -209,12 +242,9 @@ __global__ void __launch_bounds__(kSortThreads) embed_sort_kernel(const EmbedSor
     }
     p.seg[total] = lo;
   }
+  __syncthreads();  // seg[] (global) is complete and visible to the block
   // the long runs, listed for the CTA-per-chunk kernel (their order does not
   // matter: each run's sum is formed on its own)
-  __shared__ int nh;
-  if (tid == 0) nh = 0;
-  __syncthreads();  // seg[] (global) is complete and visible to the block
-  const int total = warp_sum[kSortThreads / 32 - 1];
   for (int j = tid; j < total; j += kSortThreads)
     if (p.seg[j + 1] - p.seg[j] > kHeavyRows) p.heavy[atomicAdd(&nh, 1)] = j;
   __syncthreads();
@@ -244,56 +274,81 @@ __device__ __forceinline__ float4 grad4(const EmbedAccParams& p, int row, long l
   return *reinterpret_cast<const float4*>(base + c * 4);
 }
 
-// Work items are (distinct id, 128-column chunk) pairs, one warp each: the
-// chunk's sum over the id's rows in ascending row order (eight rows loaded
-// ahead, added in order), then one add into the id's row of the gradient
-// table.  Splitting by columns spreads a frequent id over many warps; the
-// order of the additions does not depend on the split.
+// Work items are (short run, 512 columns) pairs, one warp each: four
+// 128-column chunks at once (four float4 accumulators per lane), the run's
+// rows in ascending order two at a time, so eight independent loads are in
+// flight per lane; then one add into the id's row of the gradient table.
+// The order of the additions per element does not depend on the grouping.
 __global__ void __launch_bounds__(kEmbThreads) embed_accum_kernel(const __grid_constant__ EmbedAccParams p) {
   __shared__ long long start[VPCE_MAX_SHARDS + 1];
   for (int i = threadIdx.x; i <= p.t; i += kEmbThreads) start[i] = p.gsh.start[i];
   __syncthreads();
   const int lane = threadIdx.x & 31;
+  constexpr int kU = 4;  // 128-column chunks per task
   const long long nseg = *p.n_seg;
-  const long long nch = (p.h + 127) / 128;
-  const long long tasks = nseg * nch;
+  const long long ngrp = (p.h + 128 * kU - 1) / (128 * kU);
+  const long long tasks = nseg * ngrp;
   const long long nwarps = (long long)gridDim.x * (kEmbThreads / 32);
   for (long long q = (long long)blockIdx.x * (kEmbThreads / 32) + (threadIdx.x >> 5); q < tasks; q += nwarps) {
-    const long long sgi = q / nch;
-    const long long c = (q - sgi * nch) * 128 + 4 * lane;
+    const long long sgi = q / ngrp;
+    const long long c0 = (q - sgi * ngrp) * (128 * kU) + 4 * lane;
     const int a = p.seg[sgi], b = p.seg[sgi + 1];
-    if (c >= p.h || b - a > kHeavyRows) continue;  // long runs: embed_heavy_kernel
+    if (b - a > kHeavyRows) continue;  // long runs: embed_heavy_kernel
+    bool in[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) in[u] = c0 + 128 * u < p.h;
+    float4 acc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    int k = a;
+    for (; k + 2 <= b; k += 2) {
+      const int r0 = int(p.keys[k] & 0xffffffffu), r1 = int(p.keys[k + 1] & 0xffffffffu);
+      float4 g0[kU], g1[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        g0[u] = in[u] ? grad4(p, r0, c0 + 128 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+        g1[u] = in[u] ? grad4(p, r1, c0 + 128 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        acc[u].x += g0[u].x;
+        acc[u].y += g0[u].y;
+        acc[u].z += g0[u].z;
+        acc[u].w += g0[u].w;
+        acc[u].x += g1[u].x;
+        acc[u].y += g1[u].y;
+        acc[u].z += g1[u].z;
+        acc[u].w += g1[u].w;
+      }
+    }
+    if (k < b) {
+      const int r0 = int(p.keys[k] & 0xffffffffu);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const float4 g = in[u] ? grad4(p, r0, c0 + 128 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+        acc[u].x += g.x;
+        acc[u].y += g.y;
+        acc[u].z += g.z;
+        acc[u].w += g.w;
+      }
+    }
     const long long id = static_cast<long long>(p.keys[a] >> 32);
     const int i = shard_of(start, p.t, id);
     float* dst = reinterpret_cast<float*>(const_cast<unsigned char*>(p.gsh.ptr[i]) +
-                                          (id - start[i]) * p.gsh.ld_bytes[i]) + c;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int k = a;
-    for (; k + 8 <= b; k += 8) {
-      float4 g[8];
+                                          (id - start[i]) * p.gsh.ld_bytes[i]) + c0;
+    float4 o[kU];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) g[u] = grad4(p, int(p.keys[k + u] & 0xffffffffu), c);
+    for (int u = 0; u < kU; ++u)
+      if (in[u]) o[u] = *reinterpret_cast<const float4*>(dst + 128 * u);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        acc.x += g[u].x;
-        acc.y += g[u].y;
-        acc.z += g[u].z;
-        acc.w += g[u].w;
+    for (int u = 0; u < kU; ++u)
+      if (in[u]) {
+        o[u].x += acc[u].x;
+        o[u].y += acc[u].y;
+        o[u].z += acc[u].z;
+        o[u].w += acc[u].w;
+        *reinterpret_cast<float4*>(dst + 128 * u) = o[u];
       }
-    }
-    for (; k < b; ++k) {
-      const float4 g = grad4(p, int(p.keys[k] & 0xffffffffu), c);
-      acc.x += g.x;
-      acc.y += g.y;
-      acc.z += g.z;
-      acc.w += g.w;
-    }
-    float4 o = *reinterpret_cast<float4*>(dst);
-    o.x += acc.x;
-    o.y += acc.y;
-    o.z += acc.z;
-    o.w += acc.w;
-    *reinterpret_cast<float4*>(dst) = o;
   }
 }
 
@@ -369,14 +424,11 @@ __global__ void __launch_bounds__(kEmbThreads) embed_heavy_kernel(const __grid_c
 }  // namespace
 
 size_t embed_bwd_workspace_bytes() {
-  return round256(sizeof(unsigned long long) * kEmbChunk) + round256(sizeof(int) * (kEmbChunk + 1)) +
+  return 2 * round256(sizeof(unsigned long long) * kEmbChunk) + round256(sizeof(int) * (kEmbChunk + 1)) +
          round256(sizeof(int) * (kEmbChunk / kHeavyRows)) + 256;
 }
 
-cudaError_t set_embed_smem() {
-  return cudaFuncSetAttribute(embed_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(sizeof(unsigned long long) * kEmbChunk));
-}
+cudaError_t set_embed_smem() { return cudaSuccess; }
 
 void launch_embed_forward(const ShardSet& sh, int t, long long V, long long h, int eb, const long long* ids,
                           long long s, void* out, long long ld_out, int* flag, int sms, cudaStream_t st) {
@@ -401,12 +453,12 @@ cudaError_t launch_embed_backward(const void* grad, int grad_bf16, long long ld_
                                   long long s, const ShardSet& gsh, int t, long long V, long long h, void* ws,
                                   int sms, cudaStream_t st) {
   unsigned char* w = static_cast<unsigned char*>(ws);
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(w);
-  int* seg = reinterpret_cast<int*>(w + round256(sizeof(unsigned long long) * kEmbChunk));
-  int* heavy = reinterpret_cast<int*>(w + round256(sizeof(unsigned long long) * kEmbChunk) +
-                                      round256(sizeof(int) * (kEmbChunk + 1)));
-  int* n_seg = reinterpret_cast<int*>(w + round256(sizeof(unsigned long long) * kEmbChunk) +
-                                      round256(sizeof(int) * (kEmbChunk + 1)) +
+  const size_t kb = round256(sizeof(unsigned long long) * kEmbChunk);
+  unsigned long long* keys_a = reinterpret_cast<unsigned long long*>(w);
+  unsigned long long* keys_b = reinterpret_cast<unsigned long long*>(w + kb);
+  int* seg = reinterpret_cast<int*>(w + 2 * kb);
+  int* heavy = reinterpret_cast<int*>(w + 2 * kb + round256(sizeof(int) * (kEmbChunk + 1)));
+  int* n_seg = reinterpret_cast<int*>(w + 2 * kb + round256(sizeof(int) * (kEmbChunk + 1)) +
                                       round256(sizeof(int) * (kEmbChunk / kHeavyRows)));
   int* n_heavy = n_seg + 1;
   const int eb = grad_bf16 ? 2 : 4;
@@ -414,17 +466,26 @@ cudaError_t launch_embed_backward(const void* grad, int grad_bf16, long long ld_
     const int n = int(s - r0 < kEmbChunk ? s - r0 : kEmbChunk);
     int n2 = 2;
     while (n2 < n) n2 <<= 1;
-    EmbedSortParams sp;
-    sp.ids = ids + r0;
-    sp.n = n;
-    sp.n_pow2 = n2;
-    sp.V = V;
-    sp.keys = keys;
-    sp.seg = seg;
-    sp.n_seg = n_seg;
-    sp.heavy = heavy;
-    sp.n_heavy = n_heavy;
-    embed_sort_kernel<<<1, kSortThreads, sizeof(unsigned long long) * n2, st>>>(sp);
+    // sort: blocks of kSortBlock keys, then merge rounds (ping-pong buffers)
+    const int blk = n2 < kSortBlock ? n2 : kSortBlock;
+    embed_block_sort_kernel<<<n2 / blk, kSortBlock / 2, 0, st>>>(ids + r0, n, n2, V, keys_a);
+    unsigned long long* cur = keys_a;
+    unsigned long long* nxt = keys_b;
+    for (int width = blk; width < n2; width <<= 1) {
+      embed_merge_kernel<<<(n2 + 255) / 256, 256, 0, st>>>(cur, nxt, width, n2);
+      unsigned long long* tmp = cur;
+      cur = nxt;
+      nxt = tmp;
+    }
+    unsigned long long* keys = cur;
+    EmbedRunsParams rp;
+    rp.keys = keys;
+    rp.n_pow2 = n2;
+    rp.seg = seg;
+    rp.n_seg = n_seg;
+    rp.heavy = heavy;
+    rp.n_heavy = n_heavy;
+    embed_runs_kernel<<<1, kSortThreads, 0, st>>>(rp);
     EmbedAccParams ap;
     ap.keys = keys;
     ap.seg = seg;
@@ -437,7 +498,7 @@ cudaError_t launch_embed_backward(const void* grad, int grad_bf16, long long ld_
     ap.h = h;
     ap.gsh = gsh;
     ap.t = t;
-    const long long want = ((long long)n * ((h + 127) / 128) + kEmbThreads / 32 - 1) / (kEmbThreads / 32);
+    const long long want = ((long long)n * ((h + 511) / 512) + kEmbThreads / 32 - 1) / (kEmbThreads / 32);
     const long long cap = (long long)sms * 8;
     embed_accum_kernel<<<int(want < cap ? want : cap), kEmbThreads, 0, st>>>(ap);
     const long long hwant = (long long)(n / (kHeavyRows + 1) + 1) * ((h + 127) / 128);
