@@ -314,12 +314,14 @@ vpce_status vpce_lmhead_forward(const void* hidden, int64_t ld_hidden,
  *   grad_weight_shards  host array of t device float pointers, [w_i, h],
  *                   row stride ld_grad_weight (0 = h), 16-byte aligned.
  *   workspace       256-byte aligned; vpce_lmhead_backward_workspace_bytes(V, h)
- *                   bytes give 4096-row chunks (dZ of one chunk and an fp32
- *                   dX chunk).  A smaller workspace gives smaller chunks, in
- *                   steps of 128 rows; less than 128 rows' worth returns
- *                   VPCE_ERR_WORKSPACE.
- * The cuBLAS handle is created once per device on first use and owns its
- * own workspace; calls on one device are serialised on it.
+ *                   bytes give 4096-row chunks (dZ of one chunk, an fp32 dX
+ *                   chunk, and 32 MiB of cuBLAS scratch).  A smaller
+ *                   workspace gives smaller chunks, in steps of 128 rows;
+ *                   less than 128 rows' worth returns VPCE_ERR_WORKSPACE.
+ * The cuBLAS handle is created once per device on the first call (which is
+ * therefore not capturable into a CUDA graph); it runs in the caller's
+ * workspace, so later calls allocate nothing.  Calls on one device are
+ * serialised on the handle.
  */
 size_t vpce_lmhead_backward_workspace_bytes(int64_t V, int64_t h);
 vpce_status vpce_lmhead_backward(const void* hidden, int64_t ld_hidden,

@@ -180,7 +180,9 @@ def _bwd_bound(dz, mat, ref, K):
 def _bwd_workspace(V, h, rows):
     """Backward workspace sized for chunks of `rows` rows (forces several chunks)."""
     r256 = lambda n: (n + 255) // 256 * 256  # noqa: E731
-    return torch.empty(r256(rows * ((V + 7) // 8 * 8) * 2) + r256(rows * h * 4), dtype=torch.uint8, device="cuda")
+    blas = 32 << 20  # cuBLAS scratch at the end of the workspace
+    return torch.empty(r256(rows * ((V + 7) // 8 * 8) * 2) + r256(rows * h * 4) + blas, dtype=torch.uint8,
+                       device="cuda")
 
 
 def _check_backward(m, vs=None, *, reduction="mean", grad=1.0, grad_rows=None, chunk_rows=None):

@@ -27,6 +27,9 @@ namespace {
 
 constexpr long long kBwdRows = 4096;  // rows per chunk with the suggested workspace
 constexpr long long kMinBwdRows = 128;
+// cuBLAS's own scratch, carved from the caller's workspace so that no call
+// allocates (and a stream capture records nothing but kernels).
+constexpr size_t kBlasBytes = size_t(32) << 20;
 
 __global__ void f32_to_bf16_rows(const float* src, long long lds, __nv_bfloat16* dst, long long ldd, long long rows,
                                  long long cols) {
@@ -55,7 +58,8 @@ cublasHandle_t blas_handle(int dev) {
 long long lmhead_bwd_ldz(long long V) { return (V + 7) / 8 * 8; }
 
 size_t lmhead_bwd_bytes_for(long long rows, long long V, long long h) {
-  return round256(size_t(rows) * size_t(lmhead_bwd_ldz(V)) * 2u) + round256(size_t(rows) * size_t(h) * 4u);
+  return round256(size_t(rows) * size_t(lmhead_bwd_ldz(V)) * 2u) + round256(size_t(rows) * size_t(h) * 4u) +
+         kBlasBytes;
 }
 
 size_t lmhead_bwd_workspace_bytes(long long V, long long h) { return lmhead_bwd_bytes_for(kBwdRows, V, h); }
@@ -82,13 +86,18 @@ vpce_status lmhead_backward_run(const void* x, long long ld_x, const void* const
   }
   std::lock_guard<std::mutex> lock(g_blas_mu);
   cublasHandle_t hb = blas_handle(dev);
-  if (hb == nullptr || cublasSetStream(hb, st) != CUBLAS_STATUS_SUCCESS) return VPCE_ERR_CUDA;
   const long long V = vs[t];
   const long long ldz = lmhead_bwd_ldz(V);
   const long long rows = lmhead_bwd_rows_for(ws_bytes, V, h);
   unsigned short* dz = static_cast<unsigned short*>(ws);
-  float* dx32 = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) +
-                                         round256(size_t(rows) * size_t(ldz) * 2u));
+  unsigned char* dx32_at = static_cast<unsigned char*>(ws) + round256(size_t(rows) * size_t(ldz) * 2u);
+  float* dx32 = reinterpret_cast<float*>(dx32_at);
+  void* blas_ws = dx32_at + round256(size_t(rows) * size_t(h) * 4u);
+  // setting the stream resets cuBLAS to its default workspace pool, so the
+  // caller's slice is installed after it, on every call
+  if (hb == nullptr || cublasSetStream(hb, st) != CUBLAS_STATUS_SUCCESS ||
+      cublasSetWorkspace(hb, blas_ws, kBlasBytes) != CUBLAS_STATUS_SUCCESS)
+    return VPCE_ERR_CUDA;
   const float one = 1.f, zero = 0.f;
   for (long long r0 = 0; r0 < s; r0 += rows) {
     const long long R = s - r0 < rows ? s - r0 : rows;
