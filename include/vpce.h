@@ -361,9 +361,11 @@ vpce_status vpce_embedding_forward(const void* const* table_shards, vpce_dtype d
  * lookup): adds each output-gradient row into the fp32 gradient-table row of
  * its id, accumulating into what grad_shards already hold:
  *     grad_shard_i[j] += sum over r with ids[r] = vocab_start[i] + j of grad_out[r].
- * Ids outside [0, V) contribute nothing.  Deterministic: the rows of each id
- * are summed in ascending row order (fp32), then added once; batches longer
- * than 16384 rows run in 16384-row chunks in order.
+ * Ids outside [0, V) contribute nothing.  Deterministic: the rows of an id
+ * with at most 64 rows in a chunk are summed in ascending row order (fp32);
+ * an id with more is summed as eight contiguous slices of its rows, each in
+ * ascending order, then the slices in order; the sum is then added once.
+ * Batches longer than 16384 rows run in 16384-row chunks in order.
  *   grad_out      device [s, h] of grad_dtype, row stride ld_grad (0 = h);
  *                 16-byte aligned, ld_grad * element size a multiple of 16.
  *   grad_shards   host array of t device float pointers, shard i [w_i, h],
@@ -371,7 +373,10 @@ vpce_status vpce_embedding_forward(const void* const* table_shards, vpce_dtype d
  *                 ld_grad_table a multiple of 4.
  *   h             a positive multiple of 4.
  *   workspace     vpce_embedding_backward_workspace_bytes() bytes, 256-byte
- *                 aligned, caller owned.
+ *                 aligned, caller owned.  It starts with the same header as
+ *                 the loss workspace: vpce_read_error_flag on it returns
+ *                 VPCE_FLAG_WAIT_TIMEOUT if a bounded wait of the kernels gave
+ *                 up (the gradient is then incomplete), else 0.
  */
 size_t vpce_embedding_backward_workspace_bytes(void);
 vpce_status vpce_embedding_backward(const void* grad_out, vpce_dtype grad_dtype, int64_t ld_grad,

@@ -4,8 +4,10 @@ vpce_embedding_backward) against the fp64 oracle.
 * Forward: a copy of table rows, so bit-exact; ids outside [0, V) give zero
   rows and the flag.
 * Backward: each table row receives the fp32 sum of its ids' gradient rows in
-  ascending row order, then one fp32 add.  Against fp64 that is at most
-  (count + 1) * 2^-24 * sum |g| per element (recursive summation of count + 1
+  a fixed order (ascending rows; ids with more than 64 rows in a chunk as
+  eight ascending slices, then the slices in order), then one fp32 add.
+  Against fp64 that is at most (count + 1) * 2^-24 * sum |g| per element (the
+  recursive-summation bound, which holds for any summation tree of count + 1
   terms), checked element by element; results are bitwise repeatable."""
 import numpy as np
 import pytest
@@ -75,9 +77,9 @@ def test_embedding_forward_fp32_padded_and_misaligned():
     assert not bad
 
 
-def _check_backward(V, h, vs, s, kind, grad_dtype, seed, extra=()):
+def _check_backward(V, h, vs, s, kind, grad_dtype, seed, extra=(), ld=None):
     ids = _ids(seed, s, V, kind, extra)
-    g = synth.grad_device(seed, s, h)
+    g = synth.grad_device(seed, s, ld or h)[:, :h]  # ld: padded rows
     if grad_dtype == "fp32":
         g = g.float()
     gh = O.widen(_bits(g), "bf16") if grad_dtype == "bf16" else g.cpu().numpy().astype(np.float64)
@@ -100,6 +102,25 @@ def _check_backward(V, h, vs, s, kind, grad_dtype, seed, extra=()):
 def test_embedding_backward(kind, grad_dtype):
     _check_backward(2000, 64, [0, 1, 999, 2000], 3000, kind, grad_dtype, 41,
                     extra=[(5, -1), (6, 2000), (7, -100)])
+
+
+@pytest.mark.parametrize("grad_dtype", ["bf16", "fp32"])
+def test_embedding_backward_ragged_column_blocks(grad_dtype):
+    # h = 516: two full 256-column blocks and a 4-column tail (for bf16 half
+    # of a 16-byte piece; rows padded to 520 for 16-byte row strides), with
+    # long and short runs of Zipf ids
+    _check_backward(900, 516, [0, 450, 900], 2500, "zipf1.1", grad_dtype, 45, extra=[(3, -1)], ld=520)
+
+
+def test_embedding_backward_error_flag_is_clear():
+    V, h, s = 1000, 264, 700
+    vs = [0, 500, 1000]
+    ids = torch.from_numpy(_ids(46, s, V, "zipf1.1", ())).cuda()
+    g = synth.grad_device(46, s, h)
+    grads = [torch.zeros((500, h), dtype=torch.float32, device="cuda") for _ in range(2)]
+    wk = torch.full((vpce.vpce_embedding_backward_workspace_bytes(),), 0xFF, dtype=torch.uint8, device="cuda")
+    vpce.vpce_embedding_backward(g, ids, grads, vs, workspace=wk)
+    assert vpce.vpce_read_error_flag(wk) == 0
 
 
 def test_embedding_backward_multi_chunk_is_deterministic():

@@ -13,10 +13,11 @@
 // output-gradient row into the table row of its id.  It is deterministic:
 // the (id, row) pairs of up to kEmbChunk rows are sorted (each CTA sorts 1024
 // of them in shared memory, bitonic, then merge-path rounds double the sorted
-// width), one CTA marks where each id's run starts, and one warp per
-// (distinct id, 128 columns) then sums the id's rows in ascending row order
-// and adds the sum into the fp32 gradient table.  Longer batches run chunk after chunk on
-// the stream, so the accumulation order is fixed.
+// width); one CTA marks where each id's run starts, lists the long runs and
+// groups the short ones; one persistent kernel then sums every run in a fixed
+// order and adds the sum into the fp32 gradient table, streaming the rows
+// through shared memory with cp.async.  Longer batches run chunk after chunk
+// on the stream, so the accumulation order is fixed.
 #include "vpce_kernels.cuh"
 
 namespace vpce {
@@ -28,6 +29,7 @@ constexpr int kSortThreads = 1024;
 constexpr int kEmbChunk = 16384;  // rows sorted per backward chunk (128 KB of keys)
 constexpr unsigned long long kNoKey = ~0ull;
 constexpr int kHeavyRows = 64;  // ids with more rows are summed by a whole CTA
+constexpr int kGroupRows = 16;  // short-run tasks: runs starting in this many consecutive sorted rows
 
 struct EmbedFwdParams {
   ShardSet sh;        // table shards [w_i, h] (ld_bytes = row stride)
@@ -186,13 +188,22 @@ struct EmbedRunsParams {
   int* n_seg;
   int* heavy;                      // [kEmbChunk / kHeavyRows] runs longer than kHeavyRows (any order)
   int* n_heavy;
+  int* gstart;                     // [kEmbChunk / kGroupRows + 1] first run of each group of kGroupRows rows
+  int* n_grp;
+  unsigned* work;                  // [2] the accumulation's task counters, cleared here
+  Header* hdr;                     // error flag (cleared when `first`)
+  int first;                       // first chunk of the call
+  ShardSet gsh;                    // fp32 gradient table shards
+  int t;
+  unsigned long long* rtab;        // [kEmbChunk] each run's gradient-table row (address)
 };
 
 // One CTA: the start of every run of equal ids in the sorted keys (ids outside
 // [0, V) sorted last as kNoKey and are dropped), and the list of long runs.
-__global__ void __launch_bounds__(kSortThreads) embed_runs_kernel(const EmbedRunsParams p) {
+__global__ void __launch_bounds__(kSortThreads) embed_runs_kernel(const __grid_constant__ EmbedRunsParams p) {
   __shared__ int warp_sum[kSortThreads / 32];
   __shared__ int nh;
+  __shared__ long long start[VPCE_MAX_SHARDS + 1];
   const int tid = threadIdx.x;
   const unsigned long long* key = p.keys;
   // run heads: a valid key whose id differs from its predecessor's
@@ -212,7 +223,13 @@ __global__ void __launch_bounds__(kSortThreads) embed_runs_kernel(const EmbedRun
     if (lane >= o) incl += x;
   }
   if (lane == 31) warp_sum[warp] = incl;
-  if (tid == 0) nh = 0;
+  for (int i = tid; i <= p.t; i += kSortThreads) start[i] = p.gsh.start[i];
+  if (tid == 0) {
+    nh = 0;
+    p.work[0] = 0u;
+    p.work[1] = 0u;
+    if (p.first) p.hdr->error_flag = 0;
+  }
   __syncthreads();
   if (warp == 0) {
     int w = warp_sum[lane];
@@ -245,10 +262,28 @@ __global__ void __launch_bounds__(kSortThreads) embed_runs_kernel(const EmbedRun
   __syncthreads();  // seg[] (global) is complete and visible to the block
   // the long runs, listed for the CTA-per-chunk kernel (their order does not
   // matter: each run's sum is formed on its own)
-  for (int j = tid; j < total; j += kSortThreads)
+  for (int j = tid; j < total; j += kSortThreads) {
     if (p.seg[j + 1] - p.seg[j] > kHeavyRows) p.heavy[atomicAdd(&nh, 1)] = j;
+    // the run's row of the gradient table (every key here has an id in range)
+    const long long id = static_cast<long long>(key[p.seg[j]] >> 32);
+    const int i = shard_of(start, p.t, id);
+    p.rtab[j] = reinterpret_cast<unsigned long long>(p.gsh.ptr[i] + (id - start[i]) * p.gsh.ld_bytes[i]);
+  }
+  // groups of kGroupRows sorted rows: group g holds the runs that start in
+  // [g kGroupRows, (g + 1) kGroupRows); gstart[g] is its first run
+  const int nvalid = p.seg[total];
+  const int ngrp = (nvalid + kGroupRows - 1) / kGroupRows;
+  for (int j = tid; j < total; j += kSortThreads) {
+    const int g_lo = j == 0 ? 0 : p.seg[j - 1] / kGroupRows + 1, g_hi = p.seg[j] / kGroupRows;
+    for (int g = g_lo; g <= g_hi; ++g) p.gstart[g] = j;
+  }
+  for (int g = (total > 0 ? p.seg[total - 1] / kGroupRows + 1 : 0) + tid; g <= ngrp; g += kSortThreads)
+    p.gstart[g] = total;
   __syncthreads();
-  if (tid == 0) *p.n_heavy = nh;
+  if (tid == 0) {
+    *p.n_heavy = nh;
+    *p.n_grp = ngrp;
+  }
 }
 
 struct EmbedAccParams {
@@ -263,172 +298,419 @@ struct EmbedAccParams {
   long long h;
   ShardSet gsh;  // fp32 gradient table shards (ld_bytes = row stride)
   int t;
+  const int* gstart;
+  const int* n_grp;
+  const unsigned long long* rtab;  // each run's gradient-table row
+  unsigned* work;                  // [2] task counters (zero at launch)
+  Header* hdr;
 };
 
-__device__ __forceinline__ float4 grad4(const EmbedAccParams& p, int row, long long c) {
-  const unsigned char* base = p.grad + (long long)row * p.ld_grad_bytes;
-  if (p.grad_bf16) {
-    const uint2 w = *reinterpret_cast<const uint2*>(base + c * 2);
-    return make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, unsigned src_bytes) {
+  // src_bytes < 16 zero-fills the rest of the 16 bytes
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(smem)), "l"(gmem), "r"(src_bytes)
+               : "memory");
+}
+// the mbarrier receives this thread's arrival once all its earlier cp.async
+// copies have landed
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+constexpr int kAWarps = 8;
+constexpr int kAThreads = kAWarps * 32;
+constexpr int kShortCols = 256;  // columns per short-run task (8 per lane)
+constexpr int kHeavyCols = 256;  // columns per long-run CTA task (8 per lane)
+constexpr int kTRing = 8;        // runs (table slices) in flight per warp, at most 32
+
+// A lane's share of a row slice of COLS columns, staged as 16-byte pieces:
+// piece pc of lane l starts at column c0 + (32 pc + l) 16 / EB, so that a
+// warp's piece pc is one contiguous span.  The lane's columns form COLS / 128
+// quads of four (the fp32 table side): a bf16 piece holds quads 2 pc and
+// 2 pc + 1, an fp32 piece is one quad.  Accumulator acc[4 q + e] is column e
+// of quad q.
+template <int EB, int COLS>
+struct Slice {
+  static constexpr int kPieces = COLS * EB / 512;
+  static constexpr int kQuads = COLS / 128;
+  static __device__ __forceinline__ long long piece_col(long long c0, int lane, int pc) {
+    return c0 + (32LL * pc + lane) * (16 / EB);
   }
-  return *reinterpret_cast<const float4*>(base + c * 4);
+  static __device__ __forceinline__ long long quad_col(long long c0, int lane, int qd) {
+    return EB == 2 ? c0 + 8 * lane + 4 * (qd & 1) + 256 * (qd >> 1) : c0 + 4 * lane + 128 * qd;
+  }
+};
+
+template <int EB>
+struct AccCfg {
+  static constexpr int kRingBytes = EB == 2 ? 4096 : 8192;  // per warp, shared by both phases
+  static constexpr int kRS = kRingBytes / (kShortCols * EB);  // short-run row slices in flight
+  static constexpr int kRH = kRingBytes / (kHeavyCols * EB);  // long-run row slices in flight
+};
+
+template <int EB>
+struct AccSmem {
+  uint4 ring[kAWarps][AccCfg<EB>::kRingBytes / 16];  // slot-major: [slot][piece][lane]
+  float4 table[kAWarps][kTRing][kShortCols / 128][32];
+  float4 part[kAWarps][kHeavyCols / 128][32];
+  uint64_t bar_s[kAWarps][AccCfg<EB>::kRS];
+  uint64_t bar_h[kAWarps][AccCfg<EB>::kRH];
+  unsigned task;
+};
+
+// A lane's view of 64 consecutive entries of an array, starting at a
+// warp-uniform index that only moves forward: entries base + lane and
+// base + 32 + lane, so that the next 32 are already on their way.
+template <typename T>
+struct Window {
+  const T* a;
+  long long n;  // entries [0, n) exist
+  long long base;
+  T cur, nxt;
+  __device__ __forceinline__ T ld(long long i) const { return i < n ? a[i] : T(0); }
+  __device__ __forceinline__ void init(const T* arr, long long len, long long k, int lane) {
+    a = arr;
+    n = len;
+    base = k;
+    cur = ld(k + lane);
+    nxt = ld(k + 32 + lane);
+  }
+  __device__ __forceinline__ T at(long long k, int lane) {  // k >= base, warp-uniform
+    if (k - base >= 64) {
+      base = k;
+      cur = ld(k + lane);
+      nxt = ld(k + 32 + lane);
+    } else if (k - base >= 32) {
+      base += 32;
+      cur = nxt;
+      nxt = ld(base + 32 + lane);
+    }
+    return __shfl_sync(kFull, cur, int(k - base));
+  }
+  // entries k and k + 1, leaving the window at or before k
+  __device__ __forceinline__ void pair(long long k, int lane, T& v0, T& v1) {
+    const T a0 = at(k, lane);
+    const int d = int(k - base);
+    const T c1 = __shfl_sync(kFull, cur, (d + 1) & 31);
+    const T n0 = __shfl_sync(kFull, nxt, 0);
+    v0 = a0;
+    v1 = d < 31 ? c1 : n0;
+  }
+};
+
+// One lane's cp.async copies of one row slice into ring slot `slot`, and its
+// arrival on the slot's mbarrier once they land.  Columns at or past h are
+// zero-filled, nothing is read there.
+template <int EB, int COLS>
+__device__ __forceinline__ void stage_row(uint4* ring, int slot, int lane, const unsigned char* grow, long long c0,
+                                          long long h, uint64_t* bar) {
+  using S = Slice<EB, COLS>;
+#pragma unroll
+  for (int pc = 0; pc < S::kPieces; ++pc) {
+    const long long col = S::piece_col(c0, lane, pc);
+    const long long left = (h - col) * EB;
+    const unsigned bytes = left >= 16 ? 16u : (left > 0 ? unsigned(left) : 0u);
+    cp_async16(&ring[(slot * S::kPieces + pc) * 32 + lane], bytes ? grow + col * EB : grow, bytes);
+  }
+  cp_async_arrive(bar);
 }
 
-// Work items are (short run, 512 columns) pairs, one warp each: four
-// 128-column chunks at once (four float4 accumulators per lane), the run's
-// rows in ascending order two at a time, so eight independent loads are in
-// flight per lane; then one add into the id's row of the gradient table.
-// The order of the additions per element does not depend on the grouping.
-__global__ void __launch_bounds__(kEmbThreads) embed_accum_kernel(const __grid_constant__ EmbedAccParams p) {
-  __shared__ long long start[VPCE_MAX_SHARDS + 1];
-  for (int i = threadIdx.x; i <= p.t; i += kEmbThreads) start[i] = p.gsh.start[i];
-  __syncthreads();
-  const int lane = threadIdx.x & 31;
-  constexpr int kU = 4;  // 128-column chunks per task
-  const long long nseg = *p.n_seg;
-  const long long ngrp = (p.h + 128 * kU - 1) / (128 * kU);
-  const long long tasks = nseg * ngrp;
-  const long long nwarps = (long long)gridDim.x * (kEmbThreads / 32);
-  for (long long q = (long long)blockIdx.x * (kEmbThreads / 32) + (threadIdx.x >> 5); q < tasks; q += nwarps) {
-    const long long sgi = q / ngrp;
-    const long long c0 = (q - sgi * ngrp) * (128 * kU) + 4 * lane;
-    const int a = p.seg[sgi], b = p.seg[sgi + 1];
-    if (b - a > kHeavyRows) continue;  // long runs: embed_heavy_kernel
-    bool in[kU];
+// acc += the lane's share of the row slice in ring slot `slot`
+template <int EB, int COLS>
+__device__ __forceinline__ void add_row(const uint4* ring, int slot, int lane, float* acc) {
+  using S = Slice<EB, COLS>;
 #pragma unroll
-    for (int u = 0; u < kU; ++u) in[u] = c0 + 128 * u < p.h;
-    float4 acc[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    int k = a;
-    for (; k + 2 <= b; k += 2) {
-      const int r0 = int(p.keys[k] & 0xffffffffu), r1 = int(p.keys[k + 1] & 0xffffffffu);
-      float4 g0[kU], g1[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        g0[u] = in[u] ? grad4(p, r0, c0 + 128 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
-        g1[u] = in[u] ? grad4(p, r1, c0 + 128 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        acc[u].x += g0[u].x;
-        acc[u].y += g0[u].y;
-        acc[u].z += g0[u].z;
-        acc[u].w += g0[u].w;
-        acc[u].x += g1[u].x;
-        acc[u].y += g1[u].y;
-        acc[u].z += g1[u].z;
-        acc[u].w += g1[u].w;
-      }
+  for (int pc = 0; pc < S::kPieces; ++pc) {
+    const uint4 v = ring[(slot * S::kPieces + pc) * 32 + lane];
+    if (EB == 2) {
+      float* a = acc + 8 * pc;
+      a[0] += bf16_lo(v.x);
+      a[1] += bf16_hi(v.x);
+      a[2] += bf16_lo(v.y);
+      a[3] += bf16_hi(v.y);
+      a[4] += bf16_lo(v.z);
+      a[5] += bf16_hi(v.z);
+      a[6] += bf16_lo(v.w);
+      a[7] += bf16_hi(v.w);
+    } else {
+      float* a = acc + 4 * pc;
+      a[0] += __uint_as_float(v.x);
+      a[1] += __uint_as_float(v.y);
+      a[2] += __uint_as_float(v.z);
+      a[3] += __uint_as_float(v.w);
     }
-    if (k < b) {
-      const int r0 = int(p.keys[k] & 0xffffffffu);
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const float4 g = in[u] ? grad4(p, r0, c0 + 128 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
-        acc[u].x += g.x;
-        acc[u].y += g.y;
-        acc[u].z += g.z;
-        acc[u].w += g.w;
-      }
-    }
-    const long long id = static_cast<long long>(p.keys[a] >> 32);
-    const int i = shard_of(start, p.t, id);
-    float* dst = reinterpret_cast<float*>(const_cast<unsigned char*>(p.gsh.ptr[i]) +
-                                          (id - start[i]) * p.gsh.ld_bytes[i]) + c0;
-    float4 o[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u)
-      if (in[u]) o[u] = *reinterpret_cast<const float4*>(dst + 128 * u);
-#pragma unroll
-    for (int u = 0; u < kU; ++u)
-      if (in[u]) {
-        o[u].x += acc[u].x;
-        o[u].y += acc[u].y;
-        o[u].z += acc[u].z;
-        o[u].w += acc[u].w;
-        *reinterpret_cast<float4*>(dst + 128 * u) = o[u];
-      }
   }
 }
 
-// One CTA per (long run, 128-column chunk): warp w sums the w-th of eight
-// contiguous slices of the run's rows (ascending), then warp 0 adds the eight
-// partials in warp order and the result into the table row -- a fixed
-// two-level order, so the sum does not depend on timing.
-__global__ void __launch_bounds__(kEmbThreads) embed_heavy_kernel(const __grid_constant__ EmbedAccParams p) {
-  __shared__ long long start[VPCE_MAX_SHARDS + 1];
-  __shared__ float4 part[kEmbThreads / 32][32];
-  for (int i = threadIdx.x; i <= p.t; i += kEmbThreads) start[i] = p.gsh.start[i];
+// Every run's sum, added into its id's row of the fp32 gradient table, in
+// one persistent launch.  Work is handed out through two counters.  First
+// the long runs (more than kHeavyRows rows): one CTA per (run, kHeavyCols
+// columns), each warp summing a contiguous eighth of the run and warp 0
+// adding the eight partials in warp order.  Then the short runs: one warp
+// per (group of the runs that start in kGroupRows consecutive sorted rows,
+// kShortCols columns).  A warp streams its rows through a shared-memory
+// ring: each lane copies its own 16-byte pieces with cp.async and the copy
+// of the next row is issued as soon as a slot frees, across run boundaries;
+// a run's table slice comes in with its first row, and the sum of the run's
+// rows, in ascending order, is added to it after the run's last row.  Each
+// element's sum has a fixed order whichever CTA or warp does the task.
+template <int EB>
+__global__ void __launch_bounds__(kAThreads) embed_accum_kernel(const __grid_constant__ EmbedAccParams p) {
+  using C = AccCfg<EB>;
+  using SS = Slice<EB, kShortCols>;
+  using SH = Slice<EB, kHeavyCols>;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  AccSmem<EB>& sm = *reinterpret_cast<AccSmem<EB>*>(smem_raw);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  uint4* ring = sm.ring[w];
+  if (lane == 0) {
+    for (int k = 0; k < C::kRS; ++k) mbar_init(&sm.bar_s[w][k], 32);
+    for (int k = 0; k < C::kRH; ++k) mbar_init(&sm.bar_h[w][k], 32);
+    fence_mbar_init();
+  }
   __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int kW = kEmbThreads / 32;
-  const long long nch = (p.h + 127) / 128;
-  const long long tasks = (long long)(*p.n_heavy) * nch;
-  for (long long q = blockIdx.x; q < tasks; q += gridDim.x) {
-    const long long hj = q / nch;
-    const long long c = (q - hj * nch) * 128 + 4 * lane;
-    const int sgi = p.heavy[hj];
-    const int a = p.seg[sgi], b = p.seg[sgi + 1];
-    const int n = b - a;
-    const int lo = a + int((long long)n * warp / kW), hi = a + int((long long)n * (warp + 1) / kW);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (c < p.h) {
-      int k = lo;
-      for (; k + 8 <= hi; k += 8) {
-        float4 g[8];
+  const long long h = p.h;
+  const int total = *p.n_seg;
+  const long long nkeys = p.seg[total];  // valid keys
+  bool ok = true;
+
+  // ---- long runs: CTA tasks
+  {
+    const long long ncb = (h + kHeavyCols - 1) / kHeavyCols;
+    const long long n_ht = (long long)(*p.n_heavy) * ncb;
+    unsigned issued = 0, consumed = 0;
+    for (;;) {
+      if (threadIdx.x == 0) sm.task = atomicAdd(&p.work[0], 1u);
+      __syncthreads();
+      const long long q = sm.task;
+      __syncthreads();
+      if (q >= n_ht) break;
+      const long long hj = q / ncb;
+      const long long c0 = (q - hj * ncb) * kHeavyCols;
+      const int sgi = p.heavy[hj];
+      const int ra = p.seg[sgi], n = p.seg[sgi + 1] - ra;
+      const int lo = ra + int((long long)n * w / kAWarps), hi = ra + int((long long)n * (w + 1) / kAWarps);
+      float* trow = nullptr;
+      float4 tq[SH::kQuads];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) g[u] = grad4(p, int(p.keys[k + u] & 0xffffffffu), c);
+      for (int qd = 0; qd < SH::kQuads; ++qd) tq[qd] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (w == 0) {
+        trow = reinterpret_cast<float*>(p.rtab[sgi]);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          acc.x += g[u].x;
-          acc.y += g[u].y;
-          acc.z += g[u].z;
-          acc.w += g[u].w;
+        for (int qd = 0; qd < SH::kQuads; ++qd) {
+          const long long col = SH::quad_col(c0, lane, qd);
+          if (col < h) tq[qd] = *reinterpret_cast<const float4*>(trow + col);
         }
       }
-      for (; k < hi; ++k) {
-        const float4 g = grad4(p, int(p.keys[k] & 0xffffffffu), c);
-        acc.x += g.x;
-        acc.y += g.y;
-        acc.z += g.z;
-        acc.w += g.w;
-      }
-    }
-    part[warp][lane] = acc;
-    __syncthreads();
-    if (warp == 0 && c < p.h) {
-      float4 tot = part[0][lane];
+      float acc[4 * SH::kQuads];
 #pragma unroll
-      for (int u = 1; u < kW; ++u) {
-        tot.x += part[u][lane].x;
-        tot.y += part[u][lane].y;
-        tot.z += part[u][lane].z;
-        tot.w += part[u][lane].w;
+      for (int e = 0; e < 4 * SH::kQuads; ++e) acc[e] = 0.f;
+      Window<unsigned long long> kw;
+      kw.init(p.keys, nkeys, lo, lane);
+      long long pk = lo;
+      for (int k = lo; k < hi && ok; ++k) {
+        while (pk < hi && issued - consumed < unsigned(C::kRH)) {
+          const unsigned long long key = kw.at(pk++, lane);
+          const int slot = int(issued % C::kRH);
+          stage_row<EB, kHeavyCols>(ring, slot, lane, p.grad + (long long)(key & 0xffffffffu) * p.ld_grad_bytes, c0, h,
+                                    &sm.bar_h[w][slot]);
+          ++issued;
+        }
+        const int slot = int(consumed % C::kRH);
+        ok = mbar_wait_warp(&sm.bar_h[w][slot], (consumed / C::kRH) & 1u);
+        if (ok) add_row<EB, kHeavyCols>(ring, slot, lane, acc);
+        ++consumed;
       }
-      const long long id = static_cast<long long>(p.keys[a] >> 32);
-      const int i = shard_of(start, p.t, id);
-      float* dst = reinterpret_cast<float*>(const_cast<unsigned char*>(p.gsh.ptr[i]) +
-                                            (id - start[i]) * p.gsh.ld_bytes[i]) + c;
-      float4 o = *reinterpret_cast<float4*>(dst);
-      o.x += tot.x;
-      o.y += tot.y;
-      o.z += tot.z;
-      o.w += tot.w;
-      *reinterpret_cast<float4*>(dst) = o;
+#pragma unroll
+      for (int qd = 0; qd < SH::kQuads; ++qd)
+        sm.part[w][qd][lane] = make_float4(acc[4 * qd], acc[4 * qd + 1], acc[4 * qd + 2], acc[4 * qd + 3]);
+      __syncthreads();
+      if (w == 0) {
+#pragma unroll
+        for (int qd = 0; qd < SH::kQuads; ++qd) {
+          const long long col = SH::quad_col(c0, lane, qd);
+          if (col >= h) continue;
+          float4 tot = sm.part[0][qd][lane];
+#pragma unroll
+          for (int ww = 1; ww < kAWarps; ++ww) {
+            const float4 v = sm.part[ww][qd][lane];
+            tot.x += v.x;
+            tot.y += v.y;
+            tot.z += v.z;
+            tot.w += v.w;
+          }
+          tq[qd].x += tot.x;
+          tq[qd].y += tot.y;
+          tq[qd].z += tot.z;
+          tq[qd].w += tot.w;
+          *reinterpret_cast<float4*>(trow + col) = tq[qd];
+        }
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
+
+  // ---- short runs: warp tasks
+  const long long ncb = (h + kShortCols - 1) / kShortCols;
+  const long long n_st = (long long)(*p.n_grp) * ncb;
+  unsigned issued = 0, consumed = 0, run_ord = 0, flushed = 0;
+  int r_len = 0;                 // run ordinal = lane (mod 32): its length ...
+  unsigned long long r_dst = 0;  // ... and its table row
+  float acc[4 * SS::kQuads];
+  while (ok) {
+    unsigned q = 0;
+    if (lane == 0) q = atomicAdd(&p.work[1], 1u);
+    q = __shfl_sync(kFull, q, 0);
+    if (q >= n_st) break;
+    const long long gi = q / ncb;
+    const long long c0 = ((long long)q - gi * ncb) * kShortCols;
+    const long long s1 = p.gstart[gi + 1];
+    long long ps = p.gstart[gi];
+    Window<int> sw;
+    sw.init(p.seg, total + 1, ps, lane);
+    Window<unsigned long long> pw;
+    pw.init(p.rtab, total, ps, lane);
+    Window<unsigned long long> kw;
+    kw.init(p.keys, nkeys, sw.at(ps, lane), lane);
+    long long pk = 0, pend = 0;
+    bool pdone = false;
+    // keeps the ring full: the rows of the task's short runs in order, a
+    // run's table slice issued with its first row
+    auto top_up = [&]() {
+      while (!pdone && issued - consumed < unsigned(C::kRS)) {
+        if (pk == pend) {
+          int a = 0, b = 0;
+          for (;;) {
+            if (ps >= s1) {
+              pdone = true;
+              break;
+            }
+            sw.pair(ps, lane, a, b);
+            if (b - a <= kHeavyRows) break;
+            ++ps;  // a long run: its CTA tasks sum it
+          }
+          if (pdone || run_ord - flushed >= unsigned(kTRing)) break;
+          const unsigned long long tp = pw.at(ps, lane);
+          const float* trow = reinterpret_cast<const float*>(tp);
+          const int ts = int(run_ord % kTRing);
+#pragma unroll
+          for (int qd = 0; qd < SS::kQuads; ++qd) {
+            const long long col = SS::quad_col(c0, lane, qd);
+            cp_async16(&sm.table[w][ts][qd][lane], col < h ? trow + col : trow, col < h ? 16u : 0u);
+          }
+          if (lane == int(run_ord & 31u)) {
+            r_len = b - a;
+            r_dst = tp;
+          }
+          ++run_ord;
+          ++ps;
+          pk = a;
+          pend = b;
+        }
+        const unsigned long long key = kw.at(pk, lane);
+        const int slot = int(issued % C::kRS);
+        stage_row<EB, kShortCols>(ring, slot, lane, p.grad + (long long)(key & 0xffffffffu) * p.ld_grad_bytes, c0, h,
+                                  &sm.bar_s[w][slot]);
+        ++issued;
+        ++pk;
+      }
+    };
+    top_up();
+    while (ok && consumed < issued) {
+      const int ts = int(flushed % kTRing);
+      const int len = __shfl_sync(kFull, r_len, int(flushed & 31u));
+      float* trow = reinterpret_cast<float*>(__shfl_sync(kFull, r_dst, int(flushed & 31u)));
+#pragma unroll
+      for (int e = 0; e < 4 * SS::kQuads; ++e) acc[e] = 0.f;
+      for (int r = 0; r < len; ++r) {
+        const int slot = int(consumed % C::kRS);
+        ok = mbar_wait_warp(&sm.bar_s[w][slot], (consumed / C::kRS) & 1u);
+        if (!ok) break;
+        add_row<EB, kShortCols>(ring, slot, lane, acc);
+        ++consumed;
+        top_up();
+      }
+      if (!ok) break;
+      // the table slice arrived with the run's first row
+#pragma unroll
+      for (int qd = 0; qd < SS::kQuads; ++qd) {
+        const long long col = SS::quad_col(c0, lane, qd);
+        if (col >= h) continue;
+        float4 o = sm.table[w][ts][qd][lane];
+        o.x += acc[4 * qd + 0];
+        o.y += acc[4 * qd + 1];
+        o.z += acc[4 * qd + 2];
+        o.w += acc[4 * qd + 3];
+        *reinterpret_cast<float4*>(trow + col) = o;
+      }
+      ++flushed;
+      top_up();
+    }
+  }
+  if (!ok && lane == 0) atomicOr(&p.hdr->error_flag, VPCE_FLAG_WAIT_TIMEOUT);
+  cp_async_wait_all();  // nothing lands in shared memory after the CTA ends
 }
+
+int g_accum_ctas[2] = {1, 1};  // resident CTAs per SM of embed_accum_kernel<2>, <4>
 
 }  // namespace
 
+// Workspace: a header (its error flag is where vpce_read_error_flag looks),
+// the two key buffers of the sort, the run starts, the long-run list, the
+// group starts and the counters.
+struct EmbedWs {
+  Header* hdr;
+  unsigned long long* keys_a;
+  unsigned long long* keys_b;
+  int* seg;
+  int* heavy;
+  int* gstart;
+  unsigned long long* rtab;
+  int* counts;  // n_seg, n_heavy, n_grp, work[2]
+};
+
 size_t embed_bwd_workspace_bytes() {
-  return 2 * round256(sizeof(unsigned long long) * kEmbChunk) + round256(sizeof(int) * (kEmbChunk + 1)) +
-         round256(sizeof(int) * (kEmbChunk / kHeavyRows)) + 256;
+  return 256 + 2 * round256(sizeof(unsigned long long) * kEmbChunk) + round256(sizeof(int) * (kEmbChunk + 1)) +
+         round256(sizeof(int) * (kEmbChunk / kHeavyRows)) + round256(sizeof(int) * (kEmbChunk / kGroupRows + 1)) +
+         round256(sizeof(unsigned long long) * kEmbChunk) + 256;
 }
 
-cudaError_t set_embed_smem() { return cudaSuccess; }
+EmbedWs embed_ws(void* ws) {
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  EmbedWs e;
+  e.hdr = reinterpret_cast<Header*>(w);
+  w += 256;
+  e.keys_a = reinterpret_cast<unsigned long long*>(w);
+  w += round256(sizeof(unsigned long long) * kEmbChunk);
+  e.keys_b = reinterpret_cast<unsigned long long*>(w);
+  w += round256(sizeof(unsigned long long) * kEmbChunk);
+  e.seg = reinterpret_cast<int*>(w);
+  w += round256(sizeof(int) * (kEmbChunk + 1));
+  e.heavy = reinterpret_cast<int*>(w);
+  w += round256(sizeof(int) * (kEmbChunk / kHeavyRows));
+  e.gstart = reinterpret_cast<int*>(w);
+  w += round256(sizeof(int) * (kEmbChunk / kGroupRows + 1));
+  e.rtab = reinterpret_cast<unsigned long long*>(w);
+  w += round256(sizeof(unsigned long long) * kEmbChunk);
+  e.counts = reinterpret_cast<int*>(w);
+  return e;
+}
+
+cudaError_t set_embed_smem() {
+  cudaError_t e = cudaFuncSetAttribute(embed_accum_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(sizeof(AccSmem<2>)));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(embed_accum_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(sizeof(AccSmem<4>)));
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_accum_ctas[0], embed_accum_kernel<2>, kAThreads,
+                                                      sizeof(AccSmem<2>));
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_accum_ctas[1], embed_accum_kernel<4>, kAThreads,
+                                                      sizeof(AccSmem<4>));
+  for (int& c : g_accum_ctas) c = c < 1 ? 1 : c;
+  return e;
+}
 
 void launch_embed_forward(const ShardSet& sh, int t, long long V, long long h, int eb, const long long* ids,
                           long long s, void* out, long long ld_out, int* flag, int sms, cudaStream_t st) {
@@ -452,15 +734,11 @@ void launch_embed_forward(const ShardSet& sh, int t, long long V, long long h, i
 cudaError_t launch_embed_backward(const void* grad, int grad_bf16, long long ld_grad, const long long* ids,
                                   long long s, const ShardSet& gsh, int t, long long V, long long h, void* ws,
                                   int sms, cudaStream_t st) {
-  unsigned char* w = static_cast<unsigned char*>(ws);
-  const size_t kb = round256(sizeof(unsigned long long) * kEmbChunk);
-  unsigned long long* keys_a = reinterpret_cast<unsigned long long*>(w);
-  unsigned long long* keys_b = reinterpret_cast<unsigned long long*>(w + kb);
-  int* seg = reinterpret_cast<int*>(w + 2 * kb);
-  int* heavy = reinterpret_cast<int*>(w + 2 * kb + round256(sizeof(int) * (kEmbChunk + 1)));
-  int* n_seg = reinterpret_cast<int*>(w + 2 * kb + round256(sizeof(int) * (kEmbChunk + 1)) +
-                                      round256(sizeof(int) * (kEmbChunk / kHeavyRows)));
-  int* n_heavy = n_seg + 1;
+  const EmbedWs W = embed_ws(ws);
+  int* n_seg = W.counts;
+  int* n_heavy = W.counts + 1;
+  int* n_grp = W.counts + 2;
+  unsigned* work = reinterpret_cast<unsigned*>(W.counts + 3);
   const int eb = grad_bf16 ? 2 : 4;
   for (long long r0 = 0; r0 < s; r0 += kEmbChunk) {
     const int n = int(s - r0 < kEmbChunk ? s - r0 : kEmbChunk);
@@ -468,9 +746,9 @@ cudaError_t launch_embed_backward(const void* grad, int grad_bf16, long long ld_
     while (n2 < n) n2 <<= 1;
     // sort: blocks of kSortBlock keys, then merge rounds (ping-pong buffers)
     const int blk = n2 < kSortBlock ? n2 : kSortBlock;
-    embed_block_sort_kernel<<<n2 / blk, kSortBlock / 2, 0, st>>>(ids + r0, n, n2, V, keys_a);
-    unsigned long long* cur = keys_a;
-    unsigned long long* nxt = keys_b;
+    embed_block_sort_kernel<<<n2 / blk, kSortBlock / 2, 0, st>>>(ids + r0, n, n2, V, W.keys_a);
+    unsigned long long* cur = W.keys_a;
+    unsigned long long* nxt = W.keys_b;
     for (int width = blk; width < n2; width <<= 1) {
       embed_merge_kernel<<<(n2 + 255) / 256, 256, 0, st>>>(cur, nxt, width, n2);
       unsigned long long* tmp = cur;
@@ -481,16 +759,24 @@ cudaError_t launch_embed_backward(const void* grad, int grad_bf16, long long ld_
     EmbedRunsParams rp;
     rp.keys = keys;
     rp.n_pow2 = n2;
-    rp.seg = seg;
+    rp.seg = W.seg;
     rp.n_seg = n_seg;
-    rp.heavy = heavy;
+    rp.heavy = W.heavy;
     rp.n_heavy = n_heavy;
+    rp.gstart = W.gstart;
+    rp.n_grp = n_grp;
+    rp.work = work;
+    rp.hdr = W.hdr;
+    rp.first = r0 == 0;
+    rp.gsh = gsh;
+    rp.t = t;
+    rp.rtab = W.rtab;
     embed_runs_kernel<<<1, kSortThreads, 0, st>>>(rp);
     EmbedAccParams ap;
     ap.keys = keys;
-    ap.seg = seg;
+    ap.seg = W.seg;
     ap.n_seg = n_seg;
-    ap.heavy = heavy;
+    ap.heavy = W.heavy;
     ap.n_heavy = n_heavy;
     ap.grad = static_cast<const unsigned char*>(grad) + r0 * ld_grad * eb;
     ap.ld_grad_bytes = ld_grad * eb;
@@ -498,11 +784,16 @@ cudaError_t launch_embed_backward(const void* grad, int grad_bf16, long long ld_
     ap.h = h;
     ap.gsh = gsh;
     ap.t = t;
-    const long long want = ((long long)n * ((h + 511) / 512) + kEmbThreads / 32 - 1) / (kEmbThreads / 32);
-    const long long cap = (long long)sms * 8;
-    embed_accum_kernel<<<int(want < cap ? want : cap), kEmbThreads, 0, st>>>(ap);
-    const long long hwant = (long long)(n / (kHeavyRows + 1) + 1) * ((h + 127) / 128);
-    embed_heavy_kernel<<<int(hwant < cap ? hwant : cap), kEmbThreads, 0, st>>>(ap);
+    ap.gstart = W.gstart;
+    ap.n_grp = n_grp;
+    ap.rtab = W.rtab;
+    ap.work = work;
+    ap.hdr = W.hdr;
+    // persistent: as many CTAs as fit take tasks until both lists are done
+    if (grad_bf16)
+      embed_accum_kernel<2><<<sms * g_accum_ctas[0], kAThreads, sizeof(AccSmem<2>), st>>>(ap);
+    else
+      embed_accum_kernel<4><<<sms * g_accum_ctas[1], kAThreads, sizeof(AccSmem<4>), st>>>(ap);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
