@@ -738,17 +738,8 @@ EMBED_METRIC = "vocab-parallel embedding fwd+bwd tokens/s & HBM GB/s (% of peak)
 
 def _embedding_launches(s):
     """Kernels one forward + backward launches for s ids: the gather, then per
-    16384-row chunk a block sort, its merge rounds, the run scan and the
-    accumulation."""
-    n_launch = 1
-    for r0 in range(0, s, 16384):
-        n = min(16384, s - r0)
-        n2 = 2
-        while n2 < n:
-            n2 *= 2
-        merges = max(0, (n2 // min(n2, 1024)).bit_length() - 1)
-        n_launch += 3 + merges
-    return n_launch
+    16384-row chunk the sort-and-run-scan cluster and the accumulation."""
+    return 1 + 2 * ((s + 16383) // 16384)
 
 
 def run_embedding(args):
@@ -866,7 +857,7 @@ def run_embedding(args):
         "fwd_ms": round(fwd_ms, 5),
         "bwd_ms": round(bwd_ms, 5),
         "roofline": {
-            "kernel": "the whole step: embed_forward_kernel and the backward's kernels (sort, runs, accumulation)",
+            "kernel": "the whole step: embed_forward_kernel, embed_sort_runs_kernel, embed_accum_kernel",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,

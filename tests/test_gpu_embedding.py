@@ -112,6 +112,14 @@ def test_embedding_backward_ragged_column_blocks(grad_dtype):
     _check_backward(900, 516, [0, 450, 900], 2500, "zipf1.1", grad_dtype, 45, extra=[(3, -1)], ld=520)
 
 
+@pytest.mark.parametrize("V", [262142, 300000])
+def test_embedding_backward_vocabulary_sizes(V):
+    # the largest vocabulary sorted with 32-bit (id, row) keys, and one past
+    # it (64-bit keys); the largest ids are present
+    _check_backward(V, 16, [0, V // 3, 2 * V // 3, V], 3000, "uniform", "bf16", 47,
+                    extra=[(0, V - 1), (1, V - 1), (2, V - 2), (3, 0), (4, V)])
+
+
 def test_embedding_backward_error_flag_is_clear():
     V, h, s = 1000, 264, 700
     vs = [0, 500, 1000]

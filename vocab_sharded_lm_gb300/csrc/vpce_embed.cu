@@ -10,14 +10,17 @@
 // gives a zero row and raises a flag bit.
 //
 // The backward (not on the pages; the adjoint of the lookup) adds each
-// output-gradient row into the table row of its id.  It is deterministic:
-// the (id, row) pairs of up to kEmbChunk rows are sorted (each CTA sorts 1024
-// of them in shared memory, bitonic, then merge-path rounds double the sorted
-// width); one CTA marks where each id's run starts, lists the long runs and
-// groups the short ones; one persistent kernel then sums every run in a fixed
-// order and adds the sum into the fp32 gradient table, streaming the rows
-// through shared memory with cp.async.  Longer batches run chunk after chunk
-// on the stream, so the accumulation order is fixed.
+// output-gradient row into the table row of its id.  It is deterministic and
+// takes two launches per chunk of up to kEmbChunk rows: a cluster of eight
+// CTAs sorts the chunk's (id, row) pairs (bitonic within each CTA, then
+// merge-path rounds through distributed shared memory) and marks where each
+// id's run starts, listing the long runs and grouping the short ones; one
+// persistent kernel then sums every run in a fixed order and adds the sum
+// into the fp32 gradient table, streaming the rows through shared memory with
+// cp.async.  Longer batches run chunk after chunk on the stream, so the
+// accumulation order is fixed.
+#include <cooperative_groups.h>
+
 #include "vpce_kernels.cuh"
 
 namespace vpce {
@@ -27,7 +30,6 @@ namespace {
 constexpr int kEmbThreads = 256;
 constexpr int kSortThreads = 1024;
 constexpr int kEmbChunk = 16384;  // rows sorted per backward chunk (128 KB of keys)
-constexpr unsigned long long kNoKey = ~0ull;
 constexpr int kHeavyRows = 64;  // ids with more rows are summed by a whole CTA
 constexpr int kGroupRows = 16;  // short-run tasks: runs starting in this many consecutive sorted rows
 
@@ -122,172 +124,306 @@ __global__ void __launch_bounds__(kEmbThreads) embed_forward_kernel(const __grid
 // ---------------------------------------------------------------------------
 // backward
 // ---------------------------------------------------------------------------
-constexpr int kSortBlock = 1024;  // keys sorted by one CTA before the merge rounds
+constexpr int kSortCtas = 8;                        // one thread-block cluster per chunk
+constexpr int kSortKeys = kEmbChunk / kSortCtas;    // keys per CTA, at most
+constexpr int kMaxHeavyPerCta = kSortKeys / (kHeavyRows + 1) + 1;
 
-// One CTA per kSortBlock keys: this block's (id << 32 | row) keys (kNoKey for
-// padding and for ids outside [0, V)), bitonic-sorted in shared memory.
-__global__ void __launch_bounds__(kSortBlock / 2) embed_block_sort_kernel(const long long* ids, int n, int n_pow2,
-                                                                          long long V, unsigned long long* out) {
-  __shared__ unsigned long long key[kSortBlock];
-  const int len = n_pow2 < kSortBlock ? n_pow2 : kSortBlock;
-  const int base = blockIdx.x * len;
-  for (int k = threadIdx.x; k < len; k += blockDim.x) {
-    const int g = base + k;
-    unsigned long long v = kNoKey;
-    if (g < n) {
-      const long long id = ids[g];
-      if (id >= 0 && id < V) v = (static_cast<unsigned long long>(id) << 32) | unsigned(g);
-    }
-    key[k] = v;
-  }
-  __syncthreads();
-  for (int size = 2; size <= len; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int k = threadIdx.x; k < len / 2; k += blockDim.x) {
-        const int lo = 2 * k - (k & (stride - 1));  // first element of this compare pair
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const unsigned long long x = key[lo], y = key[hi];
-        if ((x > y) == up) {
-          key[lo] = y;
-          key[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
-  for (int k = threadIdx.x; k < len; k += blockDim.x) out[base + k] = key[k];
-}
+// Sort keys (id << kShift | row): 32 bits when the ids and a chunk's rows fit
+// (ids below 2^18 - 2, rows below 2^14), 64 otherwise; kNone (padding and
+// ids outside [0, V)) sorts after every valid key.
+template <typename K>
+struct SortKey;
+template <>
+struct SortKey<unsigned> {
+  static constexpr int kShift = 14;
+  static constexpr unsigned kNone = 0xffffffffu;
+};
+template <>
+struct SortKey<unsigned long long> {
+  static constexpr int kShift = 32;
+  static constexpr unsigned long long kNone = ~0ull;
+};
+static_assert(kEmbChunk <= (1 << 14), "rows of a chunk fit the 32-bit key");
+constexpr long long kMaxV32 = (1LL << 18) - 2;  // vocabularies up to this size use 32-bit keys
 
-// One merge round: pairs of sorted runs of `width` keys become runs of
-// 2 * width.  Each key's place is its index in its own run plus the number of
-// keys of the partner run before it (a binary search; keys of the first run
-// go before equal keys of the second, so the padding keys stay in order).
-__global__ void embed_merge_kernel(const unsigned long long* in, unsigned long long* out, int width, int total) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= total) return;
-  const int pair = i / (2 * width), base = pair * 2 * width;
-  const int j = i - base;
-  const bool first = j < width;
-  const int own = first ? j : j - width;
-  const unsigned long long* other = in + base + (first ? width : 0);
-  const unsigned long long v = in[i];
-  int lo = 0, hi = width;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (first ? (other[mid] < v) : (other[mid] <= v)) lo = mid + 1;
-    else hi = mid;
-  }
-  out[base + own + lo] = v;
-}
-
-struct EmbedRunsParams {
-  const unsigned long long* keys;  // [n_pow2] sorted
-  int n_pow2;
-  int* seg;                        // [kEmbChunk + 1] start of each distinct id's run; seg[n_seg] = end
-  int* n_seg;
-  int* heavy;                      // [kEmbChunk / kHeavyRows] runs longer than kHeavyRows (any order)
-  int* n_heavy;
+struct EmbedSortParams {
+  const long long* ids;            // this chunk's ids
+  int n;                           // ids in the chunk
+  int n_pow2;                      // a power of two >= n and >= kSortCtas
+  long long V;
+  int* rows;                       // [n_pow2] out: the rows in (id, row) order, -1 for the padding last
+  int* seg;                        // [kEmbChunk + 1] start of each distinct id's run; seg[n_seg] = valid keys
+  int* heavy;                      // runs longer than kHeavyRows (any order)
   int* gstart;                     // [kEmbChunk / kGroupRows + 1] first run of each group of kGroupRows rows
-  int* n_grp;
-  unsigned* work;                  // [2] the accumulation's task counters, cleared here
+  unsigned long long* rtab;        // [kEmbChunk] each run's gradient-table row (address)
+  int* counts;                     // n_seg, n_heavy, n_grp, work[2] (the accumulation's counters, cleared)
   Header* hdr;                     // error flag (cleared when `first`)
   int first;                       // first chunk of the call
   ShardSet gsh;                    // fp32 gradient table shards
   int t;
-  unsigned long long* rtab;        // [kEmbChunk] each run's gradient-table row (address)
 };
 
-// One CTA: the start of every run of equal ids in the sorted keys (ids outside
-// [0, V) sorted last as kNoKey and are dropped), and the list of long runs.
-__global__ void __launch_bounds__(kSortThreads) embed_runs_kernel(const __grid_constant__ EmbedRunsParams p) {
-  __shared__ int warp_sum[kSortThreads / 32];
-  __shared__ int nh;
-  __shared__ long long start[VPCE_MAX_SHARDS + 1];
-  const int tid = threadIdx.x;
-  const unsigned long long* key = p.keys;
-  // run heads: a valid key whose id differs from its predecessor's
-  const int per = (p.n_pow2 + kSortThreads - 1) / kSortThreads;
-  const int k0 = tid * per;
-  int cnt = 0;
-  for (int k = k0; k < k0 + per && k < p.n_pow2; ++k) {
-    const unsigned long long v = key[k];
-    if (v != kNoKey && (k == 0 || (key[k - 1] >> 32) != (v >> 32))) ++cnt;
-  }
-  // exclusive scan of the per-thread counts (thread order = key order)
-  int incl = cnt;
-  const int lane = tid & 31, warp = tid >> 5;
+// Exclusive scan of one int per thread in thread order; *total gets the sum.
+__device__ __forceinline__ int block_scan(int v, int* warp_tmp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int x = __shfl_up_sync(kFull, incl, o);
     if (lane >= o) incl += x;
   }
-  if (lane == 31) warp_sum[warp] = incl;
-  for (int i = tid; i <= p.t; i += kSortThreads) start[i] = p.gsh.start[i];
-  if (tid == 0) {
-    nh = 0;
-    p.work[0] = 0u;
-    p.work[1] = 0u;
-    if (p.first) p.hdr->error_flag = 0;
-  }
+  if (lane == 31) warp_tmp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_sum[lane];
+    int w = lane < int(blockDim.x >> 5) ? warp_tmp[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int x = __shfl_up_sync(kFull, w, o);
       if (lane >= o) w += x;
     }
-    warp_sum[lane] = w;  // inclusive over warps
+    warp_tmp[lane] = w;  // inclusive over warps
   }
   __syncthreads();
-  int pos = incl - cnt + (warp > 0 ? warp_sum[warp - 1] : 0);
-  for (int k = k0; k < k0 + per && k < p.n_pow2; ++k) {
-    const unsigned long long v = key[k];
-    if (v != kNoKey && (k == 0 || (key[k - 1] >> 32) != (v >> 32))) p.seg[pos++] = k;
-  }
-  const int total = warp_sum[kSortThreads / 32 - 1];
-  if (tid == kSortThreads - 1) {
-    *p.n_seg = total;
-    // end of the last run: the number of valid keys, i.e. the first kNoKey
-    // of the sorted array (binary search)
-    int lo = 0, hi = p.n_pow2;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (key[mid] == kNoKey) hi = mid;
-      else lo = mid + 1;
+  const int ex = incl - v + (warp > 0 ? warp_tmp[warp - 1] : 0);
+  *total = warp_tmp[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return ex;
+}
+
+// One chunk's sort and run scan in one launch: a cluster of kSortCtas CTAs,
+// each holding B = n_pow2 / kSortCtas keys.
+//  1. CTA c builds the (id, row) keys of rows [c B, (c + 1) B) (kNone for
+//     padding and for ids outside [0, V)) and bitonic-sorts them in shared
+//     memory.
+//  2. One multiway merge: every CTA copies the other blocks from distributed
+//     shared memory, and a key's place is its index in its block plus its
+//     rank in each other block (blocks before c count keys <= it, blocks
+//     after count keys < it, so equal padding keys keep block order); the key
+//     is stored straight into the shared memory of the CTA that owns that
+//     place.
+//  3. The run heads (a valid key whose id differs from its predecessor's),
+//     numbered by a scan over the cluster, give the run starts; then each run's
+//     table row, the groups' first runs and the list of long runs.
+template <typename K>
+__global__ void __cluster_dims__(kSortCtas, 1, 1) __launch_bounds__(kSortThreads, 1)
+    embed_sort_runs_kernel(const __grid_constant__ EmbedSortParams p) {
+  namespace cg = cooperative_groups;
+  using KT = SortKey<K>;
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ __align__(16) unsigned char sort_raw[];  // [kSortCtas * B] blocks, then [B] sorted
+  __shared__ int warp_tmp[32];
+  __shared__ int tot[3];  // this CTA's valid keys, run heads, long runs
+  __shared__ int sh[4];   // head offset, total heads, valid keys, long-run offset
+  __shared__ int hcount;
+  __shared__ int hl[kMaxHeavyPerCta];
+  __shared__ long long start[VPCE_MAX_SHARDS + 1];
+  const int c = int(cluster.block_rank());
+  const int tid = threadIdx.x;
+  const int B = p.n_pow2 / kSortCtas;
+  K* blocks = reinterpret_cast<K*>(sort_raw);
+  K* mine = blocks + c * B;
+  K* sorted = blocks + kSortCtas * B;
+  for (int i = tid; i <= p.t; i += kSortThreads) start[i] = p.gsh.start[i];
+  for (int k = tid; k < B; k += kSortThreads) {
+    const int g = c * B + k;
+    K v = KT::kNone;
+    if (g < p.n) {
+      const long long id = p.ids[g];
+      if (id >= 0 && id < p.V) v = (static_cast<K>(id) << KT::kShift) | K(g);
     }
-    p.seg[total] = lo;
+    mine[k] = v;
   }
-  __syncthreads();  // seg[] (global) is complete and visible to the block
-  // the long runs, listed for the CTA-per-chunk kernel (their order does not
-  // matter: each run's sum is formed on its own)
-  for (int j = tid; j < total; j += kSortThreads) {
-    if (p.seg[j + 1] - p.seg[j] > kHeavyRows) p.heavy[atomicAdd(&nh, 1)] = j;
-    // the run's row of the gradient table (every key here has an id in range)
-    const long long id = static_cast<long long>(key[p.seg[j]] >> 32);
+  if (tid == 0) hcount = 0;
+  __syncthreads();
+  if (B <= kSortThreads) {
+    // one key per thread: strides below 32 exchange by shuffle, larger ones
+    // through shared memory (thread t >= B holds padding nobody reads)
+    K x = tid < B ? mine[tid] : KT::kNone;
+    for (int size = 2; size <= B; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        K y;
+        if (stride >= 32) {
+          __syncthreads();  // the previous exchange's reads are done
+          if (tid < B) mine[tid] = x;
+          __syncthreads();
+          y = tid < B ? mine[tid ^ stride] : KT::kNone;
+        } else {
+          y = __shfl_xor_sync(kFull, x, stride);
+        }
+        const bool up = (tid & size) == 0, low = (tid & stride) == 0;
+        x = low == up ? (x < y ? x : y) : (x < y ? y : x);
+      }
+    }
+    __syncthreads();
+    if (tid < B) mine[tid] = x;
+  } else {
+    for (int size = 2; size <= B; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int k = tid; k < B / 2; k += kSortThreads) {
+          const int lo = 2 * k - (k & (stride - 1));  // first element of this compare pair
+          const int hi = lo + stride;
+          const bool up = (lo & size) == 0;
+          const K x = mine[lo], y = mine[hi];
+          if ((x > y) == up) {
+            mine[lo] = y;
+            mine[hi] = x;
+          }
+        }
+        __syncthreads();
+      }
+    }
+  }
+  cluster.sync();  // every block is sorted
+  for (int i = tid; i < kSortCtas * B; i += kSortThreads) {
+    const int r = i / B;
+    if (r != c) blocks[i] = *cluster.map_shared_rank(&blocks[i], r);
+  }
+  __syncthreads();
+  // rank of key v in block r: the keys of block r before v in the merged
+  // order (blocks before c: keys <= v; after c: keys < v), searched in
+  // [lo, hi] (the rank is known to lie there) in lockstep steps of p, p/2, .., 1
+  auto before = [&](int r, K x, K v) { return r < c ? (x <= v) : (x < v); };
+  const int lane = tid & 31;
+  for (int k = tid; k < B; k += kSortThreads) {
+    const K v = mine[k];
+    int lo[kSortCtas], hi[kSortCtas];
+#pragma unroll
+    for (int r = 0; r < kSortCtas; ++r) {
+      lo[r] = 0;
+      hi[r] = B;
+    }
+    if (B >= 32) {
+      // the warp's 32 keys are consecutive: lanes 0..13 find the ranks of the
+      // first and the last of them in the 7 other blocks, which bound every
+      // lane's rank
+      const int k0 = k - lane;
+      const int which = lane & 1, oth = lane >> 1;  // other block number oth (skipping c)
+      const int rb = oth < c ? oth : oth + 1;
+      int pos = 0;
+      if (lane < 2 * (kSortCtas - 1)) {
+        const K ve = mine[k0 + (which ? 31 : 0)];
+        for (int step = B; step >= 1; step >>= 1)
+          if (pos + step <= B && before(rb, blocks[rb * B + pos + step - 1], ve)) pos += step;
+      }
+#pragma unroll
+      for (int j = 0; j < kSortCtas - 1; ++j) {
+        const int r = j < c ? j : j + 1;  // warp-uniform
+        const int l = __shfl_sync(kFull, pos, 2 * j), h = __shfl_sync(kFull, pos, 2 * j + 1);
+#pragma unroll
+        for (int rr = 0; rr < kSortCtas; ++rr)
+          if (rr == r) {
+            lo[rr] = l;
+            hi[rr] = h;
+          }
+      }
+    }
+    int span = 0;
+#pragma unroll
+    for (int r = 0; r < kSortCtas; ++r) span = r == c ? span : max(span, hi[r] - lo[r]);
+    int p2 = 1;
+    while (p2 < span) p2 <<= 1;
+    int o = k;
+#pragma unroll
+    for (int r = 0; r < kSortCtas; ++r) {
+      if (r == c) continue;
+      int pos = lo[r];
+      for (int step = p2; step >= 1; step >>= 1)
+        if (pos + step <= hi[r] && before(r, blocks[r * B + pos + step - 1], v)) pos += step;
+      o += pos;
+    }
+    *cluster.map_shared_rank(&sorted[o % B], o / B) = v;
+  }
+  cluster.sync();  // the sorted keys: rows [c B, (c + 1) B) in CTA c's `sorted`
+  const K* key = sorted;
+  for (int k = tid; k < B; k += kSortThreads)
+    p.rows[c * B + k] = key[k] == KT::kNone ? -1 : int(key[k] & ((K(1) << KT::kShift) - 1));
+  const K prev_last = c > 0 ? *cluster.map_shared_rank(&sorted[B - 1], c - 1) : KT::kNone;
+  const int per = (B + kSortThreads - 1) / kSortThreads;  // this thread's keys: [k0, k0 + per)
+  const int k0 = tid * per;
+  auto is_head = [&](int k) {
+    const K v = key[k];
+    if (v == KT::kNone) return false;
+    if (c == 0 && k == 0) return true;
+    const K pv = k > 0 ? key[k - 1] : prev_last;  // valid: valid keys come first
+    return (pv >> KT::kShift) != (v >> KT::kShift);
+  };
+  int nv = 0, nh = 0;
+  for (int k = k0; k < k0 + per && k < B; ++k) {
+    nv += key[k] != KT::kNone;
+    nh += is_head(k);
+  }
+  int vtot, htot;
+  block_scan(nv, warp_tmp, &vtot);
+  const int hex = block_scan(nh, warp_tmp, &htot);
+  if (tid == 0) {
+    tot[0] = vtot;
+    tot[1] = htot;
+  }
+  cluster.sync();
+  if (tid == 0) {
+    int hoff = 0, total = 0, nvalid = 0;
+    for (int r = 0; r < kSortCtas; ++r) {
+      const int* rt = cluster.map_shared_rank(tot, r);
+      const int hr = rt[1];
+      if (r < c) hoff += hr;
+      total += hr;
+      nvalid += rt[0];
+    }
+    sh[0] = hoff;
+    sh[1] = total;
+    sh[2] = nvalid;
+  }
+  __syncthreads();
+  const int total = sh[1], nvalid = sh[2];
+  int j = sh[0] + hex;
+  for (int k = k0; k < k0 + per && k < B; ++k)
+    if (is_head(k)) p.seg[j++] = c * B + k;
+  if (c == 0 && tid == 0) p.seg[total] = nvalid;
+  cluster.sync();  // every run start is in global memory
+  const int ngrp = (nvalid + kGroupRows - 1) / kGroupRows;
+  j = sh[0] + hex;
+  for (int k = k0; k < k0 + per && k < B; ++k) {
+    if (!is_head(k)) continue;
+    const int a = c * B + k, b = p.seg[j + 1];
+    if (b - a > kHeavyRows) hl[atomicAdd(&hcount, 1)] = j;
+    const long long id = static_cast<long long>(key[k] >> KT::kShift);
     const int i = shard_of(start, p.t, id);
     p.rtab[j] = reinterpret_cast<unsigned long long>(p.gsh.ptr[i] + (id - start[i]) * p.gsh.ld_bytes[i]);
+    // groups g with g kGroupRows in (previous run start, a] begin with run j
+    const int g_lo = j == 0 ? 0 : p.seg[j - 1] / kGroupRows + 1;
+    for (int g = g_lo; g <= a / kGroupRows; ++g) p.gstart[g] = j;
+    if (j == total - 1)  // groups after the last run start are empty
+      for (int g = a / kGroupRows + 1; g <= ngrp; ++g) p.gstart[g] = total;
+    ++j;
   }
-  // groups of kGroupRows sorted rows: group g holds the runs that start in
-  // [g kGroupRows, (g + 1) kGroupRows); gstart[g] is its first run
-  const int nvalid = p.seg[total];
-  const int ngrp = (nvalid + kGroupRows - 1) / kGroupRows;
-  for (int j = tid; j < total; j += kSortThreads) {
-    const int g_lo = j == 0 ? 0 : p.seg[j - 1] / kGroupRows + 1, g_hi = p.seg[j] / kGroupRows;
-    for (int g = g_lo; g <= g_hi; ++g) p.gstart[g] = j;
-  }
-  for (int g = (total > 0 ? p.seg[total - 1] / kGroupRows + 1 : 0) + tid; g <= ngrp; g += kSortThreads)
-    p.gstart[g] = total;
+  if (total == 0 && c == 0 && tid == 0) p.gstart[0] = 0;
   __syncthreads();
+  if (tid == 0) tot[2] = hcount;
+  cluster.sync();
   if (tid == 0) {
-    *p.n_heavy = nh;
-    *p.n_grp = ngrp;
+    int off = 0, nheavy = 0;
+    for (int r = 0; r < kSortCtas; ++r) {
+      const int hr = cluster.map_shared_rank(tot, r)[2];
+      if (r < c) off += hr;
+      nheavy += hr;
+    }
+    sh[3] = off;
+    if (c == 0) {
+      p.counts[0] = total;
+      p.counts[1] = nheavy;
+      p.counts[2] = ngrp;
+      p.counts[3] = 0;  // the accumulation's task counters
+      p.counts[4] = 0;
+      if (p.first) p.hdr->error_flag = 0;
+    }
   }
+  __syncthreads();
+  for (int i = tid; i < hcount; i += kSortThreads) p.heavy[sh[3] + i] = hl[i];
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 struct EmbedAccParams {
-  const unsigned long long* keys;
+  const int* rows;  // the chunk's rows in (id, row) order
   const int* seg;
   const int* n_seg;
   const int* heavy;
@@ -505,14 +641,14 @@ __global__ void __launch_bounds__(kAThreads) embed_accum_kernel(const __grid_con
       float acc[4 * SH::kQuads];
 #pragma unroll
       for (int e = 0; e < 4 * SH::kQuads; ++e) acc[e] = 0.f;
-      Window<unsigned long long> kw;
-      kw.init(p.keys, nkeys, lo, lane);
+      Window<int> kw;
+      kw.init(p.rows, nkeys, lo, lane);
       long long pk = lo;
       for (int k = lo; k < hi && ok; ++k) {
         while (pk < hi && issued - consumed < unsigned(C::kRH)) {
-          const unsigned long long key = kw.at(pk++, lane);
+          const int row = kw.at(pk++, lane);
           const int slot = int(issued % C::kRH);
-          stage_row<EB, kHeavyCols>(ring, slot, lane, p.grad + (long long)(key & 0xffffffffu) * p.ld_grad_bytes, c0, h,
+          stage_row<EB, kHeavyCols>(ring, slot, lane, p.grad + (long long)row * p.ld_grad_bytes, c0, h,
                                     &sm.bar_h[w][slot]);
           ++issued;
         }
@@ -570,8 +706,8 @@ __global__ void __launch_bounds__(kAThreads) embed_accum_kernel(const __grid_con
     sw.init(p.seg, total + 1, ps, lane);
     Window<unsigned long long> pw;
     pw.init(p.rtab, total, ps, lane);
-    Window<unsigned long long> kw;
-    kw.init(p.keys, nkeys, sw.at(ps, lane), lane);
+    Window<int> kw;
+    kw.init(p.rows, nkeys, sw.at(ps, lane), lane);
     long long pk = 0, pend = 0;
     bool pdone = false;
     // keeps the ring full: the rows of the task's short runs in order, a
@@ -607,9 +743,9 @@ __global__ void __launch_bounds__(kAThreads) embed_accum_kernel(const __grid_con
           pk = a;
           pend = b;
         }
-        const unsigned long long key = kw.at(pk, lane);
+        const int row = kw.at(pk, lane);
         const int slot = int(issued % C::kRS);
-        stage_row<EB, kShortCols>(ring, slot, lane, p.grad + (long long)(key & 0xffffffffu) * p.ld_grad_bytes, c0, h,
+        stage_row<EB, kShortCols>(ring, slot, lane, p.grad + (long long)row * p.ld_grad_bytes, c0, h,
                                   &sm.bar_s[w][slot]);
         ++issued;
         ++pk;
@@ -656,12 +792,11 @@ int g_accum_ctas[2] = {1, 1};  // resident CTAs per SM of embed_accum_kernel<2>,
 }  // namespace
 
 // Workspace: a header (its error flag is where vpce_read_error_flag looks),
-// the two key buffers of the sort, the run starts, the long-run list, the
-// group starts and the counters.
+// the sorted keys, the run starts, the long-run list, the group starts, the
+// runs' table rows and the counters.
 struct EmbedWs {
   Header* hdr;
-  unsigned long long* keys_a;
-  unsigned long long* keys_b;
+  int* rows;
   int* seg;
   int* heavy;
   int* gstart;
@@ -670,7 +805,7 @@ struct EmbedWs {
 };
 
 size_t embed_bwd_workspace_bytes() {
-  return 256 + 2 * round256(sizeof(unsigned long long) * kEmbChunk) + round256(sizeof(int) * (kEmbChunk + 1)) +
+  return 256 + round256(sizeof(int) * kEmbChunk) + round256(sizeof(int) * (kEmbChunk + 1)) +
          round256(sizeof(int) * (kEmbChunk / kHeavyRows)) + round256(sizeof(int) * (kEmbChunk / kGroupRows + 1)) +
          round256(sizeof(unsigned long long) * kEmbChunk) + 256;
 }
@@ -680,10 +815,8 @@ EmbedWs embed_ws(void* ws) {
   EmbedWs e;
   e.hdr = reinterpret_cast<Header*>(w);
   w += 256;
-  e.keys_a = reinterpret_cast<unsigned long long*>(w);
-  w += round256(sizeof(unsigned long long) * kEmbChunk);
-  e.keys_b = reinterpret_cast<unsigned long long*>(w);
-  w += round256(sizeof(unsigned long long) * kEmbChunk);
+  e.rows = reinterpret_cast<int*>(w);
+  w += round256(sizeof(int) * kEmbChunk);
   e.seg = reinterpret_cast<int*>(w);
   w += round256(sizeof(int) * (kEmbChunk + 1));
   e.heavy = reinterpret_cast<int*>(w);
@@ -696,9 +829,18 @@ EmbedWs embed_ws(void* ws) {
   return e;
 }
 
+// keys of all blocks plus the CTA's sorted slice
+size_t sort_smem_bytes(int n_pow2, size_t key_bytes) { return size_t(kSortCtas + 1) * (n_pow2 / kSortCtas) * key_bytes; }
+
 cudaError_t set_embed_smem() {
-  cudaError_t e = cudaFuncSetAttribute(embed_accum_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(sizeof(AccSmem<2>)));
+  cudaError_t e = cudaFuncSetAttribute(embed_sort_runs_kernel<unsigned>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(sort_smem_bytes(kEmbChunk, 4)));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(embed_sort_runs_kernel<unsigned long long>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(sort_smem_bytes(kEmbChunk, 8)));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(embed_accum_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(sizeof(AccSmem<2>)));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(embed_accum_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(sizeof(AccSmem<4>)));
@@ -742,38 +884,29 @@ cudaError_t launch_embed_backward(const void* grad, int grad_bf16, long long ld_
   const int eb = grad_bf16 ? 2 : 4;
   for (long long r0 = 0; r0 < s; r0 += kEmbChunk) {
     const int n = int(s - r0 < kEmbChunk ? s - r0 : kEmbChunk);
-    int n2 = 2;
+    int n2 = kSortCtas;
     while (n2 < n) n2 <<= 1;
-    // sort: blocks of kSortBlock keys, then merge rounds (ping-pong buffers)
-    const int blk = n2 < kSortBlock ? n2 : kSortBlock;
-    embed_block_sort_kernel<<<n2 / blk, kSortBlock / 2, 0, st>>>(ids + r0, n, n2, V, W.keys_a);
-    unsigned long long* cur = W.keys_a;
-    unsigned long long* nxt = W.keys_b;
-    for (int width = blk; width < n2; width <<= 1) {
-      embed_merge_kernel<<<(n2 + 255) / 256, 256, 0, st>>>(cur, nxt, width, n2);
-      unsigned long long* tmp = cur;
-      cur = nxt;
-      nxt = tmp;
-    }
-    unsigned long long* keys = cur;
-    EmbedRunsParams rp;
-    rp.keys = keys;
-    rp.n_pow2 = n2;
-    rp.seg = W.seg;
-    rp.n_seg = n_seg;
-    rp.heavy = W.heavy;
-    rp.n_heavy = n_heavy;
-    rp.gstart = W.gstart;
-    rp.n_grp = n_grp;
-    rp.work = work;
-    rp.hdr = W.hdr;
-    rp.first = r0 == 0;
-    rp.gsh = gsh;
-    rp.t = t;
-    rp.rtab = W.rtab;
-    embed_runs_kernel<<<1, kSortThreads, 0, st>>>(rp);
+    EmbedSortParams sp;
+    sp.ids = ids + r0;
+    sp.n = n;
+    sp.n_pow2 = n2;
+    sp.V = V;
+    sp.rows = W.rows;
+    sp.seg = W.seg;
+    sp.heavy = W.heavy;
+    sp.gstart = W.gstart;
+    sp.rtab = W.rtab;
+    sp.counts = W.counts;
+    sp.hdr = W.hdr;
+    sp.first = r0 == 0;
+    sp.gsh = gsh;
+    sp.t = t;
+    if (V <= kMaxV32)
+      embed_sort_runs_kernel<unsigned><<<kSortCtas, kSortThreads, sort_smem_bytes(n2, 4), st>>>(sp);
+    else
+      embed_sort_runs_kernel<unsigned long long><<<kSortCtas, kSortThreads, sort_smem_bytes(n2, 8), st>>>(sp);
     EmbedAccParams ap;
-    ap.keys = keys;
+    ap.rows = W.rows;
     ap.seg = W.seg;
     ap.n_seg = n_seg;
     ap.heavy = W.heavy;
