@@ -565,13 +565,18 @@ def run_lmhead(args):
     if train:
         gx = torch.empty_like(x)
         gw = [torch.zeros((w.shape[0], m.h), dtype=torch.float32, device=dev) for w in ws]
-        bwk = torch.empty(vpce.vpce_lmhead_backward_workspace_bytes(m.V, m.h), dtype=torch.uint8, device=dev)
+        twk = torch.empty(vpce.vpce_lmhead_forward_backward_workspace_bytes(m.s, m.V, m.h), dtype=torch.uint8,
+                          device=dev)
+
+    def call(xi, yi, li, wki):
+        if train:
+            vpce.vpce_lmhead_forward_backward(xi, ws, yi, vs, ignore_index=m.ignore_index, loss_out=li,
+                                              grad_hidden=gx, grad_weight_shards=gw, workspace=twk)
+        else:
+            vpce.vpce_lmhead_forward(xi, ws, yi, vs, ignore_index=m.ignore_index, loss_out=li, workspace=wki)
 
     def step():
-        vpce.vpce_lmhead_forward(x, ws, y, vs, ignore_index=m.ignore_index, loss_out=loss, workspace=wk)
-        if train:
-            vpce.vpce_lmhead_backward(x, ws, y, wk, vs, ignore_index=m.ignore_index, grad_hidden=gx,
-                                      grad_weight_shards=gw, workspace=bwk)
+        call(x, y, loss, wk)
 
     for _ in range(args.warmup):
         step()
@@ -625,11 +630,7 @@ def run_lmhead(args):
             yb[b].copy_(hy, non_blocking=True)
             done[b].record(cs)
         stream.wait_event(done[b])
-        vpce.vpce_lmhead_forward(xb[b], ws, yb[b], vs, ignore_index=m.ignore_index, loss_out=lb[b],
-                                 workspace=wkb[b])
-        if train:
-            vpce.vpce_lmhead_backward(xb[b], ws, yb[b], wkb[b], vs, ignore_index=m.ignore_index, grad_hidden=gx,
-                                      grad_weight_shards=gw, workspace=bwk)
+        call(xb[b], yb[b], lb[b], wkb[b])
         host_loss[max(k, 0)].copy_(lb[b], non_blocking=True)
         used[b].record(stream)
     e1.record(stream)
@@ -640,8 +641,8 @@ def run_lmhead(args):
             dist.destroy_process_group()
         return
 
-    # forward: one product; backward: the logits again, dX and dW
-    flops = 2.0 * m.s * m.h * m.V * (4 if train else 1)
+    # forward: one product (the logits); training: also dX and dW
+    flops = 2.0 * m.s * m.h * m.V * (3 if train else 1)
     burst, sustained, kind = _tensor_peaks()
     achieved = flops / (call_ms * 1e-3) / 1e12
     ms_step = total_ms / args.steps
@@ -668,12 +669,13 @@ def run_lmhead(args):
             "l2": f"inputs larger than L2: the head is {sum(w.numel() for w in ws) * 2 / 1e9:.2f} GB",
             "path": "vpce_lmhead_forward (tcgen05 GEMM, fp32 accumulators in TMEM, loss statistics in the "
                     "epilogue; the logits are never written), then the shard combine"
-                    + ("; vpce_lmhead_backward (per 4096-row chunk: tcgen05 recompute writing bf16 dZ, then "
-                       "cuBLAS dX = dZ W and dW += dZ^T X)" if train else ""),
+                    + ("; training: vpce_lmhead_forward_backward, per 4096-row chunk the same GEMM keeping the "
+                       "chunk's fp32 logits, a row kernel (logsumexp, loss, bf16 dZ), then cuBLAS dX = dZ W and "
+                       "dW += dZ^T X" if train else ""),
         },
         "tflops": round(achieved, 1),
         "roofline": {
-            "kernel": "gemm_stats_kernel" + (" + recompute + cuBLAS dX, dW (the whole step)" if train else ""),
+            "kernel": "gemm_stats_kernel" + (" + row kernel + cuBLAS dX, dW (the whole step)" if train else ""),
             "bound": "tensor",
             "achieved": round(achieved, 1),
             "peak": burst,
@@ -683,7 +685,7 @@ def run_lmhead(args):
             "frac_of_sustained": round(achieved / sustained, 4),
             "traffic": None,
             "algorithmic_flops_per_launch": flops,
-            "note": ("achieved = 8 s h V / mean CUDA-event time of one forward + backward step" if train else
+            "note": ("achieved = 6 s h V (logits, dX, dW) / mean CUDA-event time of one training step" if train else
                      "achieved = 2 s h V / mean CUDA-event time of one call (the GEMM launch plus the few-us combine)"),
         },
         "e2e": {
@@ -696,12 +698,13 @@ def run_lmhead(args):
             "note": "pinned host hidden states + targets copied in every step (copy stream, double-buffered), "
                     "loss read back; the head's weights stay on the device",
         },
-        "gpu_launches": (2 + (m.s + 4095) // 4096 * 2 if train else 2) * args.steps,
+        "gpu_launches": (2 + (m.s + 4095) // 4096 * 3 if train else 2) * args.steps,
         "clocks": clk,
     }
     if train:
-        out["gpu_launches_note"] = ("forward 2 + per row chunk: the tcgen05 dlogits kernel and the dX conversion; "
-                                    "the 2 t cuBLAS GEMMs per chunk are library launches, not counted")
+        out["gpu_launches_note"] = ("the n_valid prologue and the loss sum, and per row chunk the tcgen05 GEMM, the "
+                                    "row kernel and the dX conversion; the 2 t cuBLAS GEMMs per chunk are library "
+                                    "launches, not counted")
     if world == 1 and not args.no_cpu_baseline and not train:
         # the oracle on a bounded sample: a few rows against the first vocabulary
         # rows of the head (read back from the device generator), scaled to the

@@ -335,6 +335,44 @@ vpce_status vpce_lmhead_backward(const void* hidden, int64_t ld_hidden,
                                  void* workspace, size_t workspace_bytes, vpce_stream_t stream);
 
 /*
+ * vpce_lmhead_forward followed by vpce_lmhead_backward in one call, for a
+ * training step whose upstream gradient is known up front (grad_output, or
+ * grad_rows per row): loss, dX and dW without forming any logits twice.
+ * Per row chunk, the tensor-core kernel writes the loss statistics and keeps
+ * the chunk's fp32 logits in the workspace (a chunk is the unit the CMU notes
+ * (§5.5) keep resident instead of the whole [s, V] tensor).  A row kernel
+ * then forms each row's logsumexp, loss and bf16 dZ from them, and cuBLAS
+ * computes dX = dZ W and dW += dZ^T X.
+ *   loss_out, row_loss_out, reduction   as vpce_lmhead_forward (the mean
+ *                  divides by the batch's n_valid; the loss sum is fp64 over
+ *                  fixed 256-row blocks).
+ *   grad_output, grad_rows, grad_hidden, grad_weight_shards, their strides
+ *                  as vpce_lmhead_backward.  VPCE_NONE requires grad_rows.
+ *   workspace      256-byte aligned.  With
+ *                  vpce_lmhead_forward_backward_workspace_bytes(s, V, h)
+ *                  bytes, chunks are min(4096, s rounded up to 128) rows.
+ *                  Each chunk holds [R, V] fp32 logits and [R, V] bf16 dZ,
+ *                  2.1 GB and 1.05 GB at R = 4096, V = 128256, plus 32 MiB of
+ *                  cuBLAS scratch.  A smaller workspace gives chunks smaller
+ *                  by steps of 128 rows; less than 128 rows' worth returns
+ *                  VPCE_ERR_WORKSPACE.  The workspace starts with the loss
+ *                  header: vpce_read_error_flag works on it.
+ * Other arguments and errors as vpce_lmhead_forward and vpce_lmhead_backward.
+ * The results equal those two calls' up to the column grouping of the
+ * logsumexp (the same arithmetic on a different split of the columns).
+ */
+size_t vpce_lmhead_forward_backward_workspace_bytes(int64_t s, int64_t V, int64_t h);
+vpce_status vpce_lmhead_forward_backward(const void* hidden, int64_t ld_hidden,
+                                         const void* const* weight_shards, int64_t ld_weight,
+                                         int t, int64_t s, int64_t h, const int64_t* vocab_start,
+                                         const int64_t* targets, int64_t ignore_index,
+                                         vpce_reduction reduction, float grad_output,
+                                         const float* grad_rows, float* loss_out, float* row_loss_out,
+                                         void* grad_hidden, int64_t ld_grad_hidden,
+                                         float* const* grad_weight_shards, int64_t ld_grad_weight,
+                                         void* workspace, size_t workspace_bytes, vpce_stream_t stream);
+
+/*
  * Vocabulary-parallel input embedding ("Distributed Training III: Model
  * Parallelism", CMU 11-868 Lecture 16 notes, §5.5; "LLM Internals" §7.3.4):
  * the table [V, h] is split by vocabulary into t shards; card i looks up only

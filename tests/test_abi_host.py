@@ -195,6 +195,50 @@ def test_lmhead_rejects_bad_arguments(lib, kw, code):
     assert _lmhead(**kw) == code
 
 
+def _lmhead_fb(lib, **kw):
+    args = dict(hidden=ctypes.c_void_p(FAKE), ld_hidden=0, weights=[FAKE, FAKE + 4096], ld_weight=0, t=2, s=4,
+                h=128, vocab_start=[0, 16, 40], targets=ctypes.c_void_p(FAKE), ignore_index=-100,
+                reduction=vpce.VPCE_MEAN, grad=1.0, grad_rows=None, loss=ctypes.c_void_p(FAKE), row_loss=None,
+                grad_hidden=ctypes.c_void_p(FAKE), ld_grad_hidden=0, grad_weights=[FAKE + 8192, FAKE + 16384],
+                ld_grad_weight=0, ws=ctypes.c_void_p(FAKE), ws_bytes=1 << 30)
+    args.update(kw)
+    return lib.vpce_lmhead_forward_backward(
+        args["hidden"], args["ld_hidden"], ctypes.cast(vpce._ptr_array(args["weights"]), ctypes.c_void_p),
+        args["ld_weight"], args["t"], args["s"], args["h"], vpce._i64_array(args["vocab_start"]), args["targets"],
+        args["ignore_index"], args["reduction"], args["grad"], args["grad_rows"], args["loss"], args["row_loss"],
+        args["grad_hidden"], args["ld_grad_hidden"],
+        ctypes.cast(vpce._ptr_array(args["grad_weights"]), ctypes.c_void_p), args["ld_grad_weight"], args["ws"],
+        args["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h=100), 1),                                # not a multiple of 64
+    (dict(grad=float("inf")), 1),
+    (dict(reduction=vpce.VPCE_NONE, loss=None, row_loss=ctypes.c_void_p(FAKE)), 1),  # 'none' needs grad_rows
+    (dict(grad_weights=[FAKE, 0]), 1),
+    (dict(grad_hidden=None), 1),
+    (dict(hidden=ctypes.c_void_p(FAKE + 8)), 2),
+    (dict(grad_weights=[FAKE + 8, FAKE + 4096]), 2),  # fp32 gradient shards are 16-byte aligned
+    (dict(ws=ctypes.c_void_p(FAKE + 64)), 2),
+    (dict(ws_bytes=1 << 20), 4),                      # less than one 128-row chunk
+])
+def test_lmhead_forward_backward_rejects_bad_arguments(lib, kw, code):
+    assert _lmhead_fb(lib, **kw) == code
+
+
+def test_lmhead_forward_backward_workspace_size(lib):
+    f = lib.vpce_lmhead_forward_backward_workspace_bytes
+    r256 = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    s, V, h = 8192, 128256, 8192
+    R = 4096
+    ld = (V + 7) // 8 * 8 + 8 * 64  # the padded row's bound: each shard's columns start at a multiple of 8
+    want = (256 + 2 * r256(4 * s) + r256(8 * 256 * R) + r256(4 * R) + r256(4 * R * ld)
+            + r256(2 * R * ld) + r256(4 * R * h) + (32 << 20))
+    assert f(s, V, h) == want
+    assert f(300, 5000, 512) < f(8192, 5000, 512)   # chunks no larger than the batch (rounded to 128)
+    assert f(-1, V, h) == 0 and f(s, 0, h) == 0
+
+
 def test_embedding_rejects_bad_arguments(lib):
     vs = vpce._i64_array([0, 8, 16])
     two = ctypes.cast(vpce._ptr_array([FAKE, FAKE + 4096]), ctypes.c_void_p)

@@ -185,21 +185,54 @@ def _bwd_workspace(V, h, rows):
                        device="cuda")
 
 
-def _check_backward(m, vs=None, *, reduction="mean", grad=1.0, grad_rows=None, chunk_rows=None):
+def _train_workspace(s, V, h, rows):
+    """vpce_lmhead_forward_backward workspace for chunks of `rows` rows:
+    header, logsumexp and row losses of the batch, then per chunk the column
+    groups' partials, target logits, fp32 logits and bf16 dZ (rows padded per
+    shard), fp32 dX and the cuBLAS scratch."""
+    r256 = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    ld = (V + 7) // 8 * 8 + 8 * 64  # each shard's columns padded to a multiple of 8
+    size = (256 + 2 * r256(4 * s) + r256(8 * 256 * rows) + r256(4 * rows) + r256(4 * rows * ld)
+            + r256(2 * rows * ld) + r256(4 * rows * h) + (32 << 20))
+    return torch.empty(size, dtype=torch.uint8, device="cuda")
+
+
+def _check_backward(m, vs=None, *, reduction="mean", grad=1.0, grad_rows=None, chunk_rows=None, fused=False):
+    """dX and dW against the oracle; with fused, through
+    vpce_lmhead_forward_backward, whose row losses and loss are checked as
+    the forward's are."""
     vs = synth.even_vocab_start(m.V, m.t) if vs is None else list(vs)
     meta = synth.lmhead_meta(m)
     x, ws = synth.lmhead_device(m, vs)
     y = torch.from_numpy(meta.targets).cuda()
-    rl = torch.empty(m.s, dtype=torch.float32, device="cuda")
-    _, fwk = vpce.vpce_lmhead_forward(x, ws, y, vs, ignore_index=m.ignore_index, reduction=reduction,
-                                      row_loss_out=rl)
+    rl = torch.full((m.s,), -7.0, dtype=torch.float32, device="cuda")
     gw0 = [torch.full((w.shape[0], m.h), 0.5, dtype=torch.float32, device="cuda") for w in ws]
     gr = torch.from_numpy(np.asarray(grad_rows, dtype=np.float32)).cuda() if grad_rows is not None else None
-    bwk = _bwd_workspace(m.V, m.h, chunk_rows) if chunk_rows else None
-    dx, dw = vpce.vpce_lmhead_backward(x, ws, y, fwk, vs, ignore_index=m.ignore_index, grad_output=grad,
-                                       grad_rows=gr, grad_weight_shards=gw0, workspace=bwk)
+    if fused:
+        loss_t = torch.full((), -7.0, dtype=torch.float32, device="cuda")
+        twk = _train_workspace(m.s, m.V, m.h, chunk_rows) if chunk_rows else None
+        _, dx, dw = vpce.vpce_lmhead_forward_backward(x, ws, y, vs, ignore_index=m.ignore_index, reduction=reduction,
+                                                      grad_output=grad, grad_rows=gr, loss_out=loss_t,
+                                                      row_loss_out=rl, grad_weight_shards=gw0, workspace=twk)
+    else:
+        _, fwk = vpce.vpce_lmhead_forward(x, ws, y, vs, ignore_index=m.ignore_index, reduction=reduction,
+                                          row_loss_out=rl)
+        bwk = _bwd_workspace(m.V, m.h, chunk_rows) if chunk_rows else None
+        dx, dw = vpce.vpce_lmhead_backward(x, ws, y, fwk, vs, ignore_index=m.ignore_index, grad_output=grad,
+                                           grad_rows=gr, grad_weight_shards=gw0, workspace=bwk)
     torch.cuda.synchronize()
     xh, wh = _host(m, vs)
+    if fused:
+        z = O.lmhead_logits(xh, wh, vs)
+        ref = O.cross_entropy(z, meta.targets, m.ignore_index, reduction=reduction)
+        got_rows = rl.cpu().numpy().astype(np.float64)
+        valid = ref["valid"]
+        bound = _row_bound(xh, wh, m.h)
+        assert np.all(np.abs(got_rows - ref["row_loss"])[valid] <= bound[valid])
+        assert np.all(got_rows[meta.targets == m.ignore_index] == 0.0)
+        exp_loss = ref["loss"] if np.ndim(ref["loss"]) == 0 else float(ref["row_loss"].sum())
+        got_loss = float(loss_t.item())
+        assert abs(got_loss - exp_loss) <= LOSS_RTOL * abs(exp_loss), (got_loss, exp_loss)
     if grad_rows is not None:
         ref_x, ref_w, dz = O.lmhead_backward(xh, wh, vs, meta.targets, m.ignore_index,
                                              grad=np.asarray(grad_rows, dtype=np.float64), reduction="none")
@@ -241,3 +274,52 @@ def test_lmhead_backward_sum_and_per_row_gradients():
 def test_lmhead_backward_small_workspace_chunks():
     # a workspace for 128-row chunks: 1200 rows run as 10 chunks, dW accumulated across them
     _check_backward(synth.LmHead("bwd_small_ws", 22, 1200, 128, 700, 7, ignore_frac=0.1), chunk_rows=128)
+
+
+# ------------------------------------------------ forward and backward in one call
+@pytest.mark.parametrize("m,vs", [
+    (synth.LMHEADS["lmhead_s300_h512_v5000"], None),                    # ragged tiles, ignored rows
+    (synth.LmHead("fb_chunks", 23, 1200, 128, 700, 7, ignore_frac=0.1), None),   # several M tiles
+    (synth.LmHead("fb_uneven", 24, 130, 64, 601, 3), [0, 1, 300, 601]),  # one-column shard, odd V
+    (synth.LmHead("fb_deep", 25, 256, 8192, 2000, 2), None),             # the pages' hidden size
+])
+def test_lmhead_forward_backward_parity(m, vs):
+    _check_backward(m, vs, fused=True)
+
+
+def test_lmhead_forward_backward_sum_and_per_row_gradients():
+    m = synth.LmHead("fb_red", 26, 200, 128, 900, 2, ignore_frac=0.1)
+    _check_backward(m, reduction="sum", grad=0.75, fused=True)
+    g = np.random.default_rng(3).normal(size=m.s).astype(np.float32)
+    g[::7] = 0.0
+    _check_backward(m, reduction="none", grad_rows=g, fused=True)
+
+
+def test_lmhead_forward_backward_small_workspace_chunks():
+    # 128-row chunks: 1200 rows as 10 chunks; the loss is the whole batch's
+    _check_backward(synth.LmHead("fb_small_ws", 27, 1200, 128, 700, 7, ignore_frac=0.1), chunk_rows=128,
+                    fused=True)
+
+
+def test_lmhead_forward_backward_matches_two_calls():
+    """The one-call step against vpce_lmhead_forward + vpce_lmhead_backward on
+    the same inputs: row losses within the forward's bound, gradients within
+    a few bf16 steps (the logsumexp's column grouping may differ)."""
+    m = synth.LmHead("fb_vs_two", 28, 500, 256, 3000, 4, ignore_frac=0.05)
+    vs = synth.even_vocab_start(m.V, m.t)
+    meta = synth.lmhead_meta(m)
+    x, ws = synth.lmhead_device(m, vs)
+    y = torch.from_numpy(meta.targets).cuda()
+    rl1 = torch.empty(m.s, dtype=torch.float32, device="cuda")
+    rl2 = torch.empty(m.s, dtype=torch.float32, device="cuda")
+    l1, dx1, dw1 = vpce.vpce_lmhead_forward_backward(x, ws, y, vs, ignore_index=m.ignore_index, row_loss_out=rl1)
+    l2, fwk = vpce.vpce_lmhead_forward(x, ws, y, vs, ignore_index=m.ignore_index, row_loss_out=rl2)
+    dx2, dw2 = vpce.vpce_lmhead_backward(x, ws, y, fwk, vs, ignore_index=m.ignore_index)
+    torch.cuda.synchronize()
+    assert torch.allclose(rl1, rl2, rtol=0, atol=1e-5)
+    assert abs(float(l1) - float(l2)) <= 1e-6 * abs(float(l2))
+    # an element of dZ may round to the neighbouring bf16 value: 2^-8 of a
+    # term, so a few bf16 steps of the largest result at most
+    assert torch.allclose(dx1.float(), dx2.float(), rtol=2 ** -7, atol=2 ** -7 * float(dx2.float().abs().max()))
+    for a, b in zip(dw1, dw2):
+        assert torch.allclose(a, b, rtol=2 ** -7, atol=2 ** -7 * float(b.abs().max()))

@@ -35,7 +35,15 @@ cudaError_t launch_embed_backward(const void* grad, int grad_bf16, long long ld_
 int gemm_max_shards();
 bool launch_gemm_stats(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
                        long long h, const long long* vocab_start, const long long* targets, long long ignore_index,
-                       float2* part, float* tgt, Header* hdr, int sms, int* groups, cudaStream_t st);
+                       float2* part, float* tgt, Header* hdr, int sms, int* groups, cudaStream_t st,
+                       float* zf = nullptr, long long ldzf = 0, const long long* zcol = nullptr);
+size_t lmhead_train_workspace_bytes(long long s, long long V, long long h);
+size_t lmhead_train_min_workspace_bytes(long long s, long long V, long long h);
+vpce_status lmhead_train_run(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
+                             long long h, const long long* vs, const long long* targets, long long ignore_index,
+                             int reduction, float grad, const float* grad_rows, float* loss_out, float* row_loss_out,
+                             void* dx, long long ld_dx, float* const* dw, long long ld_dw, void* ws, size_t ws_bytes,
+                             int sms, cudaStream_t st);
 
 }  // namespace vpce
 
@@ -602,6 +610,60 @@ vpce_status vpce_lmhead_backward(const void* hidden, int64_t ld_hidden, const vo
                              reinterpret_cast<Header*>(const_cast<unsigned char*>(fws)), grad_hidden, ldgx,
                              grad_weight_shards, ldgw, workspace, workspace_bytes, g_sms,
                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t vpce_lmhead_forward_backward_workspace_bytes(int64_t s, int64_t V, int64_t h) {
+  if (s < 0 || s >= (int64_t(1) << 31) || V < 1 || h < 1) return 0;
+  return lmhead_train_workspace_bytes(s, V, h);
+}
+
+vpce_status vpce_lmhead_forward_backward(const void* hidden, int64_t ld_hidden, const void* const* weight_shards,
+                                         int64_t ld_weight, int t, int64_t s, int64_t h, const int64_t* vocab_start,
+                                         const int64_t* targets, int64_t ignore_index, vpce_reduction reduction,
+                                         float grad_output, const float* grad_rows, float* loss_out,
+                                         float* row_loss_out, void* grad_hidden, int64_t ld_grad_hidden,
+                                         float* const* grad_weight_shards, int64_t ld_grad_weight, void* workspace,
+                                         size_t workspace_bytes, vpce_stream_t stream) {
+  if (t < 1 || t > gemm_max_shards() || s < 0 || s >= (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  if (h < 64 || h % 64 != 0 || h >= (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  if (weight_shards == nullptr || grad_weight_shards == nullptr || vocab_start == nullptr || vocab_start[0] != 0)
+    return VPCE_ERR_INVALID_ARG;
+  for (int i = 0; i < t; ++i)
+    if (vocab_start[i + 1] <= vocab_start[i]) return VPCE_ERR_INVALID_ARG;
+  if (vocab_start[t] >= (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  if (!std::isfinite(grad_output)) return VPCE_ERR_INVALID_ARG;
+  if (reduction == VPCE_NONE && s > 0 && grad_rows == nullptr) return VPCE_ERR_INVALID_ARG;
+  const int64_t ldx = ld_hidden == 0 ? h : ld_hidden;
+  const int64_t ldw = ld_weight == 0 ? h : ld_weight;
+  const int64_t ldgx = ld_grad_hidden == 0 ? h : ld_grad_hidden;
+  const int64_t ldgw = ld_grad_weight == 0 ? h : ld_grad_weight;
+  if (ldx < h || ldw < h || ldgx < h || ldgw < h) return VPCE_ERR_INVALID_ARG;
+  if (s > 0) {
+    if (hidden == nullptr || targets == nullptr || grad_hidden == nullptr) return VPCE_ERR_INVALID_ARG;
+    for (int i = 0; i < t; ++i)
+      if (weight_shards[i] == nullptr || grad_weight_shards[i] == nullptr) return VPCE_ERR_INVALID_ARG;
+  }
+  if ((hidden != nullptr && !aligned(hidden, 16)) || (ldx * 2) % 16 != 0 || (ldw * 2) % 16 != 0)
+    return VPCE_ERR_ALIGNMENT;
+  for (int i = 0; i < t; ++i) {
+    if (weight_shards[i] != nullptr && !aligned(weight_shards[i], 16)) return VPCE_ERR_ALIGNMENT;
+    if (grad_weight_shards[i] != nullptr && !aligned(grad_weight_shards[i], 16)) return VPCE_ERR_ALIGNMENT;
+  }
+  if ((grad_hidden != nullptr && !aligned(grad_hidden, 2)) || (targets != nullptr && !aligned(targets, 8)) ||
+      (grad_rows != nullptr && !aligned(grad_rows, 4)))
+    return VPCE_ERR_ALIGNMENT;
+  vpce_status st = check_outputs(reduction, s, loss_out, row_loss_out);
+  if (st != VPCE_OK) return st;
+  if (workspace == nullptr) return VPCE_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return VPCE_ERR_ALIGNMENT;
+  if (workspace_bytes < lmhead_train_min_workspace_bytes(s, vocab_start[t], h)) return VPCE_ERR_WORKSPACE;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != VPCE_OK) return st;
+  const int g_sms = sms < VPCE_LMHEAD_MAX_GROUPS ? sms : VPCE_LMHEAD_MAX_GROUPS;
+  return lmhead_train_run(hidden, ldx, weight_shards, ldw, t, s, h, reinterpret_cast<const long long*>(vocab_start),
+                          reinterpret_cast<const long long*>(targets), ignore_index, int(reduction), grad_output,
+                          grad_rows, loss_out, row_loss_out, grad_hidden, ldgx, grad_weight_shards, ldgw, workspace,
+                          workspace_bytes, g_sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // Shard geometry of a [w_i, h] table split by vocabulary (row stride ld

@@ -81,10 +81,22 @@ struct GemmParams {
   float grad;                       // upstream gradient g of the reduced loss (grad_rows null)
   unsigned short* dz;               // [s, ldz] bf16 dlogits, global column c at dz + c
   long long ldz;
+  // logits-keeping epilogue only: shard i's fp32 logits [s, w_i], box 32 x 32
+  CUtensorMap tmz[kMaxGemmShards];
 };
 
 constexpr int kEpiStats = 0;  // loss statistics of the tile
 constexpr int kEpiGrad = 1;   // dlogits of the tile, from the forward's logsumexp
+constexpr int kEpiStatsZ = 2; // loss statistics of the tile, and the tile's fp32 logits kept
+
+// The logits-keeping epilogue stages each warp's 32 rows x 32 columns of fp32
+// (4 KB, 128-byte swizzle) in shared memory past GemmSmem, two buffers per
+// warp, and stores them with TMA: a thread's row is 128 contiguous bytes, so
+// plain stores from registers would touch 32 lines per warp instruction.
+constexpr int kZStageOff = int((sizeof(GemmSmem) + 1023) / 1024 * 1024);
+constexpr int kZWarpBytes = 2 * 4096;
+constexpr int kZSmem = kZStageOff + 4 * kZWarpBytes;
+static_assert(kZSmem <= 232448, "logits staging fits the shared memory of a CTA");
 
 // ---------------------------------------------------------------------------
 // inline PTX: TMA tiles, tcgen05
@@ -95,6 +107,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
           "r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
+}
+
+// shared -> global tile store (bulk group of the issuing thread)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(smem_addr(src))
+               : "memory");
 }
 
 // Shared-memory matrix descriptor of a K-major tile stored as 128-byte rows
@@ -314,6 +334,8 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
     const uint32_t lane_addr = tmem + (uint32_t(q * 32) << 16);
     unsigned tiles = 0;
     bool ok = true;
+    unsigned zc = 0;  // chunks this warp has staged (logits-keeping epilogue)
+    unsigned char* zbuf = smem_raw + kZStageOff + q * kZWarpBytes;
     for (int wv = 0; wv < waves && ok; ++wv) {
       const int mt = wv * p.gm + m_slot;
       if (mt >= p.m_tiles) break;
@@ -385,6 +407,26 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
           tmem_ld32(lane_addr + uint32_t(b * kBN + c * 32), v);
           const int lim = valid - c * 32;
           const long long rel = tc - c * 32;
+          if constexpr (EPI == kEpiStatsZ) {
+            // this warp's 32 rows x 32 columns through shared memory to the
+            // shard's kept logits; TMA clips columns past the shard and rows
+            // past the chunk
+            unsigned char* zb = zbuf + (zc & 1u) * 4096u;
+            if (lane == 0 && zc >= 2) bulk_wait_read<1>();  // the store of chunk zc - 2 has read zb
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<float4*>(zb + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                  make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int zy = mt * kBM + q * 32;
+            if (lane == 0 && zy < p.s) {
+              tma_store_2d(&p.tmz[sh], zb, col0 + c * 32, zy);
+              bulk_commit();
+            }
+            ++zc;
+          }
           if (rel >= 0 && rel < 32 && rel < lim) {
             // the target logit: a sum of products with 0/1 weights picks it
             // without a run-time index into the registers (exact: one term
@@ -421,7 +463,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
         ++tiles;
       }
       if (!ok) break;
-      if (EPI == kEpiStats && live) {
+      if (EPI != kEpiGrad && live) {
         p.part[(long long)grp * p.s + r] = make_float2(m, se);
         if (has_t) p.tgt[r] = zt;
       }
@@ -430,6 +472,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
       sm.abort_flag = 1;
       atomicOr(&p.hdr->error_flag, VPCE_FLAG_WAIT_TIMEOUT);
     }
+    if (EPI == kEpiStatsZ && lane == 0) bulk_wait_all<0>();  // the staged logits have left shared memory
   }
 
   tc_fence_before();
@@ -461,6 +504,18 @@ EncodeTiledFn encode_fn() {
 
 // A [rows, h] bf16 row-major matrix (row stride ld elements) as a 2-D tensor
 // map with a box of 64 columns x box_rows rows and the 128-byte swizzle.
+bool make_map_f32(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(ld) * 4u};
+  const cuuint32_t box[2] = {32u, 32u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* m, const void* base, long long rows, long long h, long long ld, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
@@ -482,6 +537,9 @@ cudaError_t set_gemm_smem() {
   const cudaError_t e = cudaFuncSetAttribute(gemm_stats_kernel<kEpiStats>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(GemmSmem)));
   if (e != cudaSuccess) return e;
+  const cudaError_t e2 = cudaFuncSetAttribute(gemm_stats_kernel<kEpiStatsZ>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kZSmem);
+  if (e2 != cudaSuccess) return e2;
   return cudaFuncSetAttribute(gemm_stats_kernel<kEpiGrad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(sizeof(GemmSmem)));
 }
@@ -509,7 +567,8 @@ int gemm_n_tiles(const long long* vocab_start, int t) {
 // tensor map cannot be encoded (the launch status is the caller's to read).
 bool launch_gemm_stats(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
                        long long h, const long long* vocab_start, const long long* targets, long long ignore_index,
-                       float2* part, float* tgt, Header* hdr, int sms, int* groups, cudaStream_t st) {
+                       float2* part, float* tgt, Header* hdr, int sms, int* groups, cudaStream_t st, float* zf,
+                       long long ldzf, const long long* zcol) {
   static_assert(sizeof(GemmParams) < 32000, "kernel parameter block");
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -534,7 +593,15 @@ bool launch_gemm_stats(const void* x, long long ld_x, const void* const* w, long
   p.tgt = tgt;
   p.hdr = hdr;
   *groups = p.gn;
-  gemm_stats_kernel<kEpiStats><<<p.gm * p.gn, kGThreads, sizeof(GemmSmem), st>>>(p);
+  if (zf != nullptr) {
+    // shard i's logits at columns [zcol[i], zcol[i] + w_i) of rows of ldzf
+    // floats (zcol[i] a multiple of 4, ldzf a multiple of 4)
+    for (int i = 0; i < t; ++i)
+      if (!make_map_f32(&p.tmz[i], zf + zcol[i], s, vocab_start[i + 1] - vocab_start[i], ldzf)) return false;
+    gemm_stats_kernel<kEpiStatsZ><<<p.gm * p.gn, kGThreads, kZSmem, st>>>(p);
+  }
+  else
+    gemm_stats_kernel<kEpiStats><<<p.gm * p.gn, kGThreads, sizeof(GemmSmem), st>>>(p);
   return true;
 }
 

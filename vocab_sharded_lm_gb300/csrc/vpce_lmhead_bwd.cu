@@ -22,6 +22,12 @@ bool launch_gemm_grad(const void* x, long long ld_x, const void* const* w, long 
                       long long h, const long long* vocab_start, const long long* targets, long long ignore_index,
                       const float* lse, const float* grad_rows, float grad, unsigned short* dz, long long ldz,
                       Header* hdr, int sms, cudaStream_t st);
+bool launch_gemm_stats(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
+                       long long h, const long long* vocab_start, const long long* targets, long long ignore_index,
+                       float2* part, float* tgt, Header* hdr, int sms, int* groups, cudaStream_t st, float* zf,
+                       long long ldzf, const long long* zcol);
+void launch_prep(const long long* targets, long long s, long long V, long long ignore_index, Header* hdr,
+                 int reduction, float* loss_out, cudaStream_t st);
 
 namespace {
 
@@ -73,6 +79,36 @@ long long lmhead_bwd_rows_for(size_t bytes, long long V, long long h) {
   return r;
 }
 
+// The two plain GEMMs of one row chunk of R rows, given its bf16 dZ (shard
+// i's columns from dz + zcol[i], rows of ldz elements):
+//     dX[chunk]  = sum_i dZ_i W_i          (fp32 in dx32, then rounded to bf16)
+//     dW_i      += dZ_i^T X[chunk]         (fp32, accumulated)
+vpce_status chunk_gemms(cublasHandle_t hb, const void* xr, long long ld_x, const void* const* w, long long ld_w, int t,
+                        long long R, long long h, const long long* vs, const unsigned short* dz, const long long* zcol,
+                        long long ldz,
+                        float* dx32, __nv_bfloat16* dxr, long long ld_dx, float* const* dw, long long ld_dw, int sms,
+                        cudaStream_t st) {
+  const float one = 1.f, zero = 0.f;
+  for (int i = 0; i < t; ++i) {
+    const int wi = int(vs[i + 1] - vs[i]);
+    // column-major: dX^T [h, R] (+)= W_i^T [h, w_i] * dZ_i^T [w_i, R]
+    if (cublasGemmEx(hb, CUBLAS_OP_N, CUBLAS_OP_N, int(h), int(R), wi, &one, w[i], CUDA_R_16BF, int(ld_w),
+                     dz + zcol[i], CUDA_R_16BF, int(ldz), i == 0 ? &zero : &one, dx32, CUDA_R_32F, int(h),
+                     CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+      return VPCE_ERR_CUDA;
+    // column-major: dW_i^T [h, w_i] += X^T [h, R] * dZ_i [R, w_i]
+    if (cublasGemmEx(hb, CUBLAS_OP_N, CUBLAS_OP_T, int(h), wi, int(R), &one, xr, CUDA_R_16BF, int(ld_x),
+                     dz + zcol[i], CUDA_R_16BF, int(ldz), &one, dw[i], CUDA_R_32F, int(ld_dw), CUBLAS_COMPUTE_32F,
+                     CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+      return VPCE_ERR_CUDA;
+  }
+  const long long n = R * h;
+  long long blocks = (n + 255) / 256;
+  if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
+  f32_to_bf16_rows<<<int(blocks), 256, 0, st>>>(dx32, h, dxr, ld_dx, R, h);
+  return cudaGetLastError() == cudaSuccess ? VPCE_OK : VPCE_ERR_CUDA;
+}
+
 // Returns VPCE_OK, VPCE_ERR_CUDA (a launch or a cuBLAS call failed).
 vpce_status lmhead_backward_run(const void* x, long long ld_x, const void* const* w, long long ld_w, int t,
                                 long long s, long long h, const long long* vs, const long long* targets,
@@ -98,7 +134,6 @@ vpce_status lmhead_backward_run(const void* x, long long ld_x, const void* const
   if (hb == nullptr || cublasSetStream(hb, st) != CUBLAS_STATUS_SUCCESS ||
       cublasSetWorkspace(hb, blas_ws, kBlasBytes) != CUBLAS_STATUS_SUCCESS)
     return VPCE_ERR_CUDA;
-  const float one = 1.f, zero = 0.f;
   for (long long r0 = 0; r0 < s; r0 += rows) {
     const long long R = s - r0 < rows ? s - r0 : rows;
     const unsigned char* xr = static_cast<const unsigned char*>(x) + r0 * ld_x * 2;
@@ -106,27 +141,260 @@ vpce_status lmhead_backward_run(const void* x, long long ld_x, const void* const
                           grad_rows != nullptr ? grad_rows + r0 : nullptr, grad, dz, ldz, hdr, sms, st))
       return VPCE_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return VPCE_ERR_CUDA;
-    for (int i = 0; i < t; ++i) {
-      const int wi = int(vs[i + 1] - vs[i]);
-      // column-major: dX^T [h, R] (+)= W_i^T [h, w_i] * dZ_i^T [w_i, R]
-      if (cublasGemmEx(hb, CUBLAS_OP_N, CUBLAS_OP_N, int(h), int(R), wi, &one, w[i], CUDA_R_16BF, int(ld_w),
-                       dz + vs[i], CUDA_R_16BF, int(ldz), i == 0 ? &zero : &one, dx32, CUDA_R_32F, int(h),
-                       CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-        return VPCE_ERR_CUDA;
-      // column-major: dW_i^T [h, w_i] += X^T [h, R] * dZ_i [R, w_i]
-      if (cublasGemmEx(hb, CUBLAS_OP_N, CUBLAS_OP_T, int(h), wi, int(R), &one, xr, CUDA_R_16BF, int(ld_x),
-                       dz + vs[i], CUDA_R_16BF, int(ldz), &one, dw[i], CUDA_R_32F, int(ld_dw), CUBLAS_COMPUTE_32F,
-                       CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-        return VPCE_ERR_CUDA;
-    }
-    const long long n = R * h;
-    long long blocks = (n + 255) / 256;
-    if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
-    f32_to_bf16_rows<<<int(blocks), 256, 0, st>>>(dx32, h,
-                                                   static_cast<__nv_bfloat16*>(dx) + r0 * ld_dx, ld_dx, R, h);
-    if (cudaGetLastError() != cudaSuccess) return VPCE_ERR_CUDA;
+    const vpce_status e = chunk_gemms(hb, xr, ld_x, w, ld_w, t, R, h, vs, dz, vs, ldz, dx32,
+                                      static_cast<__nv_bfloat16*>(dx) + r0 * ld_dx, ld_dx, dw, ld_dw, sms, st);
+    if (e != VPCE_OK) return e;
   }
   return VPCE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Forward and backward in one call (vpce_lmhead_forward_backward): per row
+// chunk the tensor-core kernel writes the loss statistics and keeps the
+// chunk's fp32 logits; one kernel then finishes each row (logsumexp, loss,
+// bf16 dZ from the kept logits) and the two plain GEMMs follow.  No logits
+// are formed twice.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kRowThreads = 256;
+constexpr int kLossThreads = 1024;
+
+struct TrainRowParams {
+  const float2* part;  // [groups][R] (max, sum exp) of the chunk's column groups
+  int groups;
+  long long R, V;
+  int t;
+  long long vs[VPCE_MAX_SHARDS + 1];    // shard i holds vocabulary [vs[i], vs[i + 1])
+  long long zcol[VPCE_MAX_SHARDS + 1];  // and sits at columns [zcol[i], zcol[i] + w_i) of a padded row
+  const float* tgt;    // [R] target logits
+  const float* zf;     // [R, ld] fp32 logits, padded per shard
+  unsigned short* dz;  // [R, ld] bf16 dlogits, the same layout
+  long long ld;        // a multiple of 8
+  const long long* targets;
+  long long ignore_index;
+  const float* grad_rows;  // per-row upstream gradient, or null
+  float grad;
+  const Header* hdr;       // the batch's n_valid and reduction
+  float* lse;
+  float* rowl;
+  float* row_loss;         // the caller's per-row losses, or null
+};
+
+// One row per CTA: the logsumexp of the column groups' partials, folded as
+// the combine folds them; the row loss; then dZ = (softmax - onehot) g over
+// the row's kept logits, each element as the gradient epilogue forms it.
+__global__ void __launch_bounds__(kRowThreads) train_rows_kernel(const __grid_constant__ TrainRowParams p) {
+  __shared__ float s_lse;
+  const long long rr = blockIdx.x;
+  const long long y = p.targets[rr];
+  if (threadIdx.x == 0) {
+    float rl = 0.f, lse = 0.f;
+    if (y == p.ignore_index) {
+      rl = 0.f;
+    } else if (y < 0 || y >= p.V) {
+      rl = lse = __int_as_float(0x7fc00000);
+    } else {
+      float M = -INFINITY;
+      for (int i = 0; i < p.groups; ++i) M = fmaxf(M, p.part[(long long)i * p.R + rr].x);
+      float S = 0.f;
+      for (int i = 0; i < p.groups; ++i) {
+        const float2 q = p.part[(long long)i * p.R + rr];
+        S += q.y * expf(q.x - M);
+      }
+      lse = M + logf(S);
+      rl = lse - p.tgt[rr];
+    }
+    p.lse[rr] = lse;
+    p.rowl[rr] = rl;
+    if (p.row_loss != nullptr) p.row_loss[rr] = rl;
+    s_lse = lse;
+  }
+  __syncthreads();
+  float cb = 0.f, scl = 0.f;  // 0 for ignored rows
+  if (y != p.ignore_index) {
+    const int nv = p.hdr->n_valid;
+    const float sc_all = p.hdr->reduction != VPCE_MEAN ? p.grad : (nv > 0 ? p.grad / float(nv) : 0.f);
+    cb = -s_lse * kLog2e;
+    scl = p.grad_rows != nullptr ? __ldg(p.grad_rows + rr) : sc_all;
+  }
+  // the target's column in the padded row (-1: none)
+  long long ty = -1;
+  if (y >= 0 && y < p.V) {
+    int i = 0;
+    while (p.vs[i + 1] <= y) ++i;
+    ty = p.zcol[i] + (y - p.vs[i]);
+  }
+  const float* z = p.zf + rr * p.ld;
+  unsigned short* d = p.dz + rr * p.ld;
+  auto dlogit = [&](float v, long long c) {
+    float g = ex2(fmaf(v, kLog2e, cb)) * scl;
+    if (c == ty) g -= scl;
+    return scl == 0.f ? 0.f : g;
+  };
+  // the whole padded row: the padding columns were never written and their
+  // results are never read
+  const long long n4 = p.ld / 4;
+  for (long long q = threadIdx.x; q < n4; q += kRowThreads) {
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(z) + q);
+    const long long c = 4 * q;
+    reinterpret_cast<uint2*>(d)[q] =
+        make_uint2(pack_bf16x2(dlogit(v.x, c), dlogit(v.y, c + 1)), pack_bf16x2(dlogit(v.z, c + 2), dlogit(v.w, c + 3)));
+  }
+}
+
+// The batch loss from the per-row losses: fixed 256-row blocks, summed in a
+// fixed order in fp64.
+__global__ void __launch_bounds__(kLossThreads) train_loss_kernel(const float* rowl, long long s, Header* hdr,
+                                                                  float* loss_out) {
+  __shared__ double sv[kLossThreads / 32];
+  double v = 0.0;
+  const long long nb = (s + 255) / 256;
+  for (long long b = threadIdx.x; b < nb; b += kLossThreads) {
+    double bs = 0.0;
+    const long long e = min(s, (b + 1) * 256);
+    for (long long r = b * 256; r < e; ++r) bs += double(rowl[r]);
+    v += bs;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(kFull, v, o);
+  if ((threadIdx.x & 31) == 0) sv[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int i = 0; i < kLossThreads / 32; ++i) tot += sv[i];
+    const int cnt = hdr->n_valid;
+    hdr->loss_sum = tot;
+    if (loss_out != nullptr)
+      *loss_out = hdr->reduction != VPCE_MEAN ? float(tot)
+                                              : (cnt > 0 ? float(tot / double(cnt)) : __int_as_float(0x7fc00000));
+  }
+}
+
+constexpr long long kTrainRows = 4096;  // rows per chunk with the suggested workspace
+constexpr long long kMinTrainRows = 128;
+
+// The padded row of kept logits and dZ: each shard's columns start at a
+// multiple of 8, so a row is at most round8(V) + 8 * 32 columns.
+long long train_ld_bound(long long V) { return (V + 7) / 8 * 8 + 8LL * VPCE_MAX_SHARDS; }
+
+struct TrainLayout {
+  size_t lse, rowl, part, tgt, zf, dz, dx32, blas, total;
+  TrainLayout(long long R, long long s, long long V, long long h) {
+    size_t o = 256;  // header
+    lse = o;
+    o += round256(size_t(s) * 4u);
+    rowl = o;
+    o += round256(size_t(s) * 4u);
+    part = o;
+    o += round256(size_t(VPCE_LMHEAD_MAX_GROUPS) * size_t(R) * 8u);
+    tgt = o;
+    o += round256(size_t(R) * 4u);
+    zf = o;
+    o += round256(size_t(R) * size_t(train_ld_bound(V)) * 4u);
+    dz = o;
+    o += round256(size_t(R) * size_t(train_ld_bound(V)) * 2u);
+    dx32 = o;
+    o += round256(size_t(R) * size_t(h) * 4u);
+    blas = o;
+    total = o + kBlasBytes;
+  }
+};
+
+// the chunk rows a workspace of `bytes` holds (0 when fewer than kMinTrainRows)
+long long train_rows_for(size_t bytes, long long s, long long V, long long h) {
+  long long r = (s + kMinTrainRows - 1) / kMinTrainRows * kMinTrainRows;
+  if (r > kTrainRows) r = kTrainRows;
+  if (r < kMinTrainRows) r = kMinTrainRows;
+  while (r > kMinTrainRows && TrainLayout(r, s, V, h).total > bytes) r -= kMinTrainRows;
+  return TrainLayout(r, s, V, h).total <= bytes ? r : 0;
+}
+
+}  // namespace
+
+size_t lmhead_train_workspace_bytes(long long s, long long V, long long h) {
+  long long r = (s + kMinTrainRows - 1) / kMinTrainRows * kMinTrainRows;
+  if (r > kTrainRows) r = kTrainRows;
+  if (r < kMinTrainRows) r = kMinTrainRows;
+  return TrainLayout(r, s, V, h).total;
+}
+
+size_t lmhead_train_min_workspace_bytes(long long s, long long V, long long h) {
+  return TrainLayout(kMinTrainRows, s, V, h).total;
+}
+
+// Returns VPCE_OK, VPCE_ERR_WORKSPACE, VPCE_ERR_CUDA (a launch or a cuBLAS call failed).
+vpce_status lmhead_train_run(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
+                             long long h, const long long* vs, const long long* targets, long long ignore_index,
+                             int reduction, float grad, const float* grad_rows, float* loss_out, float* row_loss_out,
+                             void* dx, long long ld_dx, float* const* dw, long long ld_dw, void* ws, size_t ws_bytes,
+                             int sms, cudaStream_t st) {
+  const long long V = vs[t];
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  Header* hdr = reinterpret_cast<Header*>(base);
+  // the batch's n_valid and reduction in the header, bad targets flagged
+  launch_prep(targets, s, V, ignore_index, hdr, reduction, loss_out, st);
+  if (cudaGetLastError() != cudaSuccess) return VPCE_ERR_CUDA;
+  if (s == 0) return VPCE_OK;
+  const long long rows = train_rows_for(ws_bytes, s, V, h);
+  if (rows == 0) return VPCE_ERR_WORKSPACE;
+  const TrainLayout L(rows, s, V, h);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return VPCE_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_blas_mu);
+  cublasHandle_t hb = blas_handle(dev);
+  if (hb == nullptr || cublasSetStream(hb, st) != CUBLAS_STATUS_SUCCESS ||
+      cublasSetWorkspace(hb, base + L.blas, kBlasBytes) != CUBLAS_STATUS_SUCCESS)
+    return VPCE_ERR_CUDA;
+  float* lse = reinterpret_cast<float*>(base + L.lse);
+  float* rowl = reinterpret_cast<float*>(base + L.rowl);
+  float* zf = reinterpret_cast<float*>(base + L.zf);
+  unsigned short* dz = reinterpret_cast<unsigned short*>(base + L.dz);
+  long long zcol[VPCE_MAX_SHARDS + 1];  // each shard's first column in a padded row
+  zcol[0] = 0;
+  for (int i = 0; i < t; ++i) zcol[i + 1] = zcol[i] + (vs[i + 1] - vs[i] + 7) / 8 * 8;
+  const long long ld = zcol[t];
+  for (long long r0 = 0; r0 < s; r0 += rows) {
+    const long long R = s - r0 < rows ? s - r0 : rows;
+    const unsigned char* xr = static_cast<const unsigned char*>(x) + r0 * ld_x * 2;
+    int groups = 1;
+    if (!launch_gemm_stats(xr, ld_x, w, ld_w, t, R, h, vs, targets + r0, ignore_index,
+                           reinterpret_cast<float2*>(base + L.part), reinterpret_cast<float*>(base + L.tgt), hdr, sms,
+                           &groups, st, zf, ld, zcol))
+      return VPCE_ERR_CUDA;
+    TrainRowParams q;
+    q.part = reinterpret_cast<const float2*>(base + L.part);
+    q.groups = groups;
+    q.R = R;
+    q.V = V;
+    q.t = t;
+    for (int i = 0; i <= t; ++i) {
+      q.vs[i] = vs[i];
+      q.zcol[i] = zcol[i];
+    }
+    q.tgt = reinterpret_cast<const float*>(base + L.tgt);
+    q.zf = zf;
+    q.dz = dz;
+    q.ld = ld;
+    q.targets = targets + r0;
+    q.ignore_index = ignore_index;
+    q.grad_rows = grad_rows != nullptr ? grad_rows + r0 : nullptr;
+    q.grad = grad;
+    q.hdr = hdr;
+    q.lse = lse + r0;
+    q.rowl = rowl + r0;
+    q.row_loss = row_loss_out != nullptr ? row_loss_out + r0 : nullptr;
+    train_rows_kernel<<<int(R), kRowThreads, 0, st>>>(q);
+    if (cudaGetLastError() != cudaSuccess) return VPCE_ERR_CUDA;
+    const vpce_status e = chunk_gemms(hb, xr, ld_x, w, ld_w, t, R, h, vs, dz, zcol, ld, reinterpret_cast<float*>(base + L.dx32),
+                                      static_cast<__nv_bfloat16*>(dx) + r0 * ld_dx, ld_dx, dw, ld_dw, sms, st);
+    if (e != VPCE_OK) return e;
+  }
+  train_loss_kernel<<<1, kLossThreads, 0, st>>>(rowl, s, hdr, loss_out);
+  return cudaGetLastError() == cudaSuccess ? VPCE_OK : VPCE_ERR_CUDA;
 }
 
 }  // namespace vpce

@@ -91,6 +91,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.vpce_lmhead_backward.argtypes = [_P, _I64, _P, _I64, ctypes.c_int, _I64, _I64, _I64P, _P, _I64,
                                              ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _I64, _P, _I64, _P,
                                              ctypes.c_size_t, _P]
+        lib.vpce_lmhead_forward_backward_workspace_bytes.restype = ctypes.c_size_t
+        lib.vpce_lmhead_forward_backward_workspace_bytes.argtypes = [_I64, _I64, _I64]
+        lib.vpce_lmhead_forward_backward.restype = ctypes.c_int
+        lib.vpce_lmhead_forward_backward.argtypes = [_P, _I64, _P, _I64, ctypes.c_int, _I64, _I64, _I64P, _P, _I64,
+                                                     ctypes.c_int, ctypes.c_float, _P, _P, _P, _P, _I64, _P, _I64,
+                                                     _P, ctypes.c_size_t, _P]
         lib.vpce_embedding_forward.restype = ctypes.c_int
         lib.vpce_embedding_forward.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64P, _I64, _I64, _P, _I64, _P,
                                                _I64, _P, _P]
@@ -523,6 +529,66 @@ def _table_desc(shards, vocab_start):
             vocab_start.append(vocab_start[-1] + e.shape[0])
     code = {torch.bfloat16: VPCE_BF16, torch.float32: VPCE_FP32}.get(dt)
     return code, h, ld, [int(v) for v in vocab_start]
+
+
+def vpce_lmhead_forward_backward_workspace_bytes(s: int, V: int, h: int) -> int:
+    return int(load_library().vpce_lmhead_forward_backward_workspace_bytes(int(s), int(V), int(h)))
+
+
+def vpce_lmhead_forward_backward(hidden, weight_shards, targets, vocab_start=None, *, ignore_index: int = -100,
+                                 reduction: str = "mean", grad_output: float = 1.0, grad_rows=None, loss_out=None,
+                                 row_loss_out=None, grad_hidden=None, grad_weight_shards=None, workspace=None,
+                                 stream=None):
+    """:func:`vpce_lmhead_forward` and :func:`vpce_lmhead_backward` in one
+    call (the upstream gradient known up front): each row chunk's logits are
+    formed once and kept in the workspace for its gradient.  Returns
+    ``(loss, grad_hidden, grad_weight_shards)`` (the per-row vector as the
+    loss for 'none'); dX is overwritten, dW accumulated."""
+    import torch
+
+    if hidden.dtype != torch.bfloat16 or hidden.dim() != 2 or not hidden.is_cuda or hidden.stride(1) != 1:
+        raise ValueError("hidden must be a CUDA bf16 [s, h] tensor with contiguous columns")
+    s, h = hidden.shape
+    if not weight_shards:
+        raise ValueError("need at least one weight shard")
+    for w in weight_shards:
+        if w.dtype != torch.bfloat16 or w.dim() != 2 or not w.is_cuda or w.shape[1] != h or w.stride(1) != 1:
+            raise ValueError("weight shards must be CUDA bf16 [w_i, h] tensors with contiguous columns")
+    strides = {w.stride(0) for w in weight_shards if w.shape[0] > 1}
+    if len(strides) > 1:
+        raise ValueError("weight shards must share one row stride")
+    ld_w = strides.pop() if strides else h
+    ld_x = hidden.stride(0) if s > 1 else h
+    if vocab_start is None:
+        vocab_start = [0]
+        for w in weight_shards:
+            vocab_start.append(vocab_start[-1] + w.shape[0])
+    vocab_start = [int(v) for v in vocab_start]
+    if targets.dtype != torch.int64 or not targets.is_cuda or targets.numel() != s:
+        raise ValueError("targets must be a CUDA int64 tensor with one entry per row")
+    dev = hidden.device
+    if grad_hidden is None:
+        grad_hidden = torch.empty((s, h), dtype=torch.bfloat16, device=dev)
+    if grad_weight_shards is None:
+        grad_weight_shards = [torch.zeros((w.shape[0], h), dtype=torch.float32, device=dev) for w in weight_shards]
+    gstr = {g.stride(0) for g in grad_weight_shards if g.shape[0] > 1}
+    ld_gw = gstr.pop() if len(gstr) == 1 else h
+    if grad_rows is not None:
+        _check_grad_rows(grad_rows, s)
+    if workspace is None:
+        workspace = torch.empty(vpce_lmhead_forward_backward_workspace_bytes(s, vocab_start[-1], h),
+                                dtype=torch.uint8, device=dev)
+    red, loss_out, row_loss_out, result = _outputs(reduction, loss_out, row_loss_out, s, dev)
+    code = int(load_library().vpce_lmhead_forward_backward(
+        ctypes.c_void_p(hidden.data_ptr()), int(ld_x), ctypes.cast(_ptr_array([w.data_ptr() for w in weight_shards]), _P),
+        int(ld_w), len(weight_shards), int(s), int(h), _i64_array(vocab_start), ctypes.c_void_p(targets.data_ptr()),
+        int(ignore_index), red, float(grad_output), _ptr(grad_rows), _ptr(loss_out), _ptr(row_loss_out),
+        ctypes.c_void_p(grad_hidden.data_ptr()), int(grad_hidden.stride(0) if s > 1 else h),
+        ctypes.cast(_ptr_array([g.data_ptr() for g in grad_weight_shards]), _P), int(ld_gw),
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream)))
+    if code != VPCE_OK:
+        raise VPCEError(code, "vpce_lmhead_forward_backward")
+    return result, grad_hidden, grad_weight_shards
 
 
 def vpce_embedding_forward(table_shards, ids, vocab_start=None, *, out=None, flag=None, stream=None):
