@@ -554,6 +554,8 @@ def run_lmhead(args):
     m = synth.LMHEADS[synth.LMHEAD_BENCH]
     if args.rows:
         m = m.replace(s=args.rows)
+    if args.vocab:  # a smaller head of the same hidden size (profiling captures that hold a few GB)
+        m = m.replace(V=args.vocab, t=args.shards or m.t)
     vs = synth.even_vocab_start(m.V, m.t)
     meta = synth.lmhead_meta(m)
     x, ws = synth.lmhead_device(m, vs, device=dev)
@@ -921,6 +923,9 @@ def main():
                     help="fused: vpce_forward_backward; split: vpce_forward then vpce_backward; "
                          "lmhead: the LM-head GEMM fused with the forward loss; embedding: the vocabulary-parallel "
                          "input embedding (each its own metric)")
+    ap.add_argument("--vocab", type=int, default=0,
+                    help="LM-head paths: vocabulary size of a smaller head (profiling captures)")
+    ap.add_argument("--shards", type=int, default=0, help="LM-head paths with --vocab: vocabulary shards")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the workload's row count (small profiling captures only)")
     args = ap.parse_args()
