@@ -108,5 +108,33 @@ def test_fused_plan(name):
     vs = synth.even_vocab_start(w.V, w.t)
     plan = vpce.vpce_fused_plan(vpce.VPCE_BF16 if w.dtype == "bf16" else vpce.VPCE_FP32, vs, w.s)
     assert plan["kernel"] == "stream" and 0 < plan["grid"] <= w.s
+    # rows over 320 KB are shared by a pair of CTAs (a cluster of 2)
+    row_bytes = w.V * (2 if w.dtype == "bf16" else 4)
+    assert plan["cluster"] == (2 if row_bytes > 320 * 1024 else 1)
+    assert plan["grid"] % plan["cluster"] == 0
     odd = [0, 3, 10]  # a 3-column bf16 shard is not a 16-byte multiple
     assert vpce.vpce_fused_plan(vpce.VPCE_BF16, odd, 4)["kernel"] == "split"
+
+
+def test_fused_paired_rows_match_split_and_are_deterministic():
+    # 512 KB rows: two CTAs of a cluster share each row
+    w = W["s32768_v256000"].replace(s=100)
+    assert vpce.vpce_fused_plan(vpce.VPCE_BF16, synth.even_vocab_start(w.V, w.t), w.s)["cluster"] == 2
+    a = run_full(w, path="fused")
+    b = run_full(w, path="fused")
+    c = run_full(w, path="split")
+    check_full(a)
+    assert a["loss"] == b["loss"]
+    for x, y in zip(a["back"], b["back"]):
+        np.testing.assert_array_equal(x, y)
+    assert abs(a["loss"] - c["loss"]) <= 1e-6 * abs(c["loss"])
+    np.testing.assert_allclose(a["row_loss"], c["row_loss"], rtol=2e-6)
+
+
+@pytest.mark.parametrize("vs", [[0, 200000], [0, 8, 180000, 180016, 200000], [0, 190000, 190008, 200000]])
+def test_fused_paired_rows_uneven_shards(vs):
+    # 400 KB bf16 rows: one shard split over 16 warps; uneven shards split at
+    # the boundary nearest half the row (the halves differ in size)
+    w = synth.Workload("paired", 15, 36, vs[-1], len(vs) - 1, "bf16", 2.0, "uniform", ignore_frac=0.1)
+    assert vpce.vpce_fused_plan(vpce.VPCE_BF16, vs, w.s)["cluster"] == 2
+    check_full(run_full(w, vocab_start=vs, path="fused"))

@@ -14,6 +14,8 @@ cudaError_t set_fused_smem();
 bool fused_supported(const ShardSet& sh, int t, int elem);
 void launch_prep(const long long* targets, long long s, long long V, long long ignore_index, Header* hdr,
                  int reduction, float* loss_out, cudaStream_t st);
+bool fused_pair(long long row_bytes);
+int fused_grid(long long s, int sms, bool pair);
 void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long long V, const long long* targets,
                          long long ignore_index, int reduction, float grad, const float* grad_rows, float* lse,
                          float* rowl, float* row_loss, float* loss_out, Header* hdr, int sms, cudaStream_t st);
@@ -374,9 +376,10 @@ vpce_status vpce_fused_plan(vpce_dtype dtype, int t, const int64_t* vocab_start,
   const vpce_status st = device_setup(&sms);
   if (st != VPCE_OK) return st;
   const int eb = dtype == VPCE_BF16 ? 2 : 4;
+  const bool pair = fused_pair(vocab_start[t] * eb);
   *kernel = 1;
-  *cluster = 1;
-  *grid = int(s < sms ? s : sms);
+  *cluster = pair ? 2 : 1;
+  *grid = fused_grid(s, sms, pair);
   for (int i = 0; i < t; ++i)
     if (((vocab_start[i + 1] - vocab_start[i]) * eb) & 15) {
       *kernel = 0;

@@ -212,6 +212,71 @@ __device__ __forceinline__ bool mbar_wait_thread(uint64_t* bar, uint32_t parity)
   }
   return true;
 }
+// ---------------------------------------------------------------------------
+// thread-block clusters: another CTA's shared memory and mbarriers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of `p` (this CTA's shared memory) in CTA `rank`
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, unsigned rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
+  return a;
+}
+
+// arrive on the mbarrier at `bar` in CTA `rank`, releasing this thread's
+// earlier writes at cluster scope
+__device__ __forceinline__ void mbar_arrive_cluster(const uint64_t* bar, unsigned rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr(bar, rank))
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Warp-uniform bounded wait for a phase completed by arrivals from any CTA
+// of the cluster (acquire at cluster scope); false once the limit passed.
+__device__ __forceinline__ bool mbar_wait_warp_cluster(uint64_t* bar, uint32_t parity) {
+  if (__all_sync(kFull, mbar_try_wait_cluster(bar, parity))) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (__all_sync(kFull, mbar_try_wait_cluster(bar, parity))) return true;
+    if (__any_sync(kFull, clock64() - t0 > kWaitLimitCycles)) return false;
+  }
+}
+
+__device__ __forceinline__ float2 ld_cluster_f2(const float2* p, unsigned rank) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(cluster_addr(p, rank))
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float ld_cluster_f(const float* p, unsigned rank) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr(p, rank)) : "memory");
+  return v;
+}
+
+// every thread of every CTA of the cluster (no time limit: callers reach it
+// only after their own bounded waits)
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }

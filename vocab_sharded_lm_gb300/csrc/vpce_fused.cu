@@ -34,6 +34,7 @@ namespace {
 
 constexpr int kPrepThreads = 1024;
 constexpr int kSW = 8;         // stats warps
+constexpr int kSWLog2 = 3;
 constexpr int kDW = 8;         // grad warps
 constexpr int kFThreads = (kSW + kDW) * 32;
 constexpr int kFChunk = 4096;  // bytes per pipeline chunk
@@ -48,6 +49,7 @@ constexpr unsigned kLiveBytesPerCta = 320u * 1024u;
 // stats warp w and grad warp w walk the same chunks: the credit between them
 // counts those chunks
 static_assert(kSW == kDW, "stats and grad warps pair up");
+static_assert((1 << kSWLog2) == kSW, "a row part's warp count is a power of two");
 constexpr int kFVPL = kFChunk / 512;
 
 struct FusedParams {
@@ -133,30 +135,67 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const long long* tar
   }
 }
 
-// Byte range [lo, hi) of a shard segment owned by warp w of NW (16-byte
-// boundaries; the last warp takes the remainder).
-template <int NW>
-__device__ __forceinline__ void sub_range(unsigned seg_bytes, int w, unsigned& lo, unsigned& hi) {
-  lo = unsigned((unsigned long long)seg_bytes * unsigned(w) / NW) & ~15u;
-  hi = w == NW - 1 ? seg_bytes : unsigned((unsigned long long)seg_bytes * unsigned(w + 1) / NW) & ~15u;
+// The part of every row one warp of a role owns: shard segments [sa, sb)
+// and, within each, the wi-th of nw = 2^nw_log2 byte ranges.  One CTA per
+// row: every segment, split over the kSW warps.  Two CTAs per row: with two
+// or more shards the CTAs take the segments on either side of the boundary
+// nearest half the row, each split over its kSW warps (the chunks stay as
+// long as with one CTA); with one shard the segment is split over 2 kSW
+// warps.
+struct RowPart {
+  int sa, sb;
+  int nw_log2, wi;
+};
+
+__device__ __forceinline__ RowPart row_part(const Geo& g, int t, bool pair, unsigned crank, int w) {
+  RowPart rp{0, t, kSWLog2, w};
+  if (!pair) return rp;
+  if (t == 1) {
+    rp.nw_log2 = kSWLog2 + 1;
+    rp.wi = int(crank) * kSW + w;
+    return rp;
+  }
+  int k = 1;
+  long long best = -1;
+  for (int i = 1; i < t; ++i) {
+    const long long d = 2LL * g.start[i] - g.start[t];
+    const long long ad = d < 0 ? -d : d;
+    if (best < 0 || ad < best) {
+      best = ad;
+      k = i;
+    }
+  }
+  if (crank == 0) rp.sb = k;
+  else rp.sa = k;
+  return rp;
 }
 
-// Walks the chunks of row r that belong to warp w of NW: segment by segment,
-// each sub-range cut into kFChunk-byte chunks and a shorter last one.  No
+// Byte range [lo, hi) of a shard segment owned by the part's warp (16-byte
+// boundaries; the last warp takes the remainder).  nw is a power of two, so
+// there is no division.
+__device__ __forceinline__ void sub_range(unsigned seg_bytes, const RowPart& rp, unsigned& lo, unsigned& hi) {
+  lo = unsigned(((unsigned long long)seg_bytes * unsigned(rp.wi)) >> rp.nw_log2) & ~15u;
+  hi = rp.wi == (1 << rp.nw_log2) - 1
+           ? seg_bytes
+           : unsigned(((unsigned long long)seg_bytes * unsigned(rp.wi + 1)) >> rp.nw_log2) & ~15u;
+}
+
+// Walks the chunks of row r in a warp's part: segment by segment, each
+// sub-range cut into kFChunk-byte chunks and a shorter last one.  No
 // division on the way: the walk runs once per chunk on the critical path of
 // both roles, where a 64-bit division by a variable chunk count cost as much
 // as the chunk's arithmetic.
-template <int EB, int NW>
+template <int EB>
 struct RowWalk {
   int seg;
   unsigned pos, hi;     // the next chunk starts at pos; the warp's share ends at hi
   unsigned char* base;  // the row's first byte in shard seg
   bool ok;
 
-  __device__ __forceinline__ bool seek(const Geo& g, int t, long long r, int w, int from) {
-    for (seg = from; seg < t; ++seg) {
+  __device__ __forceinline__ bool seek(const Geo& g, const RowPart& rp, long long r, int from) {
+    for (seg = from > rp.sa ? from : rp.sa; seg < rp.sb; ++seg) {
       unsigned lo;
-      sub_range<NW>(unsigned(g.start[seg + 1] - g.start[seg]) * EB, w, lo, hi);
+      sub_range(unsigned(g.start[seg + 1] - g.start[seg]) * EB, rp, lo, hi);
       if (hi > lo) {
         pos = lo;
         base = const_cast<unsigned char*>(g.ptr[seg]) + r * g.ld[seg];
@@ -165,9 +204,9 @@ struct RowWalk {
     }
     return ok = false;
   }
-  __device__ __forceinline__ void next(const Geo& g, int t, long long r, int w) {
+  __device__ __forceinline__ void next(const Geo& g, const RowPart& rp, long long r) {
     pos += kFChunk;
-    if (pos >= hi) seek(g, t, r, w, seg + 1);
+    if (pos >= hi) seek(g, rp, r, seg + 1);
   }
   __device__ __forceinline__ void bounds(unsigned& a, unsigned& b) const {
     a = pos;
@@ -176,34 +215,34 @@ struct RowWalk {
   __device__ __forceinline__ unsigned char* addr(unsigned a) const { return base + a; }
 };
 
-// Chunks of one row that warp w of NW owns (the same for every row).
-template <int EB, int NW>
-__device__ __forceinline__ unsigned row_chunks(const Geo& g, int t, int w) {
+// Chunks of one row in a warp's part (the same for every row).
+template <int EB>
+__device__ __forceinline__ unsigned row_chunks(const Geo& g, const RowPart& rp) {
   unsigned c = 0;
-  for (int i = 0; i < t; ++i) {
+  for (int i = rp.sa; i < rp.sb; ++i) {
     unsigned lo, hi;
-    sub_range<NW>(unsigned(g.start[i + 1] - g.start[i]) * EB, w, lo, hi);
+    sub_range(unsigned(g.start[i + 1] - g.start[i]) * EB, rp, lo, hi);
     c += (hi - lo + kFChunk - 1) / kFChunk;
   }
   return c;
 }
 
-// The load side of a warp's walk: the chunks of its share of every row the
+// The load side of a warp's walk: the chunks of its part of every row the
 // CTA owns (rows r0, r0 + step, ...), ignored rows skipped, in the order the
 // arithmetic consumes them.
-template <int EB, int NW>
+template <int EB>
 struct RowCursor {
   long long r, step;
-  RowWalk<EB, NW> wk;
+  RowWalk<EB> wk;
   bool ok;
 
-  __device__ __forceinline__ void start(const FusedParams& p, const Geo& g, int t, int w, long long r0,
+  __device__ __forceinline__ void start(const FusedParams& p, const Geo& g, const RowPart& rp, long long r0,
                                         long long st) {
     step = st;
     r = r0 - st;
-    next_row(p, g, t, w);
+    next_row(p, g, rp);
   }
-  __device__ __forceinline__ void next_row(const FusedParams& p, const Geo& g, int t, int w) {
+  __device__ __forceinline__ void next_row(const FusedParams& p, const Geo& g, const RowPart& rp) {
     for (;;) {
       r += step;
       if (r >= p.s) {
@@ -211,15 +250,15 @@ struct RowCursor {
         return;
       }
       if (__ldg(p.targets + r) == p.ignore_index) continue;
-      if (wk.seek(g, t, r, w, 0)) {
+      if (wk.seek(g, rp, r, 0)) {
         ok = true;
         return;
       }
     }
   }
-  __device__ __forceinline__ void advance(const FusedParams& p, const Geo& g, int t, int w) {
-    wk.next(g, t, r, w);
-    if (!wk.ok) next_row(p, g, t, w);
+  __device__ __forceinline__ void advance(const FusedParams& p, const Geo& g, const RowPart& rp) {
+    wk.next(g, rp, r);
+    if (!wk.ok) next_row(p, g, rp);
   }
 };
 
@@ -250,15 +289,24 @@ __device__ __forceinline__ void target_of(const Geo& g, int t, long long y, int&
   }
 }
 
-template <typename T>
+// PAIR: a cluster of two CTAs shares each row, CTA c taking the c-th half of
+// every warp role's column split (2 kSW stats warps per row).  Each CTA's
+// live L2 window then holds half-rows, which keeps rows longer than
+// kLiveBytesPerCta re-read from L2.  The stats warps of both CTAs post their
+// partials to both CTAs' mailboxes (16 arrivals), and every grad warp folds
+// the 16 partials in CTA-rank order, so both CTAs reach the same logsumexp.
+template <typename T, bool PAIR>
 __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid_constant__ FusedParams p) {
   constexpr int EB = Elem<T>::kBytes;
+  constexpr int NR = PAIR ? 2 : 1;  // CTAs per row
+  constexpr int NWR = NR * kSW;     // warps of one role per row
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   FusedSmem& sm = *reinterpret_cast<FusedSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const bool stats = warp < kSW;
   const int w = stats ? warp : warp - kSW;
+  const unsigned crank = PAIR ? cluster_rank() : 0u;
 
   if (lane == 0) {
     if (stats) {
@@ -269,10 +317,10 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     if (stats) sm.sdone[w] = 0u;
     else sm.gdone[w] = 0u;
     if (warp == 0) {
-      mbar_init(&sm.rowdone[0], kSW);
-      mbar_init(&sm.rowdone[1], kSW);
-      mbar_init(&sm.rowfree[0], kDW);
-      mbar_init(&sm.rowfree[1], kDW);
+      mbar_init(&sm.rowdone[0], NR * kSW);
+      mbar_init(&sm.rowdone[1], NR * kSW);
+      mbar_init(&sm.rowfree[0], NR * kDW);
+      mbar_init(&sm.rowfree[1], NR * kDW);
     }
     fence_mbar_init();
   }
@@ -284,12 +332,26 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     }
   }
   __syncthreads();
+  // the peer's barriers must be initialised before any arrival reaches them
+  if (PAIR) cluster_sync_all();
   const Geo& geo = sm.geo;
   const int nt = p.t;
+  const RowPart rp = row_part(geo, nt, PAIR, crank, w);  // this warp's part of every row
 
-  const long long r_step = gridDim.x;
-  const long long r0 = blockIdx.x;
+  const long long r_step = gridDim.x / NR;
+  const long long r0 = blockIdx.x / NR;
   bool alive = true;
+  auto wait_row_bar = [&](uint64_t* bar, uint32_t parity) {
+    return PAIR ? mbar_wait_warp_cluster(bar, parity) : mbar_wait_warp(bar, parity);
+  };
+  auto arrive_row_bar = [&](uint64_t* bar) {  // lane 0 only
+    if (PAIR) {
+      mbar_arrive_cluster(bar, 0u);
+      mbar_arrive_cluster(bar, 1u);
+    } else {
+      mbar_arrive_local(bar);
+    }
+  };
 
   if (stats) {
     // ---------------- stats warps: pass 1 from HBM.  The loads run ahead of
@@ -304,9 +366,9 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     // (on GB300 evict_last here measured 0.4% slower; dropping evict_first on
     // the grad side, 18% slower)
     const uint64_t pol = policy_evict_normal();
-    const unsigned budget = row_chunks<EB, kSW>(geo, nt, w) + p.credit_slack;
-    RowCursor<EB, kSW> prod;
-    prod.start(p, geo, nt, w, r0, r_step);
+    const unsigned budget = row_chunks<EB>(geo, rp) + p.credit_slack;
+    RowCursor<EB> prod;
+    prod.start(p, geo, rp, r0, r_step);
     unsigned issued = 0, kc = 0, n = 0;
     auto top_up = [&]() {
       const unsigned credit = __shfl_sync(kFull, ld_volatile(&sm.gdone[w]), 0) + budget;
@@ -319,7 +381,7 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
           bulk_load(ring[slot], prod.wk.addr(a), b - a, &full[slot], pol);
         }
         ++issued;
-        prod.advance(p, geo, nt, w);
+        prod.advance(p, geo, rp);
       }
     };
 #pragma unroll 1
@@ -331,9 +393,9 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
       target_of<EB>(geo, nt, y, ty, toff);
       float m = -INFINITY, se = 0.f, zt = 0.f;
       bool has_t = false;
-      RowWalk<EB, kSW> cw;
+      RowWalk<EB> cw;
 #pragma unroll 1
-      for (cw.seek(geo, nt, r, w, 0); cw.ok; cw.next(geo, nt, r, w)) {
+      for (cw.seek(geo, rp, r, 0); cw.ok; cw.next(geo, rp, r)) {
         top_up();
         if (issued == kc && prod.ok) {  // out of credit for the chunk needed now
           if (!wait_counter_above(&sm.gdone[w], kc - budget)) {
@@ -363,14 +425,19 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
       // the mailbox slot of this row last held row n - 2: the grad warps
       // must have taken it (with the credit above this never waits)
       const int buf = int(n & 1u);
-      if (n >= 2 && !mbar_wait_warp(&sm.rowfree[buf], ((n - 2) >> 1) & 1u)) {
+      if (n >= 2 && !wait_row_bar(&sm.rowfree[buf], ((n - 2) >> 1) & 1u)) {
         alive = false;
         break;
       }
       if (lane == 0) {
         sm.part[buf][w] = make_float2(m, se);
-        if (has_t) sm.tz[buf] = zt;
-        mbar_arrive_local(&sm.rowdone[buf]);
+        if (has_t) {
+          sm.tz[buf] = zt;
+          if (PAIR)  // the peer's grad warps read the target logit from their own mailbox
+            asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr(&sm.tz[buf], crank ^ 1u)), "f"(zt)
+                         : "memory");
+        }
+        arrive_row_bar(&sm.rowdone[buf]);
       }
       ++n;
     }
@@ -390,8 +457,8 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     const uint64_t pol = policy_evict_first();
     const int n_valid = p.hdr->n_valid;
     const float scale_all = p.reduction != VPCE_MEAN ? p.grad : (n_valid > 0 ? p.grad / float(n_valid) : 0.f);
-    RowCursor<EB, kDW> prod;
-    prod.start(p, geo, nt, w, r0, r_step);
+    RowCursor<EB> prod;
+    prod.start(p, geo, rp, r0, r_step);
     unsigned kc = 0, issued = 0, n = 0;
     auto issue = [&]() {
       unsigned a, b;
@@ -403,7 +470,7 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
         bulk_load(ring[slot], prod.wk.addr(a), b - a, &full[slot], pol);
       }
       ++issued;
-      prod.advance(p, geo, nt, w);
+      prod.advance(p, geo, rp);
     };
     auto top_up = [&]() {
       const unsigned avail = __shfl_sync(kFull, ld_volatile(&sm.sdone[w]), 0);
@@ -414,13 +481,13 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
       const long long y = __ldg(p.targets + r);
       if (y == p.ignore_index) {
         // ignored row: zeros over this warp's share, nothing read
-        for (int i = 0; i < nt; ++i) {
+        for (int i = rp.sa; i < rp.sb; ++i) {
           unsigned lo, hi;
-          sub_range<kDW>(unsigned(geo.start[i + 1] - geo.start[i]) * EB, w, lo, hi);
+          sub_range(unsigned(geo.start[i + 1] - geo.start[i]) * EB, rp, lo, hi);
           uint4* d = reinterpret_cast<uint4*>(const_cast<unsigned char*>(geo.ptr[i]) + r * geo.ld[i] + lo);
           for (unsigned v = lane; v < (hi - lo) >> 4; v += 32) d[v] = make_uint4(0u, 0u, 0u, 0u);
         }
-        if (w == 0 && lane == 0) {
+        if (w == 0 && lane == 0 && crank == 0) {
           p.rowl[r] = 0.f;
           p.lse[r] = 0.f;
           if (p.row_loss) p.row_loss[r] = 0.f;
@@ -433,20 +500,35 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
       const bool in_range = ty >= 0;
       const int buf = int(n & 1u);
       top_up();
-      if (!mbar_wait_warp(&sm.rowdone[buf], (n >> 1) & 1u)) {
+      if (!wait_row_bar(&sm.rowdone[buf], (n >> 1) & 1u)) {
         alive = false;
         break;
       }
-      // every grad warp folds the partials in the same order: the same lse
-      float M = sm.part[buf][0].x, S = sm.part[buf][0].y;
+      // every grad warp folds the partials in the same order (CTA rank, then
+      // warp): the same lse in every warp of both CTAs
+      float M, S, zt;
+      if (PAIR) {
+        const float2 q0 = ld_cluster_f2(&sm.part[buf][0], 0u);
+        M = q0.x;
+        S = q0.y;
 #pragma unroll
-      for (int j = 1; j < kSW; ++j) merge_ms(M, S, sm.part[buf][j].x, sm.part[buf][j].y);
-      const float zt = sm.tz[buf];
+        for (int j = 1; j < NWR; ++j) {
+          const float2 q = ld_cluster_f2(&sm.part[buf][j % kSW], unsigned(j / kSW));
+          merge_ms(M, S, q.x, q.y);
+        }
+        zt = sm.tz[buf];  // written here by whichever CTA's warp holds the target
+      } else {
+        M = sm.part[buf][0].x;
+        S = sm.part[buf][0].y;
+#pragma unroll
+        for (int j = 1; j < kSW; ++j) merge_ms(M, S, sm.part[buf][j].x, sm.part[buf][j].y);
+        zt = sm.tz[buf];
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive_local(&sm.rowfree[buf]);
+      if (lane == 0) arrive_row_bar(&sm.rowfree[buf]);
       ++n;
       const float lse = in_range ? M + logf(S) : __int_as_float(0x7fc00000);
-      if (w == 0 && lane == 0) {
+      if (w == 0 && lane == 0 && crank == 0) {
         const float rl = in_range ? lse - zt : lse;
         p.lse[r] = lse;
         p.rowl[r] = rl;
@@ -456,9 +538,9 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
       const float c = -lse * kLog2e;
       const float cb = folded_offset(c, scale);
 
-      RowWalk<EB, kDW> cw;
+      RowWalk<EB> cw;
 #pragma unroll 1
-      for (cw.seek(geo, nt, r, w, 0); cw.ok; cw.next(geo, nt, r, w)) {
+      for (cw.seek(geo, rp, r, 0); cw.ok; cw.next(geo, rp, r)) {
         top_up();
         if (issued == kc && prod.ok) issue();  // the stats partner has finished this row: the bytes are in L2
         unsigned a, b;
@@ -495,6 +577,8 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     }
     if (lane == 0) bulk_wait_all<0>();  // every dlogits store has landed
   }
+  // no CTA leaves while its peer may still reach its mailbox or barriers
+  if (PAIR) cluster_sync_all();
 
   // ---- batch loss: the last block sums the per-row losses in a fixed order
   __threadfence();
@@ -543,11 +627,26 @@ bool fused_supported(const ShardSet& sh, int t, int elem) {
 }
 
 cudaError_t set_fused_smem() {
-  cudaError_t e = cudaFuncSetAttribute(stream_fused_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(sizeof(FusedSmem)));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(stream_fused_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(sizeof(FusedSmem)));
+  const int b = int(sizeof(FusedSmem));
+  cudaError_t e = cudaFuncSetAttribute(stream_fused_kernel<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_fused_kernel<__nv_bfloat16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_fused_kernel<float, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_fused_kernel<__nv_bfloat16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+  return e;
+}
+
+// Two CTAs share each row once a row no longer fits one CTA's live window.
+bool fused_pair(long long row_bytes) { return row_bytes > (long long)kLiveBytesPerCta; }
+
+// CTAs of the persistent grid: one per SM (pairs of SMs per row with pair),
+// no more than the rows need.
+int fused_grid(long long s, int sms, bool pair) {
+  if (!pair) return int(s < sms ? s : sms);
+  const long long clusters = s < sms / 2 ? s : sms / 2;
+  return int(2 * clusters);
 }
 
 void launch_prep(const long long* targets, long long s, long long V, long long ignore_index, Header* hdr,
@@ -576,17 +675,37 @@ void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long
   p.reduction = reduction;
   p.grad = grad;
   p.grad_rows = grad_rows;
-  p.credit_slack = credit_slack(V * (bf16 ? 2 : 4));
+  const long long row_bytes = V * (bf16 ? 2 : 4);
+  const bool pair = fused_pair(row_bytes);
+  p.credit_slack = credit_slack(pair ? (row_bytes + 1) / 2 : row_bytes);
   p.lse = lse;
   p.rowl = rowl;
   p.row_loss = row_loss;
   p.loss_out = loss_out;
   p.hdr = hdr;
-  const int grid = int(s < sms ? s : sms);
-  if (bf16)
-    stream_fused_kernel<__nv_bfloat16><<<grid, kFThreads, sizeof(FusedSmem), st>>>(p);
-  else
-    stream_fused_kernel<float><<<grid, kFThreads, sizeof(FusedSmem), st>>>(p);
+  const int grid = fused_grid(s, sms, pair);
+  if (pair) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kFThreads);
+    cfg.dynamicSmemBytes = sizeof(FusedSmem);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (bf16)
+      cudaLaunchKernelEx(&cfg, stream_fused_kernel<__nv_bfloat16, true>, p);
+    else
+      cudaLaunchKernelEx(&cfg, stream_fused_kernel<float, true>, p);
+  } else if (bf16) {
+    stream_fused_kernel<__nv_bfloat16, false><<<grid, kFThreads, sizeof(FusedSmem), st>>>(p);
+  } else {
+    stream_fused_kernel<float, false><<<grid, kFThreads, sizeof(FusedSmem), st>>>(p);
+  }
 }
 
 }  // namespace vpce
