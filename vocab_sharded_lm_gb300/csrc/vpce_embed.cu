@@ -58,14 +58,6 @@ __device__ __forceinline__ int shard_of(const long long* start, int t, long long
   return lo;
 }
 
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 __global__ void __launch_bounds__(kEmbThreads) embed_forward_kernel(const __grid_constant__ EmbedFwdParams p) {
   __shared__ long long start[VPCE_MAX_SHARDS + 1];
   __shared__ const unsigned char* base[VPCE_MAX_SHARDS];
@@ -93,22 +85,16 @@ __global__ void __launch_bounds__(kEmbThreads) embed_forward_kernel(const __grid
       uint4* d = reinterpret_cast<uint4*>(dst);
       const uint4* sp = reinterpret_cast<const uint4*>(src);
       long long v = lane;
-      for (; v + 96 < nv; v += 128) {  // four independent 16-byte loads in flight per lane
-        uint4 a, b, c, e;
-        if (i >= 0) {
-          a = ld_stream(sp + v);
-          b = ld_stream(sp + v + 32);
-          c = ld_stream(sp + v + 64);
-          e = ld_stream(sp + v + 96);
-        } else {
-          a = b = c = e = make_uint4(0u, 0u, 0u, 0u);
-        }
-        d[v] = a;
-        d[v + 32] = b;
-        d[v + 64] = c;
-        d[v + 96] = e;
+      // eight independent 16-byte streaming loads in flight per lane (plain
+      // intrinsics, so the compiler may also start the next eight early)
+      for (; v + 224 < nv; v += 256) {
+        uint4 q[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) q[u] = i >= 0 ? __ldcs(sp + v + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) d[v + 32 * u] = q[u];
       }
-      for (; v < nv; v += 32) d[v] = i >= 0 ? ld_stream(sp + v) : make_uint4(0u, 0u, 0u, 0u);
+      for (; v < nv; v += 32) d[v] = i >= 0 ? __ldcs(sp + v) : make_uint4(0u, 0u, 0u, 0u);
     } else if (p.eb == 2) {
       unsigned short* d = reinterpret_cast<unsigned short*>(dst);
       const unsigned short* sp = reinterpret_cast<const unsigned short*>(src);
