@@ -41,9 +41,11 @@ def _capture(fn):
     return g
 
 
-@pytest.mark.parametrize("path", ["split", "fused", "rows"])
-def test_loss_paths_replay_identically(path):
-    w = synth.WORKLOADS["s8192_v128256"].replace(s=64)
+@pytest.mark.parametrize("path,wl", [("split", "s8192_v128256"), ("fused", "s8192_v128256"),
+                                     ("rows", "s8192_v128256"), ("fused", "s32768_v256000")])
+def test_loss_paths_replay_identically(path, wl):
+    # s32768_v256000: 512 KB rows, the fused kernel's two-CTA cluster launch
+    w = synth.WORKLOADS[wl].replace(s=64)
     vs = synth.even_vocab_start(w.V, w.t)
     meta = synth.row_meta(w)
     host = synth.shards_host(w, meta, vs)
@@ -103,12 +105,22 @@ def test_lmhead_and_embedding_replay_identically():
     dx = torch.empty_like(x)
     dw = [torch.zeros(sh.shape, dtype=torch.float32, device="cuda") for sh in wsh]
     bwk = torch.empty(vpce.vpce_lmhead_backward_workspace_bytes(m.V, m.h), dtype=torch.uint8, device="cuda")
+    # the one-call training step: prologue, logits-keeping GEMM, row kernel, cuBLAS, loss sum
+    loss2 = torch.empty((), dtype=torch.float32, device="cuda")
+    dx2 = torch.empty_like(x)
+    dw2 = [torch.zeros(sh.shape, dtype=torch.float32, device="cuda") for sh in wsh]
+    twk = torch.empty(vpce.vpce_lmhead_forward_backward_workspace_bytes(m.s, m.V, m.h), dtype=torch.uint8,
+                      device="cuda")
 
     def step():
         vpce.vpce_lmhead_forward(x, wsh, y, mvs, loss_out=loss, workspace=wk)
         for d in dw:
             d.zero_()
         vpce.vpce_lmhead_backward(x, wsh, y, wk, mvs, grad_hidden=dx, grad_weight_shards=dw, workspace=bwk)
+        for d in dw2:
+            d.zero_()
+        vpce.vpce_lmhead_forward_backward(x, wsh, y, mvs, loss_out=loss2, grad_hidden=dx2, grad_weight_shards=dw2,
+                                          workspace=twk)
         vpce.vpce_embedding_forward(tab, ids, tvs, out=out, flag=flag)
         for t_ in gtab:
             t_.zero_()
@@ -116,12 +128,15 @@ def test_lmhead_and_embedding_replay_identically():
 
     step()
     torch.cuda.synchronize()
-    ref = (float(loss), out.clone(), [t_.clone() for t_ in gtab], dx.clone(), [d.clone() for d in dw])
+    ref = (float(loss), out.clone(), [t_.clone() for t_ in gtab], dx.clone(), [d.clone() for d in dw],
+           float(loss2), dx2.clone(), [d.clone() for d in dw2])
     g = _capture(step)
     for _ in range(3):
         loss.fill_(-1.0)
         out.zero_()
         dx.zero_()
+        dx2.zero_()
+        loss2.fill_(-1.0)
         g.replay()
         torch.cuda.synchronize()
         assert float(loss) == ref[0]
@@ -130,4 +145,8 @@ def test_lmhead_and_embedding_replay_identically():
             assert torch.equal(a, b)
         assert torch.equal(dx, ref[3])
         for a, b in zip(ref[4], dw):
+            assert torch.equal(a, b)
+        assert float(loss2) == ref[5]
+        assert torch.equal(dx2, ref[6])
+        for a, b in zip(ref[7], dw2):
             assert torch.equal(a, b)
