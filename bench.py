@@ -135,7 +135,7 @@ class ClockSampler:
 # the source file of each kernel whose ncu traffic is recorded; the shared
 # device headers count for all of them
 _KERNEL_FILES = {"stream_fused_kernel": "vpce_fused.cu", "backward_kernel": "vpce_backward.cu",
-                 "partial_stats_kernel": "vpce_forward.cu"}
+                 "partial_stats_kernel": "vpce_forward.cu", "gemm_stats_kernel": "vpce_gemm.cu"}
 
 
 def _kernel_source_hash(kernel: str) -> str:
@@ -685,7 +685,7 @@ def run_lmhead(args):
             "unit": "TFLOP/s",
             "frac": round(achieved / burst, 4),
             "frac_of_sustained": round(achieved / sustained, 4),
-            "traffic": None,
+            "traffic": None if train else _ncu_traffic("gemm_stats_kernel", m.name),
             "algorithmic_flops_per_launch": flops,
             "note": ("achieved = 6 s h V (logits, dX, dW) / mean CUDA-event time of one training step" if train else
                      "achieved = 2 s h V / mean CUDA-event time of one call (the GEMM launch plus the few-us combine)"),

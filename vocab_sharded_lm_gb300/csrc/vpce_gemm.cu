@@ -30,11 +30,13 @@
 //               the row's target column falls in the tile.  With all 512
 //               columns holding the pair, the next tile's MMAs wait for it
 //               (a few percent of a tile's MMA time).
-// CTA c takes M-tile pair (wave * gm + c % gm) and the N tiles of group
-// c / gm, for every wave: the gm CTAs of a group read the same W tile at the
-// same time (L2 hits), and the gn CTAs of a pair read the same X tiles.  Each
-// CTA writes one partial per row and group; the combine kernel of the
-// sharded loss folds them in group order.
+// CTA c takes M-tile pair (wave * gm + c % gm) and, in each wave, one of gn
+// ranges of N tiles, the same for the gm CTAs of group c / gm: they read the
+// same W tile at the same time (L2 hits), and the gn CTAs of a pair read the
+// same X tiles.  A group's range moves on by one each wave, which spreads
+// the longer ranges evenly over the groups.  Each CTA writes one partial per
+// row for its range; the combine kernel of the sharded loss folds them in
+// range order, i.e. in vocabulary order.
 #include <cuda.h>
 
 #include <cstring>
@@ -83,7 +85,7 @@ struct GemmParams {
   int nstart[kMaxGemmShards + 1];   // first N tile of each shard
   const long long* targets;
   long long ignore_index;
-  float2* part;                     // [gn][s]: (max, sum exp) of the group's columns
+  float2* part;                     // [gn][s]: (max, sum exp) of each N-tile range
   float* tgt;                       // [s]: target logit
   Header* hdr;
   // gradient epilogue only
@@ -344,10 +346,22 @@ __device__ __forceinline__ void epi_row_tile(const GemmParams& p, EpiRow& e, uin
   }
 }
 
+// The N tiles group grp takes in wave wv, and the index of that range (the
+// partial it writes).  The gn ranges split the N tiles as evenly as integer
+// division allows, and a group's range moves on by one each wave.  The ranges
+// one tile longer than the rest then fall to each group in turn, so that no
+// CTA runs more than the ceiling of the mean tile count over all waves.
+__device__ __forceinline__ int wave_range(const GemmParams& p, int grp, int wv, int* nt0, int* nt1) {
+  const int g = (grp + wv) % p.gn;
+  *nt0 = int((long long)g * p.n_tiles / p.gn);
+  *nt1 = int((long long)(g + 1) * p.n_tiles / p.gn);
+  return g;
+}
+
 template <int EPI>
-__device__ __forceinline__ void epi_row_finish(const GemmParams& p, const EpiRow& e, int grp) {
+__device__ __forceinline__ void epi_row_finish(const GemmParams& p, const EpiRow& e, int range) {
   if (EPI != kEpiGrad && e.live) {
-    p.part[(long long)grp * p.s + e.r] = make_float2(e.m, e.se);
+    p.part[(long long)range * p.s + e.r] = make_float2(e.m, e.se);
     if (e.has_t) p.tgt[e.r] = e.zt;
   }
 }
@@ -387,8 +401,6 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
 
   const int m_slot = int(blockIdx.x) % p.gm;
   const int grp = int(blockIdx.x) / p.gm;
-  const int nt0 = int((long long)grp * p.n_tiles / p.gn);
-  const int nt1 = int((long long)(grp + 1) * p.n_tiles / p.gn);
   const int waves = (p.m_pairs + p.gm - 1) / p.gm;
 
   if (warp == 0) {
@@ -399,6 +411,8 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
       for (int wv = 0; wv < waves && ok; ++wv) {
         const int mp = wv * p.gm + m_slot;
         if (mp >= p.m_pairs) break;
+        int nt0, nt1;
+        wave_range(p, grp, wv, &nt0, &nt1);
         for (int nt = nt0; nt < nt1 && ok; ++nt) {
           const int sh = shard_of_tile(p, nt);
           const int n_off = (nt - p.nstart[sh]) * kBN;
@@ -439,6 +453,8 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
       for (int wv = 0; wv < waves && ok; ++wv) {
         const int mp = wv * p.gm + m_slot;
         if (mp >= p.m_pairs) break;
+        int nt0, nt1;
+        wave_range(p, grp, wv, &nt0, &nt1);
         for (int nt = nt0; nt < nt1 && ok; ++nt) {
           // the epilogue has read the previous tile's accumulators
           if (!wait1(&sm.acc_empty, (tiles & 1u) ^ 1u, &sm.abort_flag)) {
@@ -495,6 +511,8 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
     for (int wv = 0; wv < waves && ok; ++wv) {
       const int mp = wv * p.gm + m_slot;
       if (mp >= p.m_pairs) break;
+      int nt0, nt1;
+      const int range = wave_range(p, grp, wv, &nt0, &nt1);
       EpiRow e0, e1;
       epi_row_start<EPI>(p, (kMT * mp) * kBM + row_in_tile, e0);
       epi_row_start<EPI>(p, (kMT * mp + 1) * kBM + row_in_tile, e1);
@@ -516,8 +534,8 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
         ++tiles;
       }
       if (!ok) break;
-      epi_row_finish<EPI>(p, e0, grp);
-      epi_row_finish<EPI>(p, e1, grp);
+      epi_row_finish<EPI>(p, e0, range);
+      epi_row_finish<EPI>(p, e1, range);
     }
     if (!ok && lane == 0) {
       sm.abort_flag = 1;
