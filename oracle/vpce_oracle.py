@@ -30,7 +30,7 @@ written out in fp64 over the re-assembled full rows.  :func:`shard_partials` and
 tests check that it agrees with the unsharded definition, and nothing on the
 GPU side calls it.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings taken where the pages are silent:
 * backward: d(mean CE)/dz = g * (softmax(z) - onehot(y)) / n_valid  (the
   standard derivative of the mean loss; the pages give no backward);
 * reduction: mean over rows whose target is not ``ignore_index`` (the default
