@@ -156,4 +156,108 @@ __device__ __forceinline__ void grad_chunk(unsigned char* buf, unsigned n, int l
   }
 }
 
+// ---------------------------------------------------------------------------
+// Forms for the streaming fused kernel with bf16 logits, whose 16 warps share
+// the SM's issue slots with both passes' arithmetic.
+//   * One scalar FFMA per element.  The packed form first builds a 64-bit
+//     register pair from two unpacked halves, and those moves cost more than
+//     the pairing saves.
+//   * The gradient loop loads every vector of the lane before it stores any,
+//     so the lane's dependent chains overlap (load, exponent, round, store one
+//     vector at a time serialises them: the stores may alias the next loads).
+// Measured on GB300 at s = 8192, V = 128256: 0.748 -> 0.720 ms per fused
+// call.  fp32 logits keep the packed forms and the one-vector loop (their
+// float4 vectors already are register pairs; measured 3.65 against 3.74 ms at
+// s = 16384, V = 152064), and so do the split kernels (1% faster there) and
+// rows shared by a CTA pair.
+// ---------------------------------------------------------------------------
+template <int VPL>
+__device__ __forceinline__ void stats_chunk_fused(const unsigned char* buf, unsigned n, int lane, float& m,
+                                                  float& sm, __nv_bfloat16) {
+  const uint4* v = reinterpret_cast<const uint4*>(buf);
+  const int nv = int(n >> 4);
+  uint4 q[VPL];
+  const uint4 neg = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);  // bf16 -inf x8
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int idx = lane + 32 * j;
+    q[j] = idx < nv ? v[idx] : neg;
+  }
+  __nv_bfloat162 mx = __halves2bfloat162(__ushort_as_bfloat16(0xff80), __ushort_as_bfloat16(0xff80));
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&q[j].x));
+    mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&q[j].y));
+    mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&q[j].z));
+    mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&q[j].w));
+  }
+  const float cm = fmaxf(__low2float(mx), __high2float(mx));
+  if (cm > m) {
+    sm *= ex2((m - cm) * kLog2e);
+    m = cm;
+  }
+  if (m == -INFINITY) return;
+  const float nb = -m * kLog2e;
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    s0 += ex2(fmaf(bf16_lo(q[j].x), kLog2e, nb));
+    s1 += ex2(fmaf(bf16_hi(q[j].x), kLog2e, nb));
+    s2 += ex2(fmaf(bf16_lo(q[j].y), kLog2e, nb));
+    s3 += ex2(fmaf(bf16_hi(q[j].y), kLog2e, nb));
+    s0 += ex2(fmaf(bf16_lo(q[j].z), kLog2e, nb));
+    s1 += ex2(fmaf(bf16_hi(q[j].z), kLog2e, nb));
+    s2 += ex2(fmaf(bf16_lo(q[j].w), kLog2e, nb));
+    s3 += ex2(fmaf(bf16_hi(q[j].w), kLog2e, nb));
+  }
+  sm += (s0 + s1) + (s2 + s3);
+}
+
+template <int VPL>
+__device__ __forceinline__ void stats_chunk_fused(const unsigned char* buf, unsigned n, int lane, float& m,
+                                                  float& sm, float) {
+  stats_chunk<VPL>(buf, n, lane, m, sm, float());
+}
+
+// 2^(x log2 e + b) of every element of a vector, rounded to the element type.
+__device__ __forceinline__ uint4 grad_vec_fused(const uint4& w, float b, __nv_bfloat16) {
+  const float p0 = ex2(fmaf(bf16_lo(w.x), kLog2e, b)), p1 = ex2(fmaf(bf16_hi(w.x), kLog2e, b));
+  const float p2 = ex2(fmaf(bf16_lo(w.y), kLog2e, b)), p3 = ex2(fmaf(bf16_hi(w.y), kLog2e, b));
+  const float p4 = ex2(fmaf(bf16_lo(w.z), kLog2e, b)), p5 = ex2(fmaf(bf16_hi(w.z), kLog2e, b));
+  const float p6 = ex2(fmaf(bf16_lo(w.w), kLog2e, b)), p7 = ex2(fmaf(bf16_hi(w.w), kLog2e, b));
+  return make_uint4(pack_bf16x2(p0, p1), pack_bf16x2(p2, p3), pack_bf16x2(p4, p5), pack_bf16x2(p6, p7));
+}
+// grad_chunk for the fused kernel: bf16 with a positive scale (the folded
+// exponent) loads every vector of the lane, then transforms, then stores;
+// everything else is grad_chunk.
+template <int VPL>
+__device__ __forceinline__ void grad_chunk_fused(unsigned char* buf, unsigned n, int lane, float c, float scale,
+                                                 float cb, float) {
+  grad_chunk<float, VPL>(buf, n, lane, c, scale, cb);
+}
+
+template <int VPL>
+__device__ __forceinline__ void grad_chunk_fused(unsigned char* buf, unsigned n, int lane, float c, float scale,
+                                                 float cb, __nv_bfloat16) {
+  if (!(scale > 0.f)) {
+    grad_chunk<__nv_bfloat16, VPL>(buf, n, lane, c, scale, cb);
+    return;
+  }
+  uint4* v = reinterpret_cast<uint4*>(buf);
+  const int nv = int(n >> 4);
+  uint4 q[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int idx = lane + 32 * j;
+    q[j] = idx < nv ? v[idx] : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) q[j] = grad_vec_fused(q[j], cb, __nv_bfloat16());
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int idx = lane + 32 * j;
+    if (idx < nv) v[idx] = q[j];
+  }
+}
+
 }  // namespace vpce
