@@ -42,9 +42,12 @@ def test_fused_more_rows_than_blocks():
     check_full(run_full(W["s4096_v50304"].replace(s=700), path="fused"))
 
 
-@pytest.mark.parametrize("reduction,grad", [("sum", 0.5), ("mean", 2.5), ("mean", 0.0)])
-def test_fused_reductions(reduction, grad):
-    check_full(run_full(W["s16384_v152064"].replace(s=48), reduction=reduction, grad=grad, path="fused"))
+@pytest.mark.parametrize("wl", ["s16384_v152064", "s8192_v128256"])
+@pytest.mark.parametrize("reduction,grad", [("sum", 0.5), ("mean", 2.5), ("mean", 0.0), ("sum", -1.5)])
+def test_fused_reductions(reduction, grad, wl):
+    # fp32 and bf16 rows; a gradient of 0 or below cannot be folded into the
+    # exponent and takes the explicit product
+    check_full(run_full(W[wl].replace(s=48), reduction=reduction, grad=grad, path="fused"))
 
 
 @pytest.mark.parametrize("widths", [[8, 8, 16], [16, 1024, 8000, 24], [4] * 64])
