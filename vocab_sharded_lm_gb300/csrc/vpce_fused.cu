@@ -38,8 +38,12 @@ constexpr int kSWLog2 = 3;
 constexpr int kDW = 8;         // grad warps
 constexpr int kFThreads = (kSW + kDW) * 32;
 constexpr int kFChunk = 4096;  // bytes per pipeline chunk
-constexpr int kSSlots = 4;     // ring slots per stats warp (HBM latency)
-constexpr int kDSlots = 3;     // ring slots per grad warp (L2 latency)
+// Ring slots per stats warp (HBM latency) and per grad warp (L2 latency, and
+// the slot its last store still reads).  Measured on GB300 with the same
+// 224 KB of rings: 3 and 4 beat 4 and 3 by 1.2% at s = 8192 (bf16, one CTA
+// per row) and by 4.6% at s = 16384 (fp32, CTA pairs); 5 and 2 lose 14%.
+constexpr int kSSlots = 3;
+constexpr int kDSlots = 4;
 // L2 bytes per CTA the two passes may keep live between them: one row is
 // the least (a row's statistics precede its gradient); rows shorter than
 // this let the stats warps run further ahead.  Measured on GB300: 320 KB per
