@@ -33,6 +33,17 @@ namespace vpce {
 namespace {
 
 constexpr int kPrepThreads = 1024;
+
+// Programmatic dependent launch.  The fused kernel is launched with the
+// programmatic stream serialization attribute, so it may start while the
+// prologue kernel ahead of it is still running; grid_dependency_wait() blocks
+// the calling thread until the prologue has completed and its writes are
+// visible (at once when launched without the attribute), and the prologue's
+// grid_launch_dependents() lets the fused kernel start.  Measured on GB300:
+// 0.7129 -> 0.7071 ms per call at s = 8192 (the same change on the split
+// path's combine and backward kernels gained nothing and was left out).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 constexpr int kSW = 8;         // stats warps
 constexpr int kSWLog2 = 3;
 constexpr int kDW = 8;         // grad warps
@@ -105,6 +116,7 @@ static_assert(sizeof(FusedSmem) + 1024 <= 232448, "fused kernel shared memory");
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const long long* targets, long long s,
                                                             long long V, long long ignore_index, Header* hdr,
                                                             int reduction, float* loss_out) {
+  grid_launch_dependents();  // the fused kernel's stats warps need nothing from here
   __shared__ int sc[kPrepThreads / 32];
   __shared__ int sbad[kPrepThreads / 32];
   int c = 0, bad = 0;
@@ -462,6 +474,10 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     unsigned char(*ring)[kFChunk] = sm.dring[w];
     uint64_t* full = sm.dfull[w];
     const uint64_t pol = policy_evict_first();
+    // the prologue (header, n_valid) may still be running: this kernel is
+    // launched as its programmatic dependent, and only the grad warps read
+    // what it writes
+    grid_dependency_wait();
     const int n_valid = p.hdr->n_valid;
     const float scale_all = p.reduction != VPCE_MEAN ? p.grad : (n_valid > 0 ? p.grad / float(n_valid) : 0.f);
     RowCursor<EB> prod;
@@ -589,6 +605,7 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
   if (PAIR) cluster_sync_all();
 
   // ---- batch loss: the last block sums the per-row losses in a fixed order
+  grid_dependency_wait();  // every thread: the header (ticket) is the prologue's
   __threadfence();
   __syncthreads();
   // every copy of this CTA has completed: the stats ring is free scratch
@@ -692,27 +709,29 @@ void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long
   p.loss_out = loss_out;
   p.hdr = hdr;
   const int grid = fused_grid(s, sms, pair);
+  // a programmatic dependent of the prologue: the stats warps start streaming
+  // while it counts n_valid
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kFThreads);
+  cfg.dynamicSmemBytes = sizeof(FusedSmem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pair ? 2 : 1;
   if (pair) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(grid));
-    cfg.blockDim = dim3(kFThreads);
-    cfg.dynamicSmemBytes = sizeof(FusedSmem);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (bf16)
-      cudaLaunchKernelEx(&cfg, stream_fused_kernel<__nv_bfloat16, true>, p);
-    else
-      cudaLaunchKernelEx(&cfg, stream_fused_kernel<float, true>, p);
+    if (bf16) cudaLaunchKernelEx(&cfg, stream_fused_kernel<__nv_bfloat16, true>, p);
+    else cudaLaunchKernelEx(&cfg, stream_fused_kernel<float, true>, p);
   } else if (bf16) {
-    stream_fused_kernel<__nv_bfloat16, false><<<grid, kFThreads, sizeof(FusedSmem), st>>>(p);
+    cudaLaunchKernelEx(&cfg, stream_fused_kernel<__nv_bfloat16, false>, p);
   } else {
-    stream_fused_kernel<float, false><<<grid, kFThreads, sizeof(FusedSmem), st>>>(p);
+    cudaLaunchKernelEx(&cfg, stream_fused_kernel<float, false>, p);
   }
 }
 
