@@ -615,16 +615,24 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
   __syncthreads();
   if (!*last) return;
   __threadfence();
+  // Each warp sums whole 256-row blocks: lane l adds rows 8l .. 8l + 7 of the
+  // block, then a fixed shuffle tree; a warp adds its blocks in order, and
+  // thread 0 the warps in order (a fixed order for a given s).  A block's
+  // loads are independent of one another: one thread walking 256 rows in
+  // sequence exposed each L2 latency (26 us per call at s = 8192).
   double v = 0.0;
   const long long nb = (p.s + 255) / 256;
-  for (long long b = threadIdx.x; b < nb; b += kFThreads) {
-    double bs = 0.0;
-    const long long e = min(p.s, (b + 1) * 256);
-    for (long long r = b * 256; r < e; ++r) bs += double(__ldcg(p.rowl + r));
-    v += bs;
-  }
+  for (long long b = warp; b < nb; b += kFThreads / 32) {
+    double part = 0.0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(kFull, v, o);
+    for (int j = 0; j < 8; ++j) {
+      const long long r = b * 256 + lane * 8 + j;
+      if (r < p.s) part += double(__ldcg(p.rowl + r));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_down_sync(kFull, part, o);
+    v += part;
+  }
   if (lane == 0) sv[warp] = v;
   __syncthreads();
   if (threadIdx.x == 0) {
