@@ -168,8 +168,7 @@ __device__ __forceinline__ void grad_chunk(unsigned char* buf, unsigned n, int l
 // Measured on GB300 at s = 8192, V = 128256: 0.748 -> 0.720 ms per fused
 // call.  fp32 logits keep the packed forms and the one-vector loop (their
 // float4 vectors already are register pairs; measured 3.65 against 3.74 ms at
-// s = 16384, V = 152064), and so do the split kernels (1% faster there) and
-// rows shared by a CTA pair.
+// s = 16384, V = 152064), and so do the split kernels (1% faster there).
 // ---------------------------------------------------------------------------
 template <int VPL>
 __device__ __forceinline__ void stats_chunk_fused(const unsigned char* buf, unsigned n, int lane, float& m,

@@ -428,10 +428,7 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
           break;
         }
         if (lane == 0) st_volatile(&sm.sdone[w], kc + 1);  // these bytes are in L2 now
-        // one CTA per row: the fused kernel's scalar bf16 forms; a CTA pair
-        // keeps the packed forms (measured 6.57 against 6.62 ms at s = 32768)
-        if constexpr (PAIR) stats_chunk<kFVPL>(ring[slot], b - a, lane, m, se, T());
-        else stats_chunk_fused<kFVPL>(ring[slot], b - a, lane, m, se, T());
+        stats_chunk_fused<kFVPL>(ring[slot], b - a, lane, m, se, T());
         if (cw.seg == ty && toff >= a && toff < b) {
           has_t = true;
           zt = Elem<T>::load(ring[slot] + (toff - a));
@@ -579,8 +576,7 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
         float dt = 0.f;
         if (has_t && lane == 0) dt = (ex2(fmaf(Elem<T>::load(sbuf + (toff - a)), kLog2e, c)) - 1.f) * scale;
         __syncwarp();
-        if constexpr (PAIR) grad_chunk<T, kFVPL>(sbuf, b - a, lane, c, scale, cb);
-        else grad_chunk_fused<kFVPL>(sbuf, b - a, lane, c, scale, cb, T());
+        grad_chunk_fused<kFVPL>(sbuf, b - a, lane, c, scale, cb, T());
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
