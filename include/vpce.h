@@ -89,7 +89,15 @@ typedef enum { VPCE_MEAN = 0, VPCE_SUM = 1, VPCE_NONE = 2 } vpce_reduction;
 size_t vpce_workspace_bytes(int t, int64_t s);
 
 /*
- * Forward: loss of the vocab-sharded logits.
+ * Forward: loss of the vocab-sharded logits.  Implements the pages' sharded
+ * cross-entropy ("Distributed Training III: Model Parallelism", CMU 11-868
+ * Lecture 16 notes, §5.5 "Embedding and output layer": each card reduces its
+ * block to a maximum, a sum of exponentials and, where it holds the target,
+ * the target logit; the blocks combine to logsumexp minus the target logit;
+ * "LLM Internals" §7.3.4: the same three quantities for the [8192, 128256]
+ * head split 16032 columns per card), with the t shards on one GPU and the
+ * combine on the device.  A wait that gave up (VPCE_FLAG_WAIT_TIMEOUT) makes
+ * every valid row's loss and the reduced loss NaN.
  *   shards       host array of t device pointers (read only here).
  *   dtype        element type of every shard.
  *   t            number of shards, 1..VPCE_MAX_SHARDS.
@@ -122,7 +130,11 @@ vpce_status vpce_forward(const void* const* shards, vpce_dtype dtype, int t, int
 
 /*
  * Backward: overwrite the shards in place with dlogits (same dtype; bf16 is
- * rounded to nearest-even from the fp32 value).  Every argument describing the
+ * rounded to nearest-even from the fp32 value).  Not on the pages, which
+ * give no backward: the standard derivative of the reduced cross-entropy,
+ * g * (softmax - onehot) / n_valid for 'mean', computed shard by shard from
+ * the forward's logsumexp (the combine of the CMU notes' §5.5 and "LLM
+ * Internals" §7.3.4 is what makes softmax available per shard).  Every argument describing the
  * logits and targets must equal the preceding vpce_forward's, the shards must
  * still hold that call's logits, and `workspace` must be that call's,
  * unmodified (it carries logsumexp, n_valid and the reduction).
@@ -186,6 +198,23 @@ vpce_status vpce_combine_partials(const float* part, int n_part, const float* tg
                                   const int64_t* targets, int64_t ignore_index, vpce_reduction reduction,
                                   float* loss_out, float* row_loss_out, int t_local,
                                   void* workspace, size_t workspace_bytes, vpce_stream_t stream);
+
+/*
+ * One process's partials folded to one (max, sum exp) pair per row before
+ * the exchange, so that each process sends the pages' three scalars per
+ * token -- maximum, sum of exponentials and (through the target all-reduce)
+ * the target logit -- whatever number of shards it holds ("Distributed
+ * Training III: Model Parallelism", CMU 11-868 Lecture 16 notes, §5.5: 12
+ * bytes per token instead of the logits).  part: device float2 [t][s] as
+ * vpce_partials writes it; out: device float2 [s] (8-byte aligned, may not
+ * overlap part), out[r] = (M, S) with M = max_i part[i][r].max and
+ * S = sum over i ascending of part[i][r].sum * exp(part[i][r].max - M), the
+ * combine's arithmetic.  Folded pairs of all processes, gathered in process
+ * order, go to vpce_combine_partials as n_part = (number of processes)
+ * partials.  Errors: t outside 1..VPCE_MAX_SHARDS or s < 0
+ * (VPCE_ERR_INVALID_ARG), misaligned pointers (VPCE_ERR_ALIGNMENT).
+ */
+vpce_status vpce_fold_partials(const float* part, int t, int64_t s, float* out, vpce_stream_t stream);
 
 /*
  * Forward and backward in one call: the loss (as vpce_forward) and the shards
@@ -254,10 +283,14 @@ vpce_status vpce_fused_plan(vpce_dtype dtype, int t, const int64_t* vocab_start,
  *     e.g., t = 16 at s = 32768, t = 8 at s = 65536 and t = 64 at s = 8192;
  *     roughly 8 * t * s + 8 * s bytes are needed).
  *   - Every call on a device shares the one array and the next call overwrites
- *     it (the kernels clear what must start at zero), so calls that may
+ *     it (each call clears what must start at zero), so calls that may
  *     overlap on the GPU -- on different streams, or from different threads --
  *     race: serialise them on one stream.  The workspace stays inside the
- *     library, so no vpce_backward can follow this forward.
+ *     library, so no vpce_backward can follow this forward, and its error
+ *     flag cannot be read: a bad target gives that row, and a wait that gave
+ *     up gives every row, a NaN loss, so a NaN loss_out is the signal.
+ *   - The array's address is cached per device after the first call, so a
+ *     device reset (cudaDeviceReset) after that call is not supported.
  */
 #define VPCE_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
 vpce_status vpce_forward_static(const void* const* shards, vpce_dtype dtype, int t, int64_t s,
@@ -306,24 +339,25 @@ vpce_status vpce_lmhead_forward(const void* hidden, int64_t ld_hidden,
  *     grad_weight_shards[i] += dZ_i^T X       fp32 [w_i, h], accumulated
  * The logits are formed again tile by tile on the tensor cores (the forward
  * kept none) and written as bf16 dZ for one chunk of rows at a time into
- * `workspace`; the two products are plain cuBLAS GEMMs (bf16 in, fp32
- * accumulate).  Every argument describing X, the head, the targets and
+ * `workspace`; two more tensor-core kernels then form the products (bf16 in,
+ * fp32 accumulate): dX with the contraction over all t shards in one
+ * accumulator, rounded once to bf16; dW_i added into grad_weight_shards[i]
+ * by tile reductions, one add per element per chunk, so the result is the
+ * same on every run.  Every argument describing X, the head, the targets and
  * fwd_workspace must be the preceding vpce_lmhead_forward's, unmodified
  * (it carries logsumexp, n_valid and the reduction).
  *   grad_output / grad_rows  as vpce_backward / vpce_backward_rows (grad_rows
  *                   device float[s] or NULL).
  *   grad_hidden     device bf16 [s, h], row stride ld_grad_hidden (0 = h).
  *   grad_weight_shards  host array of t device float pointers, [w_i, h],
- *                   row stride ld_grad_weight (0 = h), 16-byte aligned.
+ *                   row stride ld_grad_weight (0 = h), 16-byte aligned,
+ *                   ld_grad_weight a multiple of 4.
  *   workspace       256-byte aligned; vpce_lmhead_backward_workspace_bytes(V, h)
- *                   bytes give 4096-row chunks (dZ of one chunk, an fp32 dX
- *                   chunk, and 32 MiB of cuBLAS scratch).  A smaller
+ *                   bytes give 8192-row chunks (the chunk's bf16 dZ, each
+ *                   shard's columns padded to a multiple of 8).  A smaller
  *                   workspace gives smaller chunks, in steps of 128 rows;
  *                   less than 128 rows' worth returns VPCE_ERR_WORKSPACE.
- * The cuBLAS handle is created once per device on the first call (which is
- * therefore not capturable into a CUDA graph); it runs in the caller's
- * workspace, so later calls allocate nothing.  Calls on one device are
- * serialised on the handle.
+ * Calls launch kernels only (no allocation, no host synchronisation).
  */
 size_t vpce_lmhead_backward_workspace_bytes(int64_t V, int64_t h);
 vpce_status vpce_lmhead_backward(const void* hidden, int64_t ld_hidden,
@@ -343,8 +377,9 @@ vpce_status vpce_lmhead_backward(const void* hidden, int64_t ld_hidden,
  * Per row chunk, the tensor-core kernel writes the loss statistics and keeps
  * the chunk's fp32 logits in the workspace (a chunk is the unit the CMU notes
  * (§5.5) keep resident instead of the whole [s, V] tensor).  A row kernel
- * then forms each row's logsumexp, loss and bf16 dZ from them, and cuBLAS
- * computes dX = dZ W and dW += dZ^T X.
+ * then forms each row's logsumexp, loss and bf16 dZ from them, and the
+ * tensor-core kernels of vpce_lmhead_backward compute dX = dZ W and
+ * dW += dZ^T X.
  *   loss_out, row_loss_out, reduction   as vpce_lmhead_forward (the mean
  *                  divides by the batch's n_valid; the loss sum is fp64 over
  *                  fixed 256-row blocks).
@@ -352,10 +387,10 @@ vpce_status vpce_lmhead_backward(const void* hidden, int64_t ld_hidden,
  *                  as vpce_lmhead_backward.  VPCE_NONE requires grad_rows.
  *   workspace      256-byte aligned.  With
  *                  vpce_lmhead_forward_backward_workspace_bytes(s, V, h)
- *                  bytes, chunks are min(4096, s rounded up to 128) rows.
+ *                  bytes, chunks are min(8192, s rounded up to 128) rows.
  *                  Each chunk holds [R, V] fp32 logits and [R, V] bf16 dZ,
- *                  2.1 GB and 1.05 GB at R = 4096, V = 128256, plus 32 MiB of
- *                  cuBLAS scratch.  A smaller workspace gives chunks smaller
+ *                  4.2 GB and 2.1 GB at R = 8192, V = 128256 (rows padded
+ *                  per shard).  A smaller workspace gives chunks smaller
  *                  by steps of 128 rows; less than 128 rows' worth returns
  *                  VPCE_ERR_WORKSPACE.  The workspace starts with the loss
  *                  header: vpce_read_error_flag works on it.
@@ -426,7 +461,8 @@ vpce_status vpce_embedding_backward(const void* grad_out, vpce_dtype grad_dtype,
 
 /*
  * Synchronise `stream`, then copy the workspace error flag to *flag (bit 0:
- * bad target seen by the last forward; bit 1: a device wait timed out).
+ * bad target seen by the last forward; bit 1: a device wait timed out, in
+ * which case the forward's loss is NaN).
  */
 vpce_status vpce_read_error_flag(const void* workspace, int* flag, vpce_stream_t stream);
 

@@ -53,6 +53,7 @@ __all__ = [
     "dlogits",
     "split_columns",
     "shard_partials",
+    "fold_partials",
     "combine_sharded",
     "lmhead_logits",
     "lmhead_backward",
@@ -330,6 +331,20 @@ def shard_partials(z_shard: np.ndarray, y: np.ndarray, vocab_lo: int, vocab_hi: 
     rows = np.nonzero(mine)[0]
     tgt[rows] = z_shard[rows, y[rows] - vocab_lo]
     return m, se, tgt
+
+
+def fold_partials(ms: np.ndarray, ses: np.ndarray):
+    """Several cards' (max, sum exp) pairs of one row set merged into the
+    pair of their union of columns, the first and third steps of the pages'
+    combine without the logarithm: M = max_i m_i, S = sum_i se_i exp(m_i - M).
+    ``ms``, ``ses``: [cards, rows].  Returns ``(M, S)``; the pair equals
+    :func:`shard_partials` of the concatenated columns up to rounding, which
+    is what lets a process send one pair per row for all of its shards."""
+    ms = np.asarray(ms, dtype=np.float64)
+    ses = np.asarray(ses, dtype=np.float64)
+    M = ms.max(axis=0)
+    S = (ses * np.exp(ms - M[None, :])).sum(axis=0)
+    return M, S
 
 
 def combine_sharded(partials, y: np.ndarray, V: int, ignore_index: int = -100):

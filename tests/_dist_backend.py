@@ -21,6 +21,11 @@ class OracleBackend:
             tgt += tg
         return torch.tensor(np.stack(part)), torch.tensor(tgt)
 
+    def fold(self, part, stream=None):
+        p = part.numpy()
+        m, se = O.fold_partials(p[:, :, 0], p[:, :, 1])
+        return torch.tensor(np.stack([m, se], axis=1)[None])
+
     def combine(self, part, tgt, V, targets, ignore_index, reduction, t_local, workspace, stream=None):
         y = targets.numpy()
         p = part.numpy()

@@ -219,8 +219,9 @@ def _lmhead_fb(lib, **kw):
     (dict(grad_hidden=None), 1),
     (dict(hidden=ctypes.c_void_p(FAKE + 8)), 2),
     (dict(grad_weights=[FAKE + 8, FAKE + 4096]), 2),  # fp32 gradient shards are 16-byte aligned
+    (dict(ld_grad_weight=130), 2),                    # ... and so are their rows (TMA tile reductions)
     (dict(ws=ctypes.c_void_p(FAKE + 64)), 2),
-    (dict(ws_bytes=1 << 20), 4),                      # less than one 128-row chunk
+    (dict(ws_bytes=1 << 16), 4),                      # less than one 128-row chunk
 ])
 def test_lmhead_forward_backward_rejects_bad_arguments(lib, kw, code):
     assert _lmhead_fb(lib, **kw) == code
@@ -230,10 +231,10 @@ def test_lmhead_forward_backward_workspace_size(lib):
     f = lib.vpce_lmhead_forward_backward_workspace_bytes
     r256 = lambda n: (n + 255) // 256 * 256  # noqa: E731
     s, V, h = 8192, 128256, 8192
-    R = 4096
+    R = 8192
     ld = (V + 7) // 8 * 8 + 8 * 64  # the padded row's bound: each shard's columns start at a multiple of 8
     want = (256 + 2 * r256(4 * s) + r256(8 * 256 * R) + r256(4 * R) + r256(4 * R * ld)
-            + r256(2 * R * ld) + r256(4 * R * h) + (32 << 20))
+            + r256(2 * R * ld))
     assert f(s, V, h) == want
     assert f(300, 5000, 512) < f(8192, 5000, 512)   # chunks no larger than the batch (rounded to 128)
     assert f(-1, V, h) == 0 and f(s, 0, h) == 0

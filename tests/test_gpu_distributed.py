@@ -1,8 +1,8 @@
 """GPU parity of the local steps of the multi-process path (vpce_partials,
-vpce_combine_partials, vpce_backward on one process's part of the
-vocabulary), with two ranks played in one process: the exchange is done
-here (concatenate the partials in rank order, sum the target logits), as the
-collectives would; no kernel waits on another."""
+vpce_fold_partials, vpce_combine_partials, vpce_backward on one process's
+part of the vocabulary), with two ranks played in one process: the exchange
+is done here (concatenate each rank's folded pairs in rank order, sum the
+target logits), as the collectives would; no kernel waits on another."""
 import numpy as np
 import pytest
 import torch
@@ -46,7 +46,15 @@ def test_two_ranks_in_one_process(name, s, split):
         ws = be.new_workspace(len(dev), s, "cuda")
         part, tgt = be.partials(dev, vs, y, w.ignore_index, ws)
         per_rank.append((vs, dev, ws, part, tgt))
-    gathered = torch.cat([r[3] for r in per_rank], dim=0)
+    folded = [be.fold(r[3]) for r in per_rank]
+    # one (max, sum exp) pair per row and rank: what the all-gather moves
+    assert all(f.shape == (1, s, 2) for f in folded)
+    ref_fold = [O.fold_partials(r[3][:, :, 0].double().cpu().numpy(), r[3][:, :, 1].double().cpu().numpy())
+                for r in per_rank]
+    for f, (M, S) in zip(folded, ref_fold):
+        np.testing.assert_array_equal(f[0, :, 0].cpu().numpy(), M.astype(np.float32))
+        np.testing.assert_allclose(f[0, :, 1].double().cpu().numpy(), S, rtol=1e-5)
+    gathered = torch.cat(folded, dim=0)
     tgt_sum = per_rank[0][4] + per_rank[1][4]
     losses = []
     for vs, dev, ws, part, tgt in per_rank:

@@ -141,3 +141,22 @@ def test_fused_paired_rows_uneven_shards(vs):
     w = synth.Workload("paired", 15, 36, vs[-1], len(vs) - 1, "bf16", 2.0, "uniform", ignore_frac=0.1)
     assert vpce.vpce_fused_plan(vpce.VPCE_BF16, vs, w.s)["cluster"] == 2
     check_full(run_full(w, vocab_start=vs, path="fused"))
+
+
+@pytest.mark.parametrize("name", ["s8192_v128256", "s16384_v152064", "s32768_v256000"])
+@pytest.mark.parametrize("t", [1, 2, 4, 8, 16])
+def test_fused_several_rows_per_cta(name, t):
+    # the persistent grid at its full width with three or four rows per CTA
+    # (or CTA pair), so that the credit flow carries the stats pass across
+    # row boundaries at the workload's own row length; every element is
+    # checked against the oracle
+    w = W[name]
+    if w.V % t:
+        pytest.skip("t does not divide V")
+    vs = synth.even_vocab_start(w.V, t)
+    dt = vpce.VPCE_BF16 if w.dtype == "bf16" else vpce.VPCE_FP32
+    plan = vpce.vpce_fused_plan(dt, vs, w.s)
+    units = plan["grid"] // plan["cluster"]
+    s = 3 * units + 7
+    assert vpce.vpce_fused_plan(dt, vs, s)["grid"] == plan["grid"]
+    check_full(run_full(w, t=t, s=s, path="fused"))

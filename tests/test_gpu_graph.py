@@ -105,7 +105,7 @@ def test_lmhead_and_embedding_replay_identically():
     dx = torch.empty_like(x)
     dw = [torch.zeros(sh.shape, dtype=torch.float32, device="cuda") for sh in wsh]
     bwk = torch.empty(vpce.vpce_lmhead_backward_workspace_bytes(m.V, m.h), dtype=torch.uint8, device="cuda")
-    # the one-call training step: prologue, logits-keeping GEMM, row kernel, cuBLAS, loss sum
+    # the one-call training step: prologue, logits-keeping GEMM, row kernel, dX and dW products, loss sum
     loss2 = torch.empty((), dtype=torch.float32, device="cuda")
     dx2 = torch.empty_like(x)
     dw2 = [torch.zeros(sh.shape, dtype=torch.float32, device="cuda") for sh in wsh]

@@ -177,23 +177,27 @@ def _bwd_bound(dz, mat, ref, K):
     return a + 2.0 ** -8 * (np.abs(ref) + a) + 1e-30
 
 
+def _padded_ld(V):
+    # each shard's columns padded to a multiple of 8, at most 64 shards
+    return (V + 7) // 8 * 8 + 8 * 64
+
+
 def _bwd_workspace(V, h, rows):
-    """Backward workspace sized for chunks of `rows` rows (forces several chunks)."""
+    """Backward workspace sized for chunks of `rows` rows (forces several
+    chunks): the chunk's bf16 dZ, rows padded per shard."""
     r256 = lambda n: (n + 255) // 256 * 256  # noqa: E731
-    blas = 32 << 20  # cuBLAS scratch at the end of the workspace
-    return torch.empty(r256(rows * ((V + 7) // 8 * 8) * 2) + r256(rows * h * 4) + blas, dtype=torch.uint8,
-                       device="cuda")
+    return torch.empty(r256(rows * _padded_ld(V) * 2), dtype=torch.uint8, device="cuda")
 
 
 def _train_workspace(s, V, h, rows):
     """vpce_lmhead_forward_backward workspace for chunks of `rows` rows:
     header, logsumexp and row losses of the batch, then per chunk the column
     groups' partials, target logits, fp32 logits and bf16 dZ (rows padded per
-    shard), fp32 dX and the cuBLAS scratch."""
+    shard)."""
     r256 = lambda n: (n + 255) // 256 * 256  # noqa: E731
-    ld = (V + 7) // 8 * 8 + 8 * 64  # each shard's columns padded to a multiple of 8
+    ld = _padded_ld(V)
     size = (256 + 2 * r256(4 * s) + r256(8 * 256 * rows) + r256(4 * rows) + r256(4 * rows * ld)
-            + r256(2 * rows * ld) + r256(4 * rows * h) + (32 << 20))
+            + r256(2 * rows * ld))
     return torch.empty(size, dtype=torch.uint8, device="cuda")
 
 
@@ -248,7 +252,7 @@ def _check_backward(m, vs=None, *, reduction="mean", grad=1.0, grad_rows=None, c
         got_w = dw[i].cpu().numpy().astype(np.float64) - 0.5
         dzi = dz[:, vs[i]:vs[i + 1]]
         # plus one fp32 rounding of the accumulation onto 0.5 per row chunk
-        rows = chunk_rows or 4096
+        rows = chunk_rows or 8192
         chunks = (m.s + rows - 1) // rows
         bw = _bwd_bound(dzi.T, X, np.zeros_like(ref_w[i]), min(m.s, rows)) + chunks * 2.0 ** -24 * (0.5 + np.abs(ref_w[i]))
         assert np.all(np.abs(got_w - ref_w[i]) <= bw), (i, np.max(np.abs(got_w - ref_w[i]) / bw))

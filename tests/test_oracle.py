@@ -349,6 +349,45 @@ def test_pages_combine_equals_unsharded(V, t):
     assert mean == pytest.approx(ref["loss"], rel=1e-12)
 
 
+@pytest.mark.parametrize("t,ranks", [(2, 1), (4, 2), (8, 2), (8, 4), (16, 8)])
+def test_fold_equals_partials_of_the_union(t, ranks):
+    # a rank's t / ranks shards folded to one pair per row is the pair of its
+    # whole column range computed directly: max over the union, then the sum
+    # of exp(z - max) over the union (no partials involved)
+    V, s = 4000, 7
+    z, y = _rand_case(s, V, scale=3.0)
+    z[0, 3] += 30.0            # a spike in the first shard of rank 0
+    z[1, V // ranks - 1] += 30.0  # a spike in the last shard of rank 0
+    z[2, V - 2] += 30.0        # a spike in the last rank's last shard
+    vs = [(i * V) // t for i in range(t + 1)]
+    per = t // ranks
+    folded = []
+    for r in range(ranks):
+        lo, hi = vs[r * per], vs[(r + 1) * per]
+        parts = [O.shard_partials(z[:, vs[i]:vs[i + 1]], y, vs[i], vs[i + 1]) for i in range(r * per, (r + 1) * per)]
+        M, S = O.fold_partials(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+        block = z[:, lo:hi]
+        M_ref = block.max(axis=1)
+        S_ref = np.array([math.fsum(np.exp(block[k] - M_ref[k])) for k in range(s)])
+        np.testing.assert_array_equal(M, M_ref)
+        np.testing.assert_allclose(S, S_ref, rtol=1e-13)
+        tgt = sum(p[2] for p in parts)
+        folded.append((M, S, tgt))
+    # the ranks' folded pairs combined as the pages combine the cards' pairs
+    lse, row_loss, mean = O.combine_sharded(folded, y, V)
+    ref = O.cross_entropy(z, y)
+    np.testing.assert_allclose(lse, ref["lse"], rtol=1e-12)
+    assert mean == pytest.approx(ref["loss"], rel=1e-12)
+
+
+def test_fold_of_one_card_is_the_identity():
+    m = np.array([[1.5, -2.0, 40.0]])
+    se = np.array([[3.0, 1.0, 7.25]])
+    M, S = O.fold_partials(m, se)
+    np.testing.assert_array_equal(M, m[0])
+    np.testing.assert_array_equal(S, se[0])
+
+
 def test_assemble_roundtrip_with_padding():
     z = RNG.normal(size=(4, 23)).astype(np.float32)
     vs = [0, 5, 6, 23]

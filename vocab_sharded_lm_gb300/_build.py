@@ -26,12 +26,11 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas"
 
 LIBS = {
     "libvpce.so": ["vpce_api.cu", "vpce_forward.cu", "vpce_backward.cu", "vpce_fused.cu", "vpce_static.cu",
-                   "vpce_gemm.cu", "vpce_embed.cu", "vpce_lmhead_bwd.cu"],
+                   "vpce_gemm.cu", "vpce_gemm_bwd.cu", "vpce_embed.cu", "vpce_lmhead_bwd.cu"],
     "libvpce_synth.so": ["synth_gen.cu"],
 }
-HEADERS = ["vpce_device.cuh", "vpce_kernels.cuh", "vpce_chunk.cuh"]
-# the LM-head backward's two plain GEMMs (dX, dW) go through cuBLAS
-LINK = {"libvpce.so": ["-lcublas"]}
+HEADERS = ["vpce_device.cuh", "vpce_kernels.cuh", "vpce_chunk.cuh", "vpce_tc.cuh"]
+LINK: dict[str, list[str]] = {}
 
 
 def _nvcc() -> str:

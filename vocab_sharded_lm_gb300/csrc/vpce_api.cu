@@ -19,7 +19,9 @@ int fused_grid(long long s, int sms, bool pair);
 void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long long V, const long long* targets,
                          long long ignore_index, int reduction, float grad, const float* grad_rows, float* lse,
                          float* rowl, float* row_loss, float* loss_out, Header* hdr, int sms, cudaStream_t st);
+void launch_fold(const float2* part, int t, long long s, float2* out, cudaStream_t st);
 cudaError_t set_gemm_smem();
+cudaError_t set_gemm_bwd_smem();
 cudaError_t set_embed_smem();
 size_t lmhead_bwd_workspace_bytes(long long V, long long h);
 size_t lmhead_bwd_min_workspace_bytes(long long V, long long h);
@@ -86,7 +88,7 @@ vpce_status device_setup(int* sms) {
     if (major != 10 || minor != 3) {
       d.status = VPCE_ERR_UNSUPPORTED_DEVICE;
     } else if (set_stats_smem() != cudaSuccess || set_backward_smem() != cudaSuccess ||
-               set_fused_smem() != cudaSuccess || set_gemm_smem() != cudaSuccess ||
+               set_fused_smem() != cudaSuccess || set_gemm_smem() != cudaSuccess || set_gemm_bwd_smem() != cudaSuccess ||
                set_embed_smem() != cudaSuccess) {
       cudaGetLastError();
       return VPCE_ERR_CUDA;
@@ -148,6 +150,16 @@ vpce_status check_workspace(const void* ws, size_t bytes, int t, int64_t s) {
 int stream_grid(int sms, long long units) {
   const long long want = (units + kWarps - 1) / kWarps;
   return int(want < sms ? (want > 0 ? want : 1) : sms);
+}
+
+// Stream-ordered clear of a workspace header's first 16 bytes (n_valid,
+// error flag, ticket, reduction).  A memset, not an allocation.
+vpce_status clear_header(void* hdr, cudaStream_t cs) {
+  if (cudaMemsetAsync(hdr, 0, 16, cs) != cudaSuccess) {
+    cudaGetLastError();
+    return VPCE_ERR_CUDA;
+  }
+  return VPCE_OK;
 }
 
 vpce_status launch_status() {
@@ -244,6 +256,9 @@ vpce_status vpce_forward(const void* const* shards, vpce_dtype dtype, int t, int
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   Header* hdr = reinterpret_cast<Header*>(ws);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // n_valid, the error flag and the combine's ticket start at zero, cleared
+  // in stream order before any block may set a flag bit
+  if ((st = clear_header(hdr, cs)) != VPCE_OK) return st;
 
   if (s > 0) {
     StatsParams p;
@@ -449,6 +464,7 @@ vpce_status vpce_lmhead_forward(const void* hidden, int64_t ld_hidden, const voi
   // partials go where the sharded loss keeps them, [groups][s] (the layout of
   // WsLayout(VPCE_LMHEAD_MAX_GROUPS, s) holds up to that many groups)
   const WsLayout L(VPCE_LMHEAD_MAX_GROUPS, s);
+  if ((st = clear_header(hdr, cs)) != VPCE_OK) return st;
   if (s > 0) {
     const int g_sms = sms < VPCE_LMHEAD_MAX_GROUPS ? sms : VPCE_LMHEAD_MAX_GROUPS;
     if (!launch_gemm_stats(hidden, ldx, weight_shards, ldw, t, s, h, reinterpret_cast<const long long*>(vocab_start),
@@ -498,6 +514,7 @@ vpce_status vpce_partials(const void* const* shards, vpce_dtype dtype, int t, in
     cudaGetLastError();
     return VPCE_ERR_CUDA;
   }
+  if ((st = clear_header(workspace, cs)) != VPCE_OK) return st;
   StatsParams p;
   p.sh = sh;
   p.s = s;
@@ -510,6 +527,19 @@ vpce_status vpce_partials(const void* const* shards, vpce_dtype dtype, int t, in
   const int grid = stream_grid(sms, p.units);
   if (dtype == VPCE_BF16) launch_stats<__nv_bfloat16>(p, grid, cs);
   else launch_stats<float>(p, grid, cs);
+  return launch_status();
+}
+
+vpce_status vpce_fold_partials(const float* part, int t, int64_t s, float* out, vpce_stream_t stream) {
+  if (t < 1 || t > VPCE_MAX_SHARDS || s < 0 || s > (int64_t(1) << 31)) return VPCE_ERR_INVALID_ARG;
+  if (s > 0 && (part == nullptr || out == nullptr)) return VPCE_ERR_INVALID_ARG;
+  if ((part != nullptr && !aligned(part, 8)) || (out != nullptr && !aligned(out, 8))) return VPCE_ERR_ALIGNMENT;
+  int sms = 0;
+  vpce_status st = device_setup(&sms);
+  if (st != VPCE_OK) return st;
+  if (s == 0) return VPCE_OK;
+  launch_fold(reinterpret_cast<const float2*>(part), t, s, reinterpret_cast<float2*>(out),
+              reinterpret_cast<cudaStream_t>(stream));
   return launch_status();
 }
 
@@ -530,10 +560,7 @@ vpce_status vpce_combine_partials(const float* part, int n_part, const float* tg
   if ((st = device_setup(&sms)) != VPCE_OK) return st;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // a fresh header: n_valid, error flag and ticket start at zero
-  if (cudaMemsetAsync(workspace, 0, 16, cs) != cudaSuccess) {
-    cudaGetLastError();
-    return VPCE_ERR_CUDA;
-  }
+  if ((st = clear_header(workspace, cs)) != VPCE_OK) return st;
   const WsLayout L(t_local, s);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   CombineParams c;
@@ -586,7 +613,10 @@ vpce_status vpce_lmhead_backward(const void* hidden, int64_t ld_hidden, const vo
     for (int i = 0; i < t; ++i)
       if (weight_shards[i] == nullptr || grad_weight_shards[i] == nullptr) return VPCE_ERR_INVALID_ARG;
   }
-  if ((hidden != nullptr && !aligned(hidden, 16)) || (ldx * 2) % 16 != 0 || (ldw * 2) % 16 != 0)
+  // the tensor-memory-access engine reads X, W_i and adds into dW_i: 16-byte
+  // aligned bases and row strides
+  if ((hidden != nullptr && !aligned(hidden, 16)) || (ldx * 2) % 16 != 0 || (ldw * 2) % 16 != 0 ||
+      (ldgw * 4) % 16 != 0)
     return VPCE_ERR_ALIGNMENT;
   for (int i = 0; i < t; ++i) {
     if (weight_shards[i] != nullptr && !aligned(weight_shards[i], 16)) return VPCE_ERR_ALIGNMENT;
@@ -646,7 +676,10 @@ vpce_status vpce_lmhead_forward_backward(const void* hidden, int64_t ld_hidden, 
     for (int i = 0; i < t; ++i)
       if (weight_shards[i] == nullptr || grad_weight_shards[i] == nullptr) return VPCE_ERR_INVALID_ARG;
   }
-  if ((hidden != nullptr && !aligned(hidden, 16)) || (ldx * 2) % 16 != 0 || (ldw * 2) % 16 != 0)
+  // the tensor-memory-access engine reads X, W_i and adds into dW_i: 16-byte
+  // aligned bases and row strides
+  if ((hidden != nullptr && !aligned(hidden, 16)) || (ldx * 2) % 16 != 0 || (ldw * 2) % 16 != 0 ||
+      (ldgw * 4) % 16 != 0)
     return VPCE_ERR_ALIGNMENT;
   for (int i = 0; i < t; ++i) {
     if (weight_shards[i] != nullptr && !aligned(weight_shards[i], 16)) return VPCE_ERR_ALIGNMENT;

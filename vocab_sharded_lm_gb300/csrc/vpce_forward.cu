@@ -60,10 +60,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1) partial_stats_kernel(const __g
   unsigned char* ring = smem + size_t(warp) * kStages * kChunk;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + size_t(kWarps) * kStages * kChunk) + warp * kStages;
 
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    p.hdr->ticket = 0u;
-    p.hdr->error_flag = 0;
-  }
   const long long nw = (long long)gridDim.x * kWarps;
   const long long gw = (long long)blockIdx.x * kWarps + warp;
   const long long u0 = p.units * gw / nw;
@@ -189,6 +185,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   const long long r = (long long)blockIdx.x * kCombineThreads + threadIdx.x;
   double v = 0.0;
   int c = 0;
+  // the partial statistics ran before this kernel (stream order); if one of
+  // their waits gave up, the partials are incomplete and every row's loss is NaN
+  const bool timed_out = (__ldcg(&p.hdr->error_flag) & VPCE_FLAG_WAIT_TIMEOUT) != 0;
   if (r < p.s) {
     const long long y = p.targets[r];
     float rl = 0.f, lse = 0.f;
@@ -210,6 +209,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
       }
       lse = M + logf(S);
       rl = lse - p.tgt[r];
+      if (timed_out) rl = lse = __int_as_float(0x7fc00000);
       v = double(rl);
       c = 1;
     }
@@ -241,7 +241,6 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     block_sum(v, c, sv, sc);
   }
   if (threadIdx.x == 0) {
-    if (p.s == 0) p.hdr->error_flag = 0;
     p.hdr->n_valid = c;
     p.hdr->loss_sum = v;
     p.hdr->reduction = p.reduction;
@@ -253,7 +252,29 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   }
 }
 
+// One process's shards folded into one (max, sum exp) pair per row, shards
+// in ascending order with the combine's arithmetic: M = max_i m_i, then
+// S = sum_i se_i exp(m_i - M).  The result is the pair the process's whole
+// vocabulary slice would give as one shard, so a process exchanges one
+// pair per row however many shards it holds.
+__global__ void __launch_bounds__(kCombineThreads) fold_kernel(const float2* part, int t, long long s, float2* out) {
+  const long long r = (long long)blockIdx.x * kCombineThreads + threadIdx.x;
+  if (r >= s) return;
+  float M = -INFINITY;
+  for (int i = 0; i < t; ++i) M = fmaxf(M, part[(long long)i * s + r].x);
+  float S = 0.f;
+  for (int i = 0; i < t; ++i) {
+    const float2 q = part[(long long)i * s + r];
+    S += q.y * expf(q.x - M);
+  }
+  out[r] = make_float2(M, S);
+}
+
 }  // namespace
+
+void launch_fold(const float2* part, int t, long long s, float2* out, cudaStream_t st) {
+  fold_kernel<<<int((s + kCombineThreads - 1) / kCombineThreads), kCombineThreads, 0, st>>>(part, t, s, out);
+}
 
 template <typename T>
 void launch_stats(const StatsParams& p, int grid, cudaStream_t st) {

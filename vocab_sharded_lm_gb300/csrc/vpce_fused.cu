@@ -116,7 +116,16 @@ static_assert(sizeof(FusedSmem) + 1024 <= 232448, "fused kernel shared memory");
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const long long* targets, long long s,
                                                             long long V, long long ignore_index, Header* hdr,
                                                             int reduction, float* loss_out) {
-  grid_launch_dependents();  // the fused kernel's stats warps need nothing from here
+  // The header's error flag and ticket are cleared before the dependent fused
+  // kernel may start, so that a bit it sets (a wait that gave up) is never
+  // overwritten by this clear; the bad-target bit below is OR-ed in.
+  if (threadIdx.x == 0) {
+    hdr->error_flag = 0;
+    hdr->ticket = 0u;
+    __threadfence();
+  }
+  __syncthreads();
+  grid_launch_dependents();  // the fused kernel's stats warps need nothing else from here
   __shared__ int sc[kPrepThreads / 32];
   __shared__ int sbad[kPrepThreads / 32];
   int c = 0, bad = 0;
@@ -143,8 +152,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const long long* tar
       tb |= sbad[i];
     }
     hdr->n_valid = tc;
-    hdr->error_flag = tb ? VPCE_FLAG_BAD_TARGET : 0;
-    hdr->ticket = 0u;
+    if (tb) atomicOr(&hdr->error_flag, VPCE_FLAG_BAD_TARGET);
     hdr->reduction = reduction;
     hdr->loss_sum = 0.0;
     if (s == 0 && loss_out != nullptr) *loss_out = reduction != VPCE_MEAN ? 0.f : __int_as_float(0x7fc00000);
@@ -635,10 +643,14 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     double tot = 0.0;
     for (int i = 0; i < kFThreads / 32; ++i) tot += sv[i];
     const int cnt = p.hdr->n_valid;
+    // a wait that gave up anywhere in the grid leaves rows unfinished: the
+    // loss is then NaN rather than a plausible partial sum
+    const bool timed_out = (atomicOr(&p.hdr->error_flag, 0) & VPCE_FLAG_WAIT_TIMEOUT) != 0;
     p.hdr->loss_sum = tot;
     p.hdr->ticket = 0u;
     if (p.loss_out != nullptr)
-      *p.loss_out = p.reduction != VPCE_MEAN ? float(tot)
+      *p.loss_out = timed_out ? __int_as_float(0x7fc00000)
+                  : p.reduction != VPCE_MEAN ? float(tot)
                                              : (cnt > 0 ? float(tot / double(cnt)) : __int_as_float(0x7fc00000));
   }
 }

@@ -37,11 +37,10 @@
 // the longer ranges evenly over the groups.  Each CTA writes one partial per
 // row for its range; the combine kernel of the sharded loss folds them in
 // range order, i.e. in vocabulary order.
-#include <cuda.h>
-
 #include <cstring>
 
 #include "vpce_kernels.cuh"
+#include "vpce_tc.cuh"
 
 namespace vpce {
 
@@ -92,8 +91,9 @@ struct GemmParams {
   const float* lse;                 // [s] logsumexp of the forward
   const float* grad_rows;           // [s] per-row upstream gradient, or null
   float grad;                       // upstream gradient g of the reduced loss (grad_rows null)
-  unsigned short* dz;               // [s, ldz] bf16 dlogits, global column c at dz + c
+  unsigned short* dz;               // [s, ldz] bf16 dlogits, shard i's column j at dz + dzcol[i] + j
   long long ldz;
+  int dzcol[kMaxGemmShards + 1];
   // logits-keeping epilogue only: shard i's fp32 logits [s, w_i], box 32 x 32
   CUtensorMap tmz[kMaxGemmShards];
 };
@@ -111,103 +111,11 @@ constexpr int kZWarpBytes = 2 * 4096;
 constexpr int kZSmem = kZStageOff + 4 * kZWarpBytes;
 static_assert(kZSmem <= 232448, "logits staging fits the shared memory of a CTA");
 
-// ---------------------------------------------------------------------------
-// inline PTX: TMA tiles, tcgen05
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-          "r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
-}
+using namespace tc;
 
-// shared -> global tile store (bulk group of the issuing thread)
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(smem_addr(src))
-               : "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major tile stored as 128-byte rows
-// with the 128-byte swizzle: start address, stride of 8-row groups 1024 B,
-// descriptor version 1, layout type 2 (128B swizzle).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= uint64_t((saddr >> 4) & 0x3FFFu);
-  d |= uint64_t(1u) << 16;             // leading byte offset (unused for swizzled K-major)
-  d |= uint64_t(1024u >> 4) << 32;     // stride byte offset
-  d |= uint64_t(1u) << 46;             // version
-  d |= uint64_t(2u) << 61;             // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N = kBN, M = kBM.
-constexpr uint32_t kIdesc = (1u << 4)                       // D format f32
-                            | (1u << 7)                     // A bf16
-                            | (1u << 10)                    // B bf16
-                            | (uint32_t(kBN >> 3) << 17)    // N / 8
-                            | (uint32_t(kBM >> 4) << 24);   // M / 16
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.  The load and its
-// wait sit in one asm statement, so no use of the registers can be scheduled
-// before the data has arrived.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-}
-
-__device__ __forceinline__ int ld_abort(const int* f) { return *const_cast<const volatile int*>(f); }
-
-// Single-thread bounded wait that also gives up once another role aborted.
-__device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t parity, const int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (ld_abort(abort_flag) || clock64() - t0 > kWaitLimitCycles) return false;
-  }
-}
-
-// Warp-uniform bounded wait with the same abort check.
-__device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t parity, const int* abort_flag) {
-  if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
-  const long long t0 = clock64();
-  for (;;) {
-    if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
-    if (__any_sync(kFull, ld_abort(abort_flag) != 0 || clock64() - t0 > kWaitLimitCycles)) return false;
-  }
-}
+// Instruction descriptor of the logits product: M = kBM, N = kBN, X and W_i
+// both K-major.
+constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN, false, false);
 
 __device__ __forceinline__ int shard_of_tile(const GemmParams& p, int nt) {
   int i = 0;
@@ -273,7 +181,7 @@ __device__ __forceinline__ void epi_row_tile(const GemmParams& p, EpiRow& e, uin
         w[j / 2] = pack_bf16x2(d0, d1);
       }
       if (e.live) {
-        const long long col = (long long)p.vstart[sh] + col0 + c * 32;
+        const long long col = (long long)p.dzcol[sh] + col0 + c * 32;
         unsigned short* dst = p.dz + (long long)e.r * p.ldz + col;
         if (lim == 32 && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
           uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -297,22 +205,26 @@ __device__ __forceinline__ void epi_row_tile(const GemmParams& p, EpiRow& e, uin
       if constexpr (EPI == kEpiStatsZ) {
         // this warp's 32 rows x 32 columns through shared memory to the
         // shard's kept logits; TMA clips columns past the shard and rows
-        // past the chunk
-        unsigned char* zb = zbuf + (zc & 1u) * 4096u;
-        if (lane == 0 && zc >= 2) bulk_wait_read<1>();  // the store of chunk zc - 2 has read zb
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<float4*>(zb + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
+        // past the chunk.  A warp whose rows all lie past the chunk stages
+        // nothing (warp-uniform), so that zc counts exactly the stores
+        // issued and the buffer-reuse wait below covers the right one.
         const int zy = mt * kBM + q * 32;
-        if (lane == 0 && zy < p.s) {
-          tma_store_2d(&p.tmz[sh], zb, col0 + c * 32, zy);
-          bulk_commit();
+        if (zy < p.s) {
+          unsigned char* zb = zbuf + (zc & 1u) * 4096u;
+          if (lane == 0 && zc >= 2) bulk_wait_read<1>();  // the store of chunk zc - 2 has read zb
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(zb + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.tmz[sh], zb, col0 + c * 32, zy);
+            bulk_commit();
+          }
+          ++zc;
         }
-        ++zc;
       }
       if (rel >= 0 && rel < 32 && rel < lim) {
         // the target logit: a sum of products with 0/1 weights picks it
@@ -383,16 +295,9 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
-    if (EPI == kEpiStats && blockIdx.x == 0) {
-      p.hdr->ticket = 0u;
-      p.hdr->error_flag = 0;
-    }
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem_base)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tmem_alloc(&sm.tmem_base, kTmemCols);
   }
   tc_fence_before();
   __syncthreads();
@@ -476,7 +381,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
               const uint64_t bdesc = sw128_desc(b0 + kk * kUK * 2);
 #pragma unroll
               for (int j = 0; j < kMT; ++j)
-                umma_bf16(tmem + uint32_t(j * kBN), sw128_desc(a0 + j * kATile + kk * kUK * 2), bdesc,
+                umma_bf16(tmem + uint32_t(j * kBN), sw128_desc(a0 + j * kATile + kk * kUK * 2), bdesc, kIdesc,
                           (kb | kk) != 0);
             }
             issued_any = 1;
@@ -548,56 +453,13 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_stats_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   if (warp == 1)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
-}
-
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against the driver library; resolved once).
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess) {
-      cudaGetLastError();
-      f = nullptr;
-    }
-    return reinterpret_cast<EncodeTiledFn>(f);
-  }();
-  return fn;
-}
-
-// A [rows, cols] fp32 row-major matrix (row stride ld elements) as a 2-D
-// tensor map with a box of 32 x 32 and the 128-byte swizzle (TMA stores of
-// the kept logits).
-bool make_map_f32(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
-  const cuuint64_t strides[1] = {cuuint64_t(ld) * 4u};
-  const cuuint32_t box[2] = {32u, 32u};
-  const cuuint32_t estr[2] = {1u, 1u};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    tmem_dealloc(tmem, kTmemCols);
 }
 
 // A [rows, h] bf16 row-major matrix (row stride ld elements) as a 2-D tensor
 // map with a box of 64 columns x box_rows rows and the 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, long long rows, long long h, long long ld, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {cuuint64_t(h), cuuint64_t(rows)};
-  const cuuint64_t strides[1] = {cuuint64_t(ld) * 2u};
-  const cuuint32_t box[2] = {cuuint32_t(kBK), cuuint32_t(box_rows)};
-  const cuuint32_t estr[2] = {1u, 1u};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_map_bf16(m, base, rows, h, ld, kBK, box_rows);
 }
 
 }  // namespace
@@ -682,11 +544,11 @@ bool launch_gemm_stats(const void* x, long long ld_x, const void* const* w, long
 
 // dlogits of rows [0, s) of X (the caller offsets X, targets, lse and
 // grad_rows to a chunk), written as bf16 into dz (row stride ldz elements;
-// global vocabulary column c of a row at dz + c).
+// shard i's column j of a row at dz + zcol[i] + j).
 bool launch_gemm_grad(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
                       long long h, const long long* vocab_start, const long long* targets, long long ignore_index,
                       const float* lse, const float* grad_rows, float grad, unsigned short* dz, long long ldz,
-                      Header* hdr, int sms, cudaStream_t st) {
+                      const long long* zcol, Header* hdr, int sms, cudaStream_t st) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   if (!make_map(&p.tmx, x, s, h, ld_x, kBM)) return false;
@@ -712,6 +574,7 @@ bool launch_gemm_grad(const void* x, long long ld_x, const void* const* w, long 
   p.grad = grad;
   p.dz = dz;
   p.ldz = ldz;
+  for (int i = 0; i <= t; ++i) p.dzcol[i] = int(zcol[i]);
   gemm_stats_kernel<kEpiGrad><<<p.gm * p.gn, kGThreads, sizeof(GemmSmem), st>>>(p);
   return true;
 }

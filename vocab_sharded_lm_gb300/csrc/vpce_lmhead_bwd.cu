@@ -3,17 +3,13 @@
 // The forward never wrote the logits, so the backward forms them again: per
 // chunk of rows, the tensor-core kernel recomputes each logits tile and
 // writes dZ = (softmax - onehot) * g as bf16 (the epilogue uses the
-// forward's logsumexp and n_valid); then two plain GEMMs through cuBLAS give
-//     dX[chunk]  = sum_i dZ_i W_i          (fp32, then rounded to bf16)
-//     dW_i      += dZ_i^T X[chunk]         (fp32, accumulated)
-// The chunk bounds the dZ scratch to rows x V bf16 (1.05 GB for the default
-// 4096 rows at V = 128256; a smaller workspace gives smaller chunks, down to
+// forward's logsumexp and n_valid); then two more tensor-core kernels give
+//     dX[chunk]  = sum_i dZ_i W_i          (fp32 accumulators, bf16 out)
+//     dW_i      += dZ_i^T X[chunk]         (fp32, accumulated at L2)
+// The chunk bounds the dZ scratch to rows x V bf16 (2.1 GB for the default
+// 8192 rows at V = 128256; a smaller workspace gives smaller chunks, down to
 // 128 rows), the "do not assemble the big tensor" of the CMU notes (§5.5)
-// applied to the gradient.  Larger chunks give cuBLAS larger products.
-#include <cublas_v2.h>
-
-#include <mutex>
-
+// applied to the gradient.
 #include "vpce_kernels.cuh"
 
 namespace vpce {
@@ -21,51 +17,41 @@ namespace vpce {
 bool launch_gemm_grad(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
                       long long h, const long long* vocab_start, const long long* targets, long long ignore_index,
                       const float* lse, const float* grad_rows, float grad, unsigned short* dz, long long ldz,
-                      Header* hdr, int sms, cudaStream_t st);
+                      const long long* zcol, Header* hdr, int sms, cudaStream_t st);
 bool launch_gemm_stats(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
                        long long h, const long long* vocab_start, const long long* targets, long long ignore_index,
                        float2* part, float* tgt, Header* hdr, int sms, int* groups, cudaStream_t st, float* zf,
                        long long ldzf, const long long* zcol);
+bool launch_dgrad_x(const unsigned short* dz, long long ldz, const long long* zcol, const void* const* w,
+                    long long ld_w, int t, long long R, long long h, const long long* vs, void* dx, long long ld_dx,
+                    Header* hdr, int sms, cudaStream_t st);
+bool launch_dgrad_w(const unsigned short* dz, long long ldz, const long long* zcol, const void* x, long long ld_x,
+                    int t, long long R, long long h, const long long* vs, float* const* dw, long long ld_dw,
+                    Header* hdr, int sms, cudaStream_t st);
 void launch_prep(const long long* targets, long long s, long long V, long long ignore_index, Header* hdr,
                  int reduction, float* loss_out, cudaStream_t st);
 
 namespace {
 
-constexpr long long kBwdRows = 4096;  // rows per chunk with the suggested workspace
+constexpr long long kBwdRows = 8192;  // rows per chunk with the suggested workspace
 constexpr long long kMinBwdRows = 128;
-// cuBLAS's own scratch, carved from the caller's workspace so that no call
-// allocates (and a stream capture records nothing but kernels).
-constexpr size_t kBlasBytes = size_t(32) << 20;
 
-__global__ void f32_to_bf16_rows(const float* src, long long lds, __nv_bfloat16* dst, long long ldd, long long rows,
-                                 long long cols) {
-  const long long n = rows * cols;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
-    const long long r = e / cols, c = e - r * cols;
-    dst[r * ldd + c] = __float2bfloat16_rn(src[r * lds + c]);
-  }
-}
-
-std::mutex g_blas_mu;
-cublasHandle_t g_blas[64] = {};
-
-cublasHandle_t blas_handle(int dev) {
-  if (dev < 0 || dev >= 64) return nullptr;
-  if (g_blas[dev] == nullptr) {
-    cublasHandle_t hnd = nullptr;
-    if (cublasCreate(&hnd) != CUBLAS_STATUS_SUCCESS) return nullptr;
-    g_blas[dev] = hnd;
-  }
-  return g_blas[dev];
-}
+// The padded row of dZ (and of the kept logits): each shard's columns start
+// at a multiple of 8 (16-byte aligned for the TMA), so a row is at most
+// round8(V) + 8 * VPCE_MAX_SHARDS columns.
+long long padded_ld_bound(long long V) { return (V + 7) / 8 * 8 + 8LL * VPCE_MAX_SHARDS; }
 
 }  // namespace
 
-long long lmhead_bwd_ldz(long long V) { return (V + 7) / 8 * 8; }
+// Each shard's first column in a padded row; returns the row's width.
+long long padded_columns(const long long* vs, int t, long long* zcol) {
+  zcol[0] = 0;
+  for (int i = 0; i < t; ++i) zcol[i + 1] = zcol[i] + (vs[i + 1] - vs[i] + 7) / 8 * 8;
+  return zcol[t];
+}
 
-size_t lmhead_bwd_bytes_for(long long rows, long long V, long long h) {
-  return round256(size_t(rows) * size_t(lmhead_bwd_ldz(V)) * 2u) + round256(size_t(rows) * size_t(h) * 4u) +
-         kBlasBytes;
+size_t lmhead_bwd_bytes_for(long long rows, long long V, long long /*h*/) {
+  return round256(size_t(rows) * size_t(padded_ld_bound(V)) * 2u);
 }
 
 size_t lmhead_bwd_workspace_bytes(long long V, long long h) { return lmhead_bwd_bytes_for(kBwdRows, V, h); }
@@ -79,70 +65,41 @@ long long lmhead_bwd_rows_for(size_t bytes, long long V, long long h) {
   return r;
 }
 
-// The two plain GEMMs of one row chunk of R rows, given its bf16 dZ (shard
-// i's columns from dz + zcol[i], rows of ldz elements):
-//     dX[chunk]  = sum_i dZ_i W_i          (fp32 in dx32, then rounded to bf16)
+// The two products of one row chunk of R rows, given its bf16 dZ (shard i's
+// columns from dz + zcol[i], rows of ldz elements):
+//     dX[chunk]  = sum_i dZ_i W_i          (bf16, written)
 //     dW_i      += dZ_i^T X[chunk]         (fp32, accumulated)
-vpce_status chunk_gemms(cublasHandle_t hb, const void* xr, long long ld_x, const void* const* w, long long ld_w, int t,
-                        long long R, long long h, const long long* vs, const unsigned short* dz, const long long* zcol,
-                        long long ldz,
-                        float* dx32, __nv_bfloat16* dxr, long long ld_dx, float* const* dw, long long ld_dw, int sms,
-                        cudaStream_t st) {
-  const float one = 1.f, zero = 0.f;
-  for (int i = 0; i < t; ++i) {
-    const int wi = int(vs[i + 1] - vs[i]);
-    // column-major: dX^T [h, R] (+)= W_i^T [h, w_i] * dZ_i^T [w_i, R]
-    if (cublasGemmEx(hb, CUBLAS_OP_N, CUBLAS_OP_N, int(h), int(R), wi, &one, w[i], CUDA_R_16BF, int(ld_w),
-                     dz + zcol[i], CUDA_R_16BF, int(ldz), i == 0 ? &zero : &one, dx32, CUDA_R_32F, int(h),
-                     CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-      return VPCE_ERR_CUDA;
-    // column-major: dW_i^T [h, w_i] += X^T [h, R] * dZ_i [R, w_i]
-    if (cublasGemmEx(hb, CUBLAS_OP_N, CUBLAS_OP_T, int(h), wi, int(R), &one, xr, CUDA_R_16BF, int(ld_x),
-                     dz + zcol[i], CUDA_R_16BF, int(ldz), &one, dw[i], CUDA_R_32F, int(ld_dw), CUBLAS_COMPUTE_32F,
-                     CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-      return VPCE_ERR_CUDA;
-  }
-  const long long n = R * h;
-  long long blocks = (n + 255) / 256;
-  if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
-  f32_to_bf16_rows<<<int(blocks), 256, 0, st>>>(dx32, h, dxr, ld_dx, R, h);
+vpce_status chunk_gemms(const void* xr, long long ld_x, const void* const* w, long long ld_w, int t, long long R,
+                        long long h, const long long* vs, const unsigned short* dz, const long long* zcol,
+                        long long ldz, void* dxr, long long ld_dx, float* const* dw, long long ld_dw, Header* hdr,
+                        int sms, cudaStream_t st) {
+  if (!launch_dgrad_x(dz, ldz, zcol, w, ld_w, t, R, h, vs, dxr, ld_dx, hdr, sms, st)) return VPCE_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return VPCE_ERR_CUDA;
+  if (!launch_dgrad_w(dz, ldz, zcol, xr, ld_x, t, R, h, vs, dw, ld_dw, hdr, sms, st)) return VPCE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? VPCE_OK : VPCE_ERR_CUDA;
 }
 
-// Returns VPCE_OK, VPCE_ERR_CUDA (a launch or a cuBLAS call failed).
+// Returns VPCE_OK, VPCE_ERR_CUDA (a launch failed or a tensor map could not
+// be encoded).
 vpce_status lmhead_backward_run(const void* x, long long ld_x, const void* const* w, long long ld_w, int t,
                                 long long s, long long h, const long long* vs, const long long* targets,
                                 long long ignore_index, float grad, const float* grad_rows, const float* lse,
                                 Header* hdr, void* dx, long long ld_dx, float* const* dw, long long ld_dw, void* ws,
                                 size_t ws_bytes, int sms, cudaStream_t st) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return VPCE_ERR_CUDA;
-  }
-  std::lock_guard<std::mutex> lock(g_blas_mu);
-  cublasHandle_t hb = blas_handle(dev);
   const long long V = vs[t];
-  const long long ldz = lmhead_bwd_ldz(V);
   const long long rows = lmhead_bwd_rows_for(ws_bytes, V, h);
+  long long zcol[VPCE_MAX_SHARDS + 1];
+  const long long ldz = padded_columns(vs, t, zcol);
   unsigned short* dz = static_cast<unsigned short*>(ws);
-  unsigned char* dx32_at = static_cast<unsigned char*>(ws) + round256(size_t(rows) * size_t(ldz) * 2u);
-  float* dx32 = reinterpret_cast<float*>(dx32_at);
-  void* blas_ws = dx32_at + round256(size_t(rows) * size_t(h) * 4u);
-  // setting the stream resets cuBLAS to its default workspace pool, so the
-  // caller's slice is installed after it, on every call
-  if (hb == nullptr || cublasSetStream(hb, st) != CUBLAS_STATUS_SUCCESS ||
-      cublasSetWorkspace(hb, blas_ws, kBlasBytes) != CUBLAS_STATUS_SUCCESS)
-    return VPCE_ERR_CUDA;
   for (long long r0 = 0; r0 < s; r0 += rows) {
     const long long R = s - r0 < rows ? s - r0 : rows;
     const unsigned char* xr = static_cast<const unsigned char*>(x) + r0 * ld_x * 2;
     if (!launch_gemm_grad(xr, ld_x, w, ld_w, t, R, h, vs, targets + r0, ignore_index, lse + r0,
-                          grad_rows != nullptr ? grad_rows + r0 : nullptr, grad, dz, ldz, hdr, sms, st))
+                          grad_rows != nullptr ? grad_rows + r0 : nullptr, grad, dz, ldz, zcol, hdr, sms, st))
       return VPCE_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return VPCE_ERR_CUDA;
-    const vpce_status e = chunk_gemms(hb, xr, ld_x, w, ld_w, t, R, h, vs, dz, vs, ldz, dx32,
-                                      static_cast<__nv_bfloat16*>(dx) + r0 * ld_dx, ld_dx, dw, ld_dw, sms, st);
+    const vpce_status e = chunk_gemms(xr, ld_x, w, ld_w, t, R, h, vs, dz, zcol, ldz,
+                                      static_cast<unsigned short*>(dx) + r0 * ld_dx, ld_dx, dw, ld_dw, hdr, sms, st);
     if (e != VPCE_OK) return e;
   }
   return VPCE_OK;
@@ -152,8 +109,8 @@ vpce_status lmhead_backward_run(const void* x, long long ld_x, const void* const
 // Forward and backward in one call (vpce_lmhead_forward_backward): per row
 // chunk the tensor-core kernel writes the loss statistics and keeps the
 // chunk's fp32 logits; one kernel then finishes each row (logsumexp, loss,
-// bf16 dZ from the kept logits) and the two plain GEMMs follow.  No logits
-// are formed twice.
+// bf16 dZ from the kept logits) and the two tensor-core products follow.  No
+// logits are formed twice.
 // ---------------------------------------------------------------------------
 namespace {
 
@@ -278,16 +235,12 @@ __global__ void __launch_bounds__(kLossThreads) train_loss_kernel(const float* r
   }
 }
 
-constexpr long long kTrainRows = 4096;  // rows per chunk with the suggested workspace
+constexpr long long kTrainRows = 8192;  // rows per chunk with the suggested workspace
 constexpr long long kMinTrainRows = 128;
 
-// The padded row of kept logits and dZ: each shard's columns start at a
-// multiple of 8, so a row is at most round8(V) + 8 * 32 columns.
-long long train_ld_bound(long long V) { return (V + 7) / 8 * 8 + 8LL * VPCE_MAX_SHARDS; }
-
 struct TrainLayout {
-  size_t lse, rowl, part, tgt, zf, dz, dx32, blas, total;
-  TrainLayout(long long R, long long s, long long V, long long h) {
+  size_t lse, rowl, part, tgt, zf, dz, total;
+  TrainLayout(long long R, long long s, long long V, long long /*h*/) {
     size_t o = 256;  // header
     lse = o;
     o += round256(size_t(s) * 4u);
@@ -298,13 +251,10 @@ struct TrainLayout {
     tgt = o;
     o += round256(size_t(R) * 4u);
     zf = o;
-    o += round256(size_t(R) * size_t(train_ld_bound(V)) * 4u);
+    o += round256(size_t(R) * size_t(padded_ld_bound(V)) * 4u);
     dz = o;
-    o += round256(size_t(R) * size_t(train_ld_bound(V)) * 2u);
-    dx32 = o;
-    o += round256(size_t(R) * size_t(h) * 4u);
-    blas = o;
-    total = o + kBlasBytes;
+    o += round256(size_t(R) * size_t(padded_ld_bound(V)) * 2u);
+    total = o;
   }
 };
 
@@ -330,7 +280,8 @@ size_t lmhead_train_min_workspace_bytes(long long s, long long V, long long h) {
   return TrainLayout(kMinTrainRows, s, V, h).total;
 }
 
-// Returns VPCE_OK, VPCE_ERR_WORKSPACE, VPCE_ERR_CUDA (a launch or a cuBLAS call failed).
+// Returns VPCE_OK, VPCE_ERR_WORKSPACE, VPCE_ERR_CUDA (a launch failed or a
+// tensor map could not be encoded).
 vpce_status lmhead_train_run(const void* x, long long ld_x, const void* const* w, long long ld_w, int t, long long s,
                              long long h, const long long* vs, const long long* targets, long long ignore_index,
                              int reduction, float grad, const float* grad_rows, float* loss_out, float* row_loss_out,
@@ -346,24 +297,12 @@ vpce_status lmhead_train_run(const void* x, long long ld_x, const void* const* w
   const long long rows = train_rows_for(ws_bytes, s, V, h);
   if (rows == 0) return VPCE_ERR_WORKSPACE;
   const TrainLayout L(rows, s, V, h);
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return VPCE_ERR_CUDA;
-  }
-  std::lock_guard<std::mutex> lock(g_blas_mu);
-  cublasHandle_t hb = blas_handle(dev);
-  if (hb == nullptr || cublasSetStream(hb, st) != CUBLAS_STATUS_SUCCESS ||
-      cublasSetWorkspace(hb, base + L.blas, kBlasBytes) != CUBLAS_STATUS_SUCCESS)
-    return VPCE_ERR_CUDA;
   float* lse = reinterpret_cast<float*>(base + L.lse);
   float* rowl = reinterpret_cast<float*>(base + L.rowl);
   float* zf = reinterpret_cast<float*>(base + L.zf);
   unsigned short* dz = reinterpret_cast<unsigned short*>(base + L.dz);
   long long zcol[VPCE_MAX_SHARDS + 1];  // each shard's first column in a padded row
-  zcol[0] = 0;
-  for (int i = 0; i < t; ++i) zcol[i + 1] = zcol[i] + (vs[i + 1] - vs[i] + 7) / 8 * 8;
-  const long long ld = zcol[t];
+  const long long ld = padded_columns(vs, t, zcol);
   for (long long r0 = 0; r0 < s; r0 += rows) {
     const long long R = s - r0 < rows ? s - r0 : rows;
     const unsigned char* xr = static_cast<const unsigned char*>(x) + r0 * ld_x * 2;
@@ -396,8 +335,8 @@ vpce_status lmhead_train_run(const void* x, long long ld_x, const void* const* w
     q.row_loss = row_loss_out != nullptr ? row_loss_out + r0 : nullptr;
     train_rows_kernel<<<int(R), kRowThreads, 0, st>>>(q);
     if (cudaGetLastError() != cudaSuccess) return VPCE_ERR_CUDA;
-    const vpce_status e = chunk_gemms(hb, xr, ld_x, w, ld_w, t, R, h, vs, dz, zcol, ld, reinterpret_cast<float*>(base + L.dx32),
-                                      static_cast<__nv_bfloat16*>(dx) + r0 * ld_dx, ld_dx, dw, ld_dw, sms, st);
+    const vpce_status e = chunk_gemms(xr, ld_x, w, ld_w, t, R, h, vs, dz, zcol, ld,
+                                      static_cast<unsigned short*>(dx) + r0 * ld_dx, ld_dx, dw, ld_dw, hdr, sms, st);
     if (e != VPCE_OK) return e;
   }
   train_loss_kernel<<<1, kLossThreads, 0, st>>>(rowl, s, hdr, loss_out);

@@ -58,8 +58,10 @@ extern "C" vpce_status vpce_forward_static(const void* const* shards, vpce_dtype
   void* scratch = nullptr;
   const vpce_status st = static_scratch_address(&scratch);
   if (st != VPCE_OK) return st;
-  // The kernels clear the scratch header (batch counter, error flag) at the
-  // start of every call; everything else is written before it is read.
+  // vpce_forward clears the scratch header (batch counter, error flag) in
+  // stream order at the start of every call; everything else is written
+  // before it is read.  A wait that gave up makes the loss NaN, so a caller
+  // without access to the error flag still sees the failure.
   return vpce_forward(shards, dtype, t, s, vocab_start, ld, targets, ignore_index, reduction, loss_out,
                       row_loss_out, scratch, size_t(VPCE_STATIC_SCRATCH_BYTES), stream);
 }

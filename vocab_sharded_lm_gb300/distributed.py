@@ -6,14 +6,17 @@ slice; it reduces them to three scalars per row (maximum, sum of exponentials,
 target logit when it holds the target), the cards exchange those scalars, and
 every card finishes the loss and computes its own slice's gradient locally.
 
-Here the exchange is one all-gather of the per-row (max, sum exp) pairs (8
-bytes per row and local shard) and one all-reduce (sum) of the target logits
-(4 bytes per row, exact: one rank contributes per row).  The gathered pairs
-are folded in rank order, so every rank computes the same logsumexp, loss and
+Here each rank first folds its own shards' partials into one (max, sum exp)
+pair per row, so the exchange is the pages' three scalars per token
+whatever the number of local shards: one all-gather of the folded pairs (8
+bytes per row and rank) and one all-reduce (sum) of the target logits (4
+bytes per row, exact: one rank contributes per row).  The gathered pairs are
+folded in rank order, so every rank computes the same logsumexp, loss and
 n_valid; the backward then needs no communication.
 
 The local steps run in the library's kernels (``vpce_partials``,
-``vpce_combine_partials``, ``vpce_backward``) through :class:`CudaBackend`;
+``vpce_fold_partials``, ``vpce_combine_partials``, ``vpce_backward``) through
+:class:`CudaBackend`;
 the collectives are ``torch.distributed`` (NCCL on GPUs).  A backend is any
 object with the three methods below, which is how the orchestration is
 exercised on CPU ranks.
@@ -45,6 +48,18 @@ class CudaBackend:
         if code != vpce.VPCE_OK:
             raise vpce.VPCEError(code, "vpce_partials")
         return part, tgt
+
+    def fold(self, part, stream=None):
+        """[t, s, 2] partials -> [1, s, 2], shards folded in order."""
+        import torch
+
+        t, s = int(part.shape[0]), int(part.shape[1])
+        out = torch.empty((1, s, 2), dtype=torch.float32, device=part.device)
+        code = int(vpce.load_library().vpce_fold_partials(ctypes.c_void_p(part.data_ptr()), t, s,
+                                                           ctypes.c_void_p(out.data_ptr()), vpce._stream_ptr(stream)))
+        if code != vpce.VPCE_OK:
+            raise vpce.VPCEError(code, "vpce_fold_partials")
+        return out
 
     def combine(self, part, tgt, V, targets, ignore_index, reduction, t_local, workspace, stream=None):
         import torch
@@ -89,10 +104,12 @@ def forward(shards, vocab_start, targets, V, *, group=None, ignore_index: int = 
     if workspace is None:
         workspace = be.new_workspace(t_local, s, targets.device)
     part, tgt = be.partials(shards, vocab_start, targets, ignore_index, workspace)
+    # one (max, sum exp) pair per row for this rank's whole vocabulary slice
+    mine = be.fold(part)
     world = dist.get_world_size(group)
-    pieces = [torch.empty_like(part) for _ in range(world)]
-    dist.all_gather(pieces, part.contiguous(), group=group)
-    # rank-major order: the combine folds rank 0's shards first, then rank 1's, ...
+    pieces = [torch.empty_like(mine) for _ in range(world)]
+    dist.all_gather(pieces, mine.contiguous(), group=group)
+    # rank order: the combine folds rank 0's pair first, then rank 1's, ...
     gathered = torch.cat(pieces, dim=0)
     dist.all_reduce(tgt, op=dist.ReduceOp.SUM, group=group)
     loss, row_loss = be.combine(gathered, tgt, V, targets, ignore_index, reduction, t_local, workspace)

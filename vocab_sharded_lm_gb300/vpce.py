@@ -80,6 +80,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.vpce_forward_static.restype = ctypes.c_int
         lib.vpce_forward_static.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64,
                                             ctypes.c_int, _P, _P, _P]
+        lib.vpce_partials.restype = ctypes.c_int
+        lib.vpce_partials.argtypes = [_P, ctypes.c_int, ctypes.c_int, _I64, _I64P, _I64, _P, _I64, _P, _P, _P,
+                                      ctypes.c_size_t, _P]
+        lib.vpce_combine_partials.restype = ctypes.c_int
+        lib.vpce_combine_partials.argtypes = [_P, ctypes.c_int, _P, _I64, _I64, _P, _I64, ctypes.c_int, _P, _P,
+                                              ctypes.c_int, _P, ctypes.c_size_t, _P]
+        lib.vpce_fold_partials.restype = ctypes.c_int
+        lib.vpce_fold_partials.argtypes = [_P, ctypes.c_int, _I64, _P, _P]
         lib.vpce_lmhead_workspace_bytes.restype = ctypes.c_size_t
         lib.vpce_lmhead_workspace_bytes.argtypes = [_I64]
         lib.vpce_lmhead_forward.restype = ctypes.c_int
