@@ -441,6 +441,207 @@ def run_ours(args):
 
 
 # ----------------------------------------------------------------------------
+# the pages' multi-card method: the vocabulary split over the processes
+# ----------------------------------------------------------------------------
+DISTRIBUTED_METRIC = "VPCE fwd+bwd tokens/s, vocabulary split over N processes (one GPU each), s=8192 V=128256 bf16"
+
+
+def _free_port() -> int:
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def run_distributed(args, backend=None, device: str = "cuda", emit=print):
+    """One shared batch whose vocabulary is split over the N processes ("Distributed
+    Training III: Model Parallelism", CMU 11-868 Lecture 16 notes, §5.5; "LLM
+    Internals" §7.3.4): rank r holds shards [r t/N, (r+1) t/N) of the workload's t.
+    A step is distributed.forward (local partial statistics, the rank's shards
+    folded to one (max, sum exp) pair per row, one all-gather of the pairs, one
+    all-reduce of the target logits, the combine on every rank) and
+    distributed.backward (dlogits in place, no communication).  The batch is
+    the same on every rank, so the work per rank shrinks as N grows (strong
+    scaling); tokens/s counts each token once.  ``backend`` and ``device='cpu'``
+    let the orchestration run on CPU ranks over gloo (tests); the GPU run uses
+    the library's kernels and NCCL."""
+    import torch
+    import torch.distributed as dist
+
+    from vocab_sharded_lm_gb300 import distributed
+
+    rank, world, local = _env_rank()
+    cpu = device == "cpu"
+    own_group = False
+    if not dist.is_initialized():
+        if world == 1:
+            # a group of one, so that the exchange runs as written
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            os.environ.setdefault("MASTER_PORT", str(_free_port()))
+            dist.init_process_group("gloo" if cpu else "nccl", rank=0, world_size=1)
+        else:
+            dist.init_process_group("gloo" if cpu else "nccl")
+        own_group = True
+    if cpu:
+        dev = torch.device("cpu")
+    else:
+        from vocab_sharded_lm_gb300 import _build, vpce
+
+        torch.cuda.set_device(local)
+        dev = torch.device("cuda", local)
+        _build.build()
+        vpce.load_library()
+
+    w = synth.WORKLOADS[args.workload]
+    if args.rows:
+        w = w.replace(s=args.rows)
+    if w.t % world:
+        if rank == 0:
+            emit(json.dumps({"metric": DISTRIBUTED_METRIC, "unavailable":
+                             f"{w.t} shards do not split evenly over {world} processes"}))
+        if own_group:
+            dist.destroy_process_group()
+        return
+    per = w.t // world
+    vs = synth.even_vocab_start(w.V, w.t)
+    vs_local = vs[rank * per:(rank + 1) * per + 1]
+    meta = synth.row_meta(w)  # one batch, the same targets on every rank
+    e = w.elem_bytes
+    slice_bytes = w.s * (vs_local[-1] - vs_local[0]) * e
+    if cpu:
+        host = synth.shards_host(w, meta, vs_local)
+        pristine = [torch.from_numpy(h.astype(np.float32) if w.dtype == "fp32" else h) for h in host]
+        nbuf = 2
+    else:
+        pristine = synth.device_shards(w, meta, vs_local, device=dev)
+        free, _ = torch.cuda.mem_get_info(dev)
+        nbuf = max(2, min(args.warmup + args.steps, int(0.5 * free // max(slice_bytes, 1)), args.max_buffers))
+    bufs = [[p.clone() for p in pristine] for _ in range(nbuf)]
+    y = torch.from_numpy(meta.targets).to(dev)
+    be = backend or distributed.CudaBackend()
+    ws = [be.new_workspace(per, w.s, dev) for _ in range(2)]
+    last = {}
+
+    def step(k):
+        b = bufs[k % nbuf]
+        loss, _, wk = distributed.forward(b, vs_local, y, w.V, ignore_index=w.ignore_index, backend=be,
+                                          workspace=ws[k % 2])
+        distributed.backward(b, vs_local, y, wk, ignore_index=w.ignore_index, backend=be)
+        last["loss"] = loss
+
+    for k in range(args.warmup):
+        step(k)
+    for b in bufs:  # the timed steps start from generated logits
+        for d, p_ in zip(b, pristine):
+            d.copy_(p_)
+    coll_dev = None if cpu else dev
+    clocks = None if cpu else ClockSampler(local)
+    if clocks is not None:
+        clocks.start()
+    dist.barrier()
+    if cpu:
+        t_start = time.perf_counter()
+        for k in range(args.steps):
+            step(k)
+        total_ms = (time.perf_counter() - t_start) * 1e3
+    else:
+        stream = torch.cuda.current_stream(dev)
+        torch.cuda.synchronize(dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for k in range(args.steps):
+            step(k)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = t0.elapsed_time(t1)
+    dist.barrier()
+    clk = clocks.stop() if clocks is not None else None
+    total_ms = _max_over_ranks(total_ms, coll_dev)
+    loss_v = float(last["loss"])
+
+    # end to end: every step copies this rank's logits slice and the targets
+    # in from pinned host memory and reads the loss back
+    if cpu:
+        e2e_ms, h2d, d2h = total_ms / args.steps, 0, 0
+    else:
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        host_in = [p_.cpu().pin_memory() for p_ in pristine]
+        host_y = torch.from_numpy(meta.targets).pin_memory()
+        host_loss = torch.empty(e2e_steps, dtype=torch.float32).pin_memory()
+        torch.cuda.synchronize(dev)
+        dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(e2e_steps):
+            b = bufs[k % nbuf]
+            for d, h in zip(b, host_in):
+                d.copy_(h, non_blocking=True)
+            y.copy_(host_y, non_blocking=True)
+            step(k)
+            host_loss[k].copy_(last["loss"].reshape(()), non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, coll_dev)
+        h2d, d2h = slice_bytes + w.s * 8, 4
+    if rank != 0:
+        if own_group:
+            dist.destroy_process_group()
+        return
+    ms_step = total_ms / args.steps
+    out = {
+        "metric": DISTRIBUTED_METRIC,
+        "value": round(w.s * args.steps / (total_ms * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "strong",
+        "vs_baseline": None,
+        # logits of logits_dtype widened to fp32 for the arithmetic
+        "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator; no dataset)",
+        "config": {
+            "workload": _workload_desc(w),
+            "global_batch": w.s,
+            "seq_len": w.s,
+            "logits_dtype": w.dtype,
+            "parallelism": f"vocabulary split: {world} process(es) x {per} of the {w.t} shards, one shared batch",
+            "path": "distributed.forward + distributed.backward: vpce_partials, vpce_fold_partials, all_gather of "
+                    "one (max, sum exp) pair per row and rank, all_reduce of the target logits, "
+                    "vpce_combine_partials, vpce_backward",
+            "backend": "gloo, CPU ranks" if cpu else "NCCL",
+        },
+        "exchange": {
+            # what one rank puts on the wire per step: its folded pair per row
+            # (all-gather) and its target-logit vector (all-reduce) -- the
+            # pages' three fp32 scalars per token
+            "bytes_sent_per_rank": 12 * w.s if world > 1 else 0,
+            "bytes_per_token": 12,
+        },
+        "loss": loss_v,
+        "e2e": {
+            "value": round(w.s / (e2e_ms * 1e-3), 1),
+            "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_ms, 4),
+        },
+        # vpce_partials, vpce_fold_partials, vpce_combine_partials and vpce_backward:
+        # one kernel each (the collectives are NCCL's)
+        "gpu_launches": 0 if cpu else 4 * args.steps,
+        "clocks": clk,
+    }
+    emit(json.dumps(out))
+    if own_group:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
 # the fp64 oracle on the host cores: CPU baseline and the reference arm
 # ----------------------------------------------------------------------------
 class _RowPool:
@@ -994,10 +1195,12 @@ def main():
                     help="seconds of oracle timing on one core, and again on every core")
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=["fused", "split", "lmhead", "lmhead_train", "embedding"], default="fused",
+    ap.add_argument("--path", choices=["fused", "split", "lmhead", "lmhead_train", "embedding", "distributed"],
+                    default="fused",
                     help="fused: vpce_forward_backward; split: vpce_forward then vpce_backward; "
                          "lmhead: the LM-head GEMM fused with the forward loss; embedding: the vocabulary-parallel "
-                         "input embedding (each its own metric)")
+                         "input embedding; distributed: one batch with its vocabulary split over the torchrun "
+                         "processes (each its own metric)")
     ap.add_argument("--vocab", type=int, default=0,
                     help="LM-head paths: vocabulary size of a smaller head (profiling captures)")
     ap.add_argument("--shards", type=int, default=0, help="LM-head paths with --vocab: vocabulary shards")
@@ -1012,6 +1215,8 @@ def main():
         run_lmhead(args)
     elif args.path == "embedding":
         run_embedding(args)
+    elif args.path == "distributed":
+        run_distributed(args)
     else:
         run_ours(args)
 
