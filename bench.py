@@ -134,13 +134,15 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # the source file of each kernel whose ncu traffic is recorded; the shared
 # device headers count for all of them
-_KERNEL_FILES = {"stream_fused_kernel": "vpce_fused.cu", "backward_kernel": "vpce_backward.cu",
-                 "partial_stats_kernel": "vpce_forward.cu", "gemm_stats_kernel": "vpce_gemm.cu"}
+# each kernel's source file and the headers it includes beyond the shared ones
+_KERNEL_FILES = {"stream_fused_kernel": ("vpce_fused.cu",), "backward_kernel": ("vpce_backward.cu",),
+                 "partial_stats_kernel": ("vpce_forward.cu",), "gemm_stats_kernel": ("vpce_gemm.cu", "vpce_tc.cuh"),
+                 "gemm_bwd_kernel": ("vpce_gemm_bwd.cu", "vpce_tc.cuh")}
 
 
 def _kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in ("vpce_device.cuh", "vpce_kernels.cuh", "vpce_chunk.cuh", _KERNEL_FILES[kernel]):
+    for f in ("vpce_device.cuh", "vpce_kernels.cuh", "vpce_chunk.cuh", *_KERNEL_FILES[kernel]):
         with open(os.path.join(ROOT, "vocab_sharded_lm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

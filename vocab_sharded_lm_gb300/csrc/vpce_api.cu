@@ -14,8 +14,8 @@ cudaError_t set_fused_smem();
 bool fused_supported(const ShardSet& sh, int t, int elem);
 void launch_prep(const long long* targets, long long s, long long V, long long ignore_index, Header* hdr,
                  int reduction, float* loss_out, cudaStream_t st);
-bool fused_pair(long long row_bytes);
-int fused_grid(long long s, int sms, bool pair);
+int fused_cluster(long long row_bytes);
+int fused_grid(long long s, int sms, int nr);
 void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long long V, const long long* targets,
                          long long ignore_index, int reduction, float grad, const float* grad_rows, float* lse,
                          float* rowl, float* row_loss, float* loss_out, Header* hdr, int sms, cudaStream_t st);
@@ -391,10 +391,10 @@ vpce_status vpce_fused_plan(vpce_dtype dtype, int t, const int64_t* vocab_start,
   const vpce_status st = device_setup(&sms);
   if (st != VPCE_OK) return st;
   const int eb = dtype == VPCE_BF16 ? 2 : 4;
-  const bool pair = fused_pair(vocab_start[t] * eb);
+  const int nr = fused_cluster(vocab_start[t] * eb);
   *kernel = 1;
-  *cluster = pair ? 2 : 1;
-  *grid = fused_grid(s, sms, pair);
+  *cluster = nr;
+  *grid = fused_grid(s, sms, nr);
   for (int i = 0; i < t; ++i)
     if (((vocab_start[i + 1] - vocab_start[i]) * eb) & 15) {
       *kernel = 0;

@@ -26,6 +26,8 @@
 // (needed for the 1/n_valid of the mean before any gradient is written) comes
 // from a one-block prologue kernel that also clears the workspace header; the
 // batch loss is summed in a fixed order by the last block to finish.
+#include <mutex>
+
 #include "vpce_chunk.cuh"
 
 namespace vpce {
@@ -61,6 +63,11 @@ constexpr int kDSlots = 4;
 // SM (49 MB over 152 SMs) is where the re-reads still hit L2; more slack
 // turns them into HBM reads.
 constexpr unsigned kLiveBytesPerCta = 320u * 1024u;
+// The same budget for CTAs that share rows (a cluster per row): their row
+// statistics also cross SMs, and a smaller window measured faster there
+// (s = 32768 bf16 half rows of 250 KB: 6.16 ms with one chunk of slack per
+// stats warp, 6.35 ms with two, 6.37 ms with none).
+constexpr unsigned kLiveBytesPerCtaShared = 288u * 1024u;
 // stats warp w and grad warp w walk the same chunks: the credit between them
 // counts those chunks
 static_assert(kSW == kDW, "stats and grad warps pair up");
@@ -102,15 +109,15 @@ struct FusedSmem {
   uint64_t dfull[kDW][kDSlots];
   uint64_t rowdone[2];  // stats warps -> grad warps: a row's partials are in
   uint64_t rowfree[2];  // grad warps -> stats warps: the grad warps have begun that row
-  float2 part[2][kSW];
+  float2 part[2][2 * kSW];  // (max, sum exp) of every stats warp of the row's CTAs, CTA-rank major
   float tz[2];
   unsigned sdone[kSW];  // chunks stats warp w has received (its grad partner may re-read them)
   unsigned gdone[kDW];  // chunks grad warp w has received (credit back to its stats partner)
   Geo geo;
 };
-// Within the 227 KB a CTA may use, with room for a 1 KB granule of static
-// shared memory should the compiler reserve one.
-static_assert(sizeof(FusedSmem) + 1024 <= 232448, "fused kernel shared memory");
+// Within the 227 KB of dynamic shared memory a CTA may use (the kernel has
+// no static shared memory).
+static_assert(sizeof(FusedSmem) <= 232448, "fused kernel shared memory");
 
 // Prologue: clear the header, count the valid rows, flag bad targets.
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const long long* targets, long long s,
@@ -161,36 +168,46 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const long long* tar
 
 // The part of every row one warp of a role owns: shard segments [sa, sb)
 // and, within each, the wi-th of nw = 2^nw_log2 byte ranges.  One CTA per
-// row: every segment, split over the kSW warps.  Two CTAs per row: with two
-// or more shards the CTAs take the segments on either side of the boundary
-// nearest half the row, each split over its kSW warps (the chunks stay as
-// long as with one CTA); with one shard the segment is split over 2 kSW
-// warps.
+// row: every segment, split over the kSW warps.  A cluster of NR CTAs per
+// row: with at least NR shards, CTA c takes the segments between the shard
+// boundaries nearest c/NR and (c+1)/NR of the row (at least one each), each
+// split over its kSW warps, so the chunks stay as long as with one CTA;
+// with fewer shards every segment is split over the NR kSW warps.
 struct RowPart {
   int sa, sb;
   int nw_log2, wi;
 };
 
-__device__ __forceinline__ RowPart row_part(const Geo& g, int t, bool pair, unsigned crank, int w) {
+template <int NR>
+__device__ __forceinline__ RowPart row_part(const Geo& g, int t, unsigned crank, int w) {
   RowPart rp{0, t, kSWLog2, w};
-  if (!pair) return rp;
-  if (t == 1) {
-    rp.nw_log2 = kSWLog2 + 1;
+  if (NR == 1) return rp;
+  if (t < NR) {
+    rp.nw_log2 = kSWLog2 + (NR == 2 ? 1 : 2);
     rp.wi = int(crank) * kSW + w;
     return rp;
   }
-  int k = 1;
-  long long best = -1;
-  for (int i = 1; i < t; ++i) {
-    const long long d = 2LL * g.start[i] - g.start[t];
-    const long long ad = d < 0 ? -d : d;
-    if (best < 0 || ad < best) {
-      best = ad;
-      k = i;
+  int prev = 0;
+  for (int c = 1; c <= int(crank) + 1; ++c) {
+    int k = t;
+    if (c < NR) {
+      // the boundary nearest c/NR of the row, leaving a segment for each CTA
+      long long best = -1;
+      for (int i = prev + 1; i <= t - (NR - c); ++i) {
+        const long long d = (long long)NR * g.start[i] - (long long)c * g.start[t];
+        const long long ad = d < 0 ? -d : d;
+        if (best < 0 || ad < best) {
+          best = ad;
+          k = i;
+        }
+      }
     }
+    if (c == int(crank) + 1) {
+      rp.sa = prev;
+      rp.sb = k;
+    }
+    prev = k;
   }
-  if (crank == 0) rp.sb = k;
-  else rp.sa = k;
   return rp;
 }
 
@@ -313,16 +330,18 @@ __device__ __forceinline__ void target_of(const Geo& g, int t, long long y, int&
   }
 }
 
-// PAIR: a cluster of two CTAs shares each row, CTA c taking the c-th half of
-// every warp role's column split (2 kSW stats warps per row).  Each CTA's
-// live L2 window then holds half-rows, which keeps rows longer than
-// kLiveBytesPerCta re-read from L2.  The stats warps of both CTAs post their
-// partials to both CTAs' mailboxes (16 arrivals), and every grad warp folds
-// the 16 partials in CTA-rank order, so both CTAs reach the same logsumexp.
-template <typename T, bool PAIR>
+// NR > 1: a cluster of NR CTAs shares each row, CTA c taking the c-th part
+// of every warp role's column split (NR kSW stats warps per row).  Each CTA's
+// live L2 window then holds part rows, which keeps rows longer than the
+// live budget re-read from L2.  The stats warps of all NR CTAs post their
+// partials to every CTA's mailbox barrier (NR kSW arrivals), and every grad
+// warp folds the NR kSW partials (one per lane, then a fixed butterfly), so
+// all CTAs reach the same logsumexp.
+template <typename T, int NR>
 __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid_constant__ FusedParams p) {
   constexpr int EB = Elem<T>::kBytes;
-  constexpr int NR = PAIR ? 2 : 1;  // CTAs per row
+  constexpr bool PAIR = NR > 1;     // CTAs of a cluster share each row
+  static_assert(NR == 1 || NR == 2, "one row per CTA or per pair of CTAs");
   constexpr int NWR = NR * kSW;     // warps of one role per row
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   FusedSmem& sm = *reinterpret_cast<FusedSmem*>(smem_raw);
@@ -360,7 +379,7 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
   if (PAIR) cluster_sync_all();
   const Geo& geo = sm.geo;
   const int nt = p.t;
-  const RowPart rp = row_part(geo, nt, PAIR, crank, w);  // this warp's part of every row
+  const RowPart rp = row_part<NR>(geo, nt, crank, w);  // this warp's part of every row
 
   const long long r_step = gridDim.x / NR;
   const long long r0 = blockIdx.x / NR;
@@ -368,10 +387,10 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
   auto wait_row_bar = [&](uint64_t* bar, uint32_t parity) {
     return PAIR ? mbar_wait_warp_cluster(bar, parity) : mbar_wait_warp(bar, parity);
   };
-  auto arrive_row_bar = [&](uint64_t* bar) {  // lane 0 only
+  auto arrive_row_bar = [&](uint64_t* bar) {  // one lane only
     if (PAIR) {
-      mbar_arrive_cluster(bar, 0u);
-      mbar_arrive_cluster(bar, 1u);
+#pragma unroll
+      for (int c = 0; c < NR; ++c) mbar_arrive_cluster(bar, unsigned(c));
     } else {
       mbar_arrive_local(bar);
     }
@@ -453,13 +472,28 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
         alive = false;
         break;
       }
-      if (lane == 0) {
-        sm.part[buf][w] = make_float2(m, se);
+      // lane 1 posts the row: lane 0 issues this warp's bulk copies, and a
+      // release at cluster scope from that thread measured 1.8 us per row
+      // against 0.7 us from another lane (s = 32768, CTA pairs)
+      if (lane == 1) {
+        // the partial goes to every CTA's mailbox: the grad warps then read
+        // all of a row's partials from their own shared memory
+        sm.part[buf][crank * kSW + w] = make_float2(m, se);
+#pragma unroll
+        for (int c = 0; c < NR; ++c)
+          if (unsigned(c) != crank)
+            asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(
+                             cluster_addr(&sm.part[buf][crank * kSW + w], unsigned(c))),
+                         "f"(m), "f"(se)
+                         : "memory");
         if (has_t) {
           sm.tz[buf] = zt;
-          if (PAIR)  // the peer's grad warps read the target logit from their own mailbox
-            asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr(&sm.tz[buf], crank ^ 1u)), "f"(zt)
-                         : "memory");
+          // the other CTAs' grad warps read the target logit from their own mailbox
+#pragma unroll
+          for (int c = 0; c < NR; ++c)
+            if (unsigned(c) != crank)
+              asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr(&sm.tz[buf], unsigned(c))), "f"(zt)
+                           : "memory");
         }
         arrive_row_bar(&sm.rowdone[buf]);
       }
@@ -533,17 +567,15 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
         break;
       }
       // every grad warp folds the partials in the same order (CTA rank, then
-      // warp): the same lse in every warp of both CTAs
+      // warp; for a pair, one partial per lane and a fixed butterfly): the
+      // same lse in every warp of both CTAs
       float M, S, zt;
       if (PAIR) {
-        const float2 q0 = ld_cluster_f2(&sm.part[buf][0], 0u);
-        M = q0.x;
-        S = q0.y;
-#pragma unroll
-        for (int j = 1; j < NWR; ++j) {
-          const float2 q = ld_cluster_f2(&sm.part[buf][j % kSW], unsigned(j / kSW));
-          merge_ms(M, S, q.x, q.y);
-        }
+        float2 q = make_float2(-INFINITY, 0.f);
+        if (lane < NWR) q = sm.part[buf][lane];
+        M = q.x;
+        S = q.y;
+        warp_merge_ms(M, S);
         zt = sm.tz[buf];  // written here by whichever CTA's warp holds the target
       } else {
         M = sm.part[buf][0].x;
@@ -553,7 +585,7 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
         zt = sm.tz[buf];
       }
       __syncwarp();
-      if (lane == 0) arrive_row_bar(&sm.rowfree[buf]);
+      if (lane == 1) arrive_row_bar(&sm.rowfree[buf]);  // lane 0 issues the bulk copies (see the stats side)
       ++n;
       const float lse = in_range ? M + logf(S) : __int_as_float(0x7fc00000);
       if (w == 0 && lane == 0 && crank == 0) {
@@ -669,25 +701,62 @@ bool fused_supported(const ShardSet& sh, int t, int elem) {
 
 cudaError_t set_fused_smem() {
   const int b = int(sizeof(FusedSmem));
-  cudaError_t e = cudaFuncSetAttribute(stream_fused_kernel<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(stream_fused_kernel<__nv_bfloat16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(stream_fused_kernel<float, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(stream_fused_kernel<__nv_bfloat16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+  cudaError_t e = cudaSuccess;
+  const void* kernels[] = {
+      reinterpret_cast<const void*>(stream_fused_kernel<float, 1>),
+      reinterpret_cast<const void*>(stream_fused_kernel<float, 2>),
+      reinterpret_cast<const void*>(stream_fused_kernel<__nv_bfloat16, 1>),
+      reinterpret_cast<const void*>(stream_fused_kernel<__nv_bfloat16, 2>)};
+  for (const void* k : kernels)
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
   return e;
 }
 
-// Two CTAs share each row once a row no longer fits one CTA's live window.
-bool fused_pair(long long row_bytes) { return row_bytes > (long long)kLiveBytesPerCta; }
+// Pairs of CTAs (one per SM) that fit on the device at once, from the
+// occupancy calculator (a GPC with an odd number of free SMs leaves one
+// over).  Computed once per device.
+int fused_max_clusters(int nr, int sms) {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  if (nr == 1) return sms;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return sms / nr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(nr * (sms / nr)));
+    cfg.blockDim = dim3(kFThreads);
+    cfg.dynamicSmemBytes = sizeof(FusedSmem);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = unsigned(nr);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, stream_fused_kernel<__nv_bfloat16, 2>, &cfg);
+    if (e != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = sms / nr;
+    }
+    cache[dev] = n < sms / nr ? n : sms / nr;
+  }
+  return cache[dev];
+}
 
-// CTAs of the persistent grid: one per SM (pairs of SMs per row with pair),
-// no more than the rows need.
-int fused_grid(long long s, int sms, bool pair) {
-  if (!pair) return int(s < sms ? s : sms);
-  const long long clusters = s < sms / 2 ? s : sms / 2;
-  return int(2 * clusters);
+// CTAs per row: one while a row fits one CTA's live window, else a pair.
+int fused_cluster(long long row_bytes) { return row_bytes > (long long)kLiveBytesPerCta ? 2 : 1; }
+
+// CTAs of the persistent grid: one per SM (a cluster of nr SMs per row, as
+// many clusters as fit at once), no more than the rows need.
+int fused_grid(long long s, int sms, int nr) {
+  const int fit = fused_max_clusters(nr, sms);
+  const long long clusters = s < fit ? s : fit;
+  return int(nr * clusters);
 }
 
 void launch_prep(const long long* targets, long long s, long long V, long long ignore_index, Header* hdr,
@@ -695,10 +764,10 @@ void launch_prep(const long long* targets, long long s, long long V, long long i
   prep_kernel<<<1, kPrepThreads, 0, st>>>(targets, s, V, ignore_index, hdr, reduction, loss_out);
 }
 
-// Chunks of slack per stats warp for rows of row_bytes: whatever of
-// kLiveBytesPerCta one row leaves, shared by the kSW stats warps.
-unsigned credit_slack(long long row_bytes) {
-  const long long spare = (long long)kLiveBytesPerCta - row_bytes;
+// Chunks of slack per stats warp for rows of row_bytes per CTA: whatever of
+// the live budget one row leaves, shared by the kSW stats warps.
+unsigned credit_slack(long long row_bytes, bool shared) {
+  const long long spare = (long long)(shared ? kLiveBytesPerCtaShared : kLiveBytesPerCta) - row_bytes;
   return spare > 0 ? unsigned(spare / (long long)(kSW * kFChunk)) : 0u;
 }
 
@@ -717,14 +786,14 @@ void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long
   p.grad = grad;
   p.grad_rows = grad_rows;
   const long long row_bytes = V * (bf16 ? 2 : 4);
-  const bool pair = fused_pair(row_bytes);
-  p.credit_slack = credit_slack(pair ? (row_bytes + 1) / 2 : row_bytes);
+  const int nr = fused_cluster(row_bytes);
+  p.credit_slack = credit_slack((row_bytes + nr - 1) / nr, nr > 1);
   p.lse = lse;
   p.rowl = rowl;
   p.row_loss = row_loss;
   p.loss_out = loss_out;
   p.hdr = hdr;
-  const int grid = fused_grid(s, sms, pair);
+  const int grid = fused_grid(s, sms, nr);
   // a programmatic dependent of the prologue: the stats warps start streaming
   // while it counts n_valid
   cudaLaunchConfig_t cfg = {};
@@ -736,18 +805,17 @@ void launch_stream_fused(const ShardSet& sh, bool bf16, int t, long long s, long
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.x = unsigned(nr);
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pair ? 2 : 1;
-  if (pair) {
-    if (bf16) cudaLaunchKernelEx(&cfg, stream_fused_kernel<__nv_bfloat16, true>, p);
-    else cudaLaunchKernelEx(&cfg, stream_fused_kernel<float, true>, p);
-  } else if (bf16) {
-    cudaLaunchKernelEx(&cfg, stream_fused_kernel<__nv_bfloat16, false>, p);
+  cfg.numAttrs = nr > 1 ? 2 : 1;
+  if (bf16) {
+    if (nr == 2) cudaLaunchKernelEx(&cfg, stream_fused_kernel<__nv_bfloat16, 2>, p);
+    else cudaLaunchKernelEx(&cfg, stream_fused_kernel<__nv_bfloat16, 1>, p);
   } else {
-    cudaLaunchKernelEx(&cfg, stream_fused_kernel<float, false>, p);
+    if (nr == 2) cudaLaunchKernelEx(&cfg, stream_fused_kernel<float, 2>, p);
+    else cudaLaunchKernelEx(&cfg, stream_fused_kernel<float, 1>, p);
   }
 }
 
