@@ -327,3 +327,97 @@ def test_lmhead_forward_backward_matches_two_calls():
     assert torch.allclose(dx1.float(), dx2.float(), rtol=2 ** -7, atol=2 ** -7 * float(dx2.float().abs().max()))
     for a, b in zip(dw1, dw2):
         assert torch.allclose(a, b, rtol=2 ** -7, atol=2 ** -7 * float(b.abs().max()))
+
+
+def test_lmhead_backward_ragged_hidden_and_many_shards():
+    # h = 320: the second N tile of dX and dW holds 64 valid columns; V and the
+    # rows are ragged; ten shards of unequal width
+    m = synth.LmHead("bwd_ragged_h", 29, 333, 320, 1337, 10, ignore_frac=0.05)
+    _check_backward(m)
+    _check_backward(m, fused=True)
+
+
+def _strided_outputs(m, ws, pad_x, pad_w, off_x=0):
+    """dX and dW outputs as views of larger buffers: row strides h + pad, and
+    dX starting off_x elements past a 16-byte boundary (element stores)."""
+    base = torch.zeros(m.s * (m.h + pad_x) + off_x, dtype=torch.bfloat16, device="cuda")
+    gx = base[off_x:].view(m.s, m.h + pad_x)[:, :m.h]
+    gw = []
+    for w in ws:
+        b = torch.full((w.shape[0], m.h + pad_w), 0.5, dtype=torch.float32, device="cuda")
+        gw.append(b[:, :m.h])
+    return gx, gw
+
+
+@pytest.mark.parametrize("off_x", [0, 1])
+def test_lmhead_backward_strided_outputs(off_x):
+    m = synth.LmHead("bwd_strided", 30, 200, 192, 900, 3, ignore_frac=0.1)
+    vs = synth.even_vocab_start(m.V, m.t)
+    meta = synth.lmhead_meta(m)
+    x, ws = synth.lmhead_device(m, vs)
+    y = torch.from_numpy(meta.targets).cuda()
+    gx, gw = _strided_outputs(m, ws, pad_x=24, pad_w=12, off_x=off_x)
+    _, fwk = vpce.vpce_lmhead_forward(x, ws, y, vs, ignore_index=m.ignore_index)
+    vpce.vpce_lmhead_backward(x, ws, y, fwk, vs, ignore_index=m.ignore_index, grad_hidden=gx,
+                              grad_weight_shards=gw)
+    torch.cuda.synchronize()
+    xh, wh = _host(m, vs)
+    ref_x, ref_w, dz = O.lmhead_backward(xh, wh, vs, meta.targets, m.ignore_index)
+    got_x = O.widen(gx.contiguous().view(torch.int16).cpu().numpy().view(np.uint16), "bf16")
+    W = np.concatenate([O.widen(w, "bf16") for w in wh])
+    bx = _bwd_bound(dz, W, ref_x, m.V)
+    assert np.all(np.abs(got_x - ref_x) <= bx)
+    X = O.widen(xh, "bf16")
+    for i in range(m.t):
+        got_w = gw[i].cpu().numpy().astype(np.float64) - 0.5
+        bw = _bwd_bound(dz[:, vs[i]:vs[i + 1]].T, X, np.zeros_like(ref_w[i]), m.s) + 2.0 ** -24 * (0.5 + np.abs(ref_w[i]))
+        assert np.all(np.abs(got_w - ref_w[i]) <= bw)
+    # the padding columns are neither read nor written
+    assert torch.all(gw[0].as_strided((gw[0].shape[0], 12), (m.h + 12, 1), m.h) == 0.5)
+
+
+def test_lmhead_train_full_size_sampled_rows():
+    """The one-call training step on the pages' head (s = 8192, h = 8192,
+    V = 128256, t = 8) in the configuration bench.py times: sampled rows of
+    the loss and of dX against the oracle, formed in fp64 from the hidden
+    states and head read back from the device; every row of dW is summed
+    over the vocabulary, which is zero for exact arithmetic (each valid row of
+    dZ sums to zero), to within the rounding of dZ."""
+    m = synth.LMHEADS["lmhead_s8192_h8192_v128256"]
+    vs = synth.even_vocab_start(m.V, m.t)
+    meta = synth.lmhead_meta(m)
+    x, ws = synth.lmhead_device(m, vs)
+    y = torch.from_numpy(meta.targets).cuda()
+    rl = torch.empty(m.s, dtype=torch.float32, device="cuda")
+    loss, dx, dw = vpce.vpce_lmhead_forward_backward(x, ws, y, vs, ignore_index=m.ignore_index, row_loss_out=rl)
+    torch.cuda.synchronize()
+    n_valid = int(np.sum(meta.targets != m.ignore_index))
+    got_rl = rl.cpu().numpy().astype(np.float64)
+    assert abs(float(loss) - got_rl.sum() / n_valid) <= 1e-6 * abs(float(loss))
+    rng = np.random.default_rng(11)
+    rows = np.concatenate([[0, m.s - 1], rng.integers(1, m.s - 1, size=4)])
+    xr = x[torch.from_numpy(rows).cuda()].view(torch.int16).cpu().numpy().view(np.uint16)
+    w_host = [w.view(torch.int16).cpu().numpy().view(np.uint16) for w in ws]
+    z = O.lmhead_logits(xr, w_host, vs)
+    ref = O.cross_entropy(z, meta.targets[rows], m.ignore_index, n_valid=n_valid)
+    assert np.all(np.abs(got_rl[rows] - ref["row_loss"]) <= _row_bound(xr, w_host, m.h))
+    dz = O.dlogits(z, meta.targets[rows], m.ignore_index, n_valid=n_valid)
+    ref_x = np.zeros((len(rows), m.h))
+    bound = np.zeros((len(rows), m.h))
+    eps = 2.0 ** -8 + 2.0 ** -11 + (m.V / 16) * 2.0 ** -24
+    for i in range(m.t):
+        Wi = O.widen(w_host[i], "bf16")
+        dzi = dz[:, vs[i]:vs[i + 1]]
+        ref_x += dzi @ Wi
+        bound += eps * (np.abs(dzi) @ np.abs(Wi))
+    bound += 2.0 ** -8 * (np.abs(ref_x) + bound)
+    got_x = O.widen(dx[torch.from_numpy(rows).cuda()].view(torch.int16).cpu().numpy().view(np.uint16), "bf16")
+    assert np.all(np.abs(got_x - ref_x) <= bound), np.max(np.abs(got_x - ref_x) / bound)
+    # sum over the vocabulary of dW_i[v, :] = sum_r (sum_v dZ[r, v]) X[r, :]: zero for
+    # exact arithmetic.  A valid row of dZ has sum_v |dZ[r, v]| <= 2 / n_valid, so its
+    # bf16 rounding (2^-9 relative) moves the row sum by at most 2^-8 / n_valid; the
+    # fp32 accumulation of dW over the 8192 rows (512 MMA steps of 16) adds at most
+    # 512 * 2^-24 of the same sum, 2^-14 / n_valid
+    col = sum(d.double().sum(dim=0) for d in dw).cpu().numpy()
+    xs = np.abs(x.float().cpu().numpy().astype(np.float64)).sum(axis=0)
+    assert np.all(np.abs(col) <= (2.0 ** -8 + 2.0 ** -14) / n_valid * xs + 1e-12)
