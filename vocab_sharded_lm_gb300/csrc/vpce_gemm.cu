@@ -59,7 +59,7 @@ constexpr int kGThreads = 192;  // 6 warps
 constexpr int kTmemCols = 512;  // the pair's two accumulators of kBN fp32 columns
 static_assert(kMT * kBN <= kTmemCols, "the pair's accumulators fit in TMEM");
 constexpr int kMaxGemmShards = 32;
-constexpr int kMaxGroupsPerWave = 8;  // M tiles that share a W tile (kMaxGroupsPerWave / kMT pairs)
+constexpr int kMaxGroupsPerWave = 16;  // M tiles that share a W tile (kMaxGroupsPerWave / kMT pairs)
 
 struct GemmSmem {
   unsigned char stage[kGStages][kGStage];  // 1024-byte aligned (swizzle atoms): A0, A1, B

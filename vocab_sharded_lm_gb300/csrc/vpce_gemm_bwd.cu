@@ -91,6 +91,7 @@ struct BwdParams {
   int pstart[kMaxShards + 1];   // dW: first M-tile pair of shard i (pairs of 256 vocabulary rows)
   int width[kMaxShards];        // w_i
   int tiles;
+  int group;                    // M-tile pairs per raster group
   unsigned short* dx;           // dX: bf16 [R, ld_dx]
   long long ld_dx;
   Header* hdr;
@@ -99,17 +100,26 @@ struct BwdParams {
 constexpr uint32_t kIdescDX = idesc_bf16(kBM, kBN, false, true);
 constexpr uint32_t kIdescDW = idesc_bf16(kBM, kBN, true, true);
 
-// Tile k of the walk: dX (mp, nt), nt fastest; dW (shard, mp within it, nt),
-// nt fastest, so the CTAs that run at the same time share their A blocks.
+// Tile k of the walk.  The M-tile pairs (counted over all shards for dW) run
+// in groups of p.group: within a group the N tiles in order, the group's
+// pairs fastest.  The CTAs that run at the same time then share both their A
+// blocks (the group's pairs) and their B blocks (a few N tiles), so each
+// block comes from HBM about once per group instead of once per wave.
 struct Tile {
   int sh, mp, nt;
 };
 
 template <int MODE>
 __device__ __forceinline__ Tile tile_at(const BwdParams& p, int k) {
+  const int total = MODE == kDX ? p.m_pairs : p.pstart[p.t];
+  const int per_group = p.group * p.n_tiles;
+  const int g = k / per_group;
+  const int j = k - g * per_group;
+  const int first = g * p.group;
+  const int gsize = min(p.group, total - first);
   Tile tl;
-  tl.nt = k % p.n_tiles;
-  const int q = k / p.n_tiles;
+  tl.nt = j / gsize;
+  const int q = first + (j - tl.nt * gsize);
   if (MODE == kDX) {
     tl.sh = 0;
     tl.mp = q;
@@ -368,6 +378,10 @@ bool launch_dgrad_x(const unsigned short* dz, long long ldz, const long long* zc
   p.m_pairs = int((R + kMT * kBM - 1) / (kMT * kBM));
   p.k_steps = p.kstart[t];
   p.tiles = p.m_pairs * p.n_tiles;
+  // groups of 8 pairs: 18.3 GB of reads per full-size launch against 17.2 for one pair per
+  // group, but the sustained training step is 1.5 % faster (31.0 against 31.5 ms, six
+  // interleaved runs of ten steps)
+  p.group = 8;
   p.dx = static_cast<unsigned short*>(dx);
   p.ld_dx = ld_dx;
   p.hdr = hdr;
@@ -399,6 +413,7 @@ bool launch_dgrad_w(const unsigned short* dz, long long ldz, const long long* zc
   p.n_tiles = int((h + kBN - 1) / kBN);
   p.k_steps = int((R + kBK - 1) / kBK);
   p.tiles = p.pstart[t] * p.n_tiles;
+  p.group = 16;  // measured: 17.7 GB of reads per full-size launch against 19.7 (8) and 22.4 (32)
   p.hdr = hdr;
   const int grid = p.tiles < sms ? p.tiles : sms;
   gemm_bwd_kernel<kDW><<<grid, kThreads, kSmemDW, st>>>(p);
