@@ -9,8 +9,8 @@
 // up front (the loss is the last op, g = 1 or a loss scale), the backward of a
 // row can follow its forward while the row is still on chip:
 //
-//   * a CTA owns whole rows; its 8 "stats" warps each take 1/8 of every shard
-//     segment of a row and stream it from HBM through their own shared-memory
+//   * a CTA owns whole rows; its 8 "stats" warps each take 1/8 of a row (one
+//     contiguous range of its shard segments) and stream it from HBM through their own shared-memory
 //     rings (cp.async.bulk + mbarrier), keeping an online (max, sum-exp) --
 //     the streaming pattern of the split forward;
 //   * per row they leave 8 partials (and the target logit) in a two-deep
@@ -166,92 +166,107 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const long long* tar
   }
 }
 
-// The part of every row one warp of a role owns: shard segments [sa, sb)
-// and, within each, the wi-th of nw = 2^nw_log2 byte ranges.  One CTA per
-// row: every segment, split over the kSW warps.  A cluster of NR CTAs per
-// row: with at least NR shards, CTA c takes the segments between the shard
-// boundaries nearest c/NR and (c+1)/NR of the row (at least one each), each
-// split over its kSW warps, so the chunks stay as long as with one CTA;
-// with fewer shards every segment is split over the NR kSW warps.
+// The part of every row one warp of a role owns: the bytes [lo, hi) of the
+// row's shard segments laid end to end (segment i starts at byte start[i] *
+// element size), 16-byte aligned.  One CTA per row: the whole row, cut into
+// kSW equal ranges.  A cluster of NR CTAs per row: with at least NR shards,
+// CTA c takes the segments between the shard boundaries nearest c/NR and
+// (c+1)/NR of the row (at least one each), with fewer shards the c-th NR-th
+// of the row; its kSW warps then cut that part into equal ranges.  A range
+// may cross segment boundaries, so a warp's chunks are full kFChunk bytes
+// except where a segment or its range ends.
 struct RowPart {
-  int sa, sb;
-  int nw_log2, wi;
+  int sa, sb;        // the segments the CTA's part touches
+  unsigned lo, hi;   // this warp's bytes of the row
 };
 
-template <int NR>
+template <int NR, int EB>
 __device__ __forceinline__ RowPart row_part(const Geo& g, int t, unsigned crank, int w) {
-  RowPart rp{0, t, kSWLog2, w};
-  if (NR == 1) return rp;
-  if (t < NR) {
-    rp.nw_log2 = kSWLog2 + (NR == 2 ? 1 : 2);
-    rp.wi = int(crank) * kSW + w;
-    return rp;
-  }
-  int prev = 0;
-  for (int c = 1; c <= int(crank) + 1; ++c) {
-    int k = t;
-    if (c < NR) {
-      // the boundary nearest c/NR of the row, leaving a segment for each CTA
-      long long best = -1;
-      for (int i = prev + 1; i <= t - (NR - c); ++i) {
-        const long long d = (long long)NR * g.start[i] - (long long)c * g.start[t];
-        const long long ad = d < 0 ? -d : d;
-        if (best < 0 || ad < best) {
-          best = ad;
-          k = i;
+  RowPart rp{0, t, 0u, 0u};
+  unsigned clo = 0, chi = unsigned(g.start[t]) * EB;
+  if (NR > 1) {
+    if (t < NR) {
+      const unsigned long long len = chi;
+      clo = unsigned((len * crank) / NR) & ~15u;
+      chi = int(crank) == NR - 1 ? chi : unsigned((len * (crank + 1)) / NR) & ~15u;
+    } else {
+      int prev = 0;
+      for (int c = 1; c <= int(crank) + 1; ++c) {
+        int k = t;
+        if (c < NR) {
+          // the boundary nearest c/NR of the row, leaving a segment for each CTA
+          long long best = -1;
+          for (int i = prev + 1; i <= t - (NR - c); ++i) {
+            const long long d = (long long)NR * g.start[i] - (long long)c * g.start[t];
+            const long long ad = d < 0 ? -d : d;
+            if (best < 0 || ad < best) {
+              best = ad;
+              k = i;
+            }
+          }
         }
+        if (c == int(crank) + 1) {
+          rp.sa = prev;
+          rp.sb = k;
+        }
+        prev = k;
       }
+      clo = unsigned(g.start[rp.sa]) * EB;
+      chi = unsigned(g.start[rp.sb]) * EB;
     }
-    if (c == int(crank) + 1) {
-      rp.sa = prev;
-      rp.sb = k;
-    }
-    prev = k;
   }
+  // kSW equal ranges of the CTA's part (a power of two: no division)
+  const unsigned long long len = chi - clo;
+  rp.lo = clo + (unsigned((len * unsigned(w)) >> kSWLog2) & ~15u);
+  rp.hi = w == kSW - 1 ? chi : clo + (unsigned((len * unsigned(w + 1)) >> kSWLog2) & ~15u);
+  // the segments the warp's range touches
+  while (rp.sa + 1 < rp.sb && unsigned(g.start[rp.sa + 1]) * EB <= rp.lo) ++rp.sa;
+  while (rp.sb - 1 > rp.sa && unsigned(g.start[rp.sb - 1]) * EB >= rp.hi) --rp.sb;
   return rp;
 }
 
-// Byte range [lo, hi) of a shard segment owned by the part's warp (16-byte
-// boundaries; the last warp takes the remainder).  nw is a power of two, so
-// there is no division.
-__device__ __forceinline__ void sub_range(unsigned seg_bytes, const RowPart& rp, unsigned& lo, unsigned& hi) {
-  lo = unsigned(((unsigned long long)seg_bytes * unsigned(rp.wi)) >> rp.nw_log2) & ~15u;
-  hi = rp.wi == (1 << rp.nw_log2) - 1
-           ? seg_bytes
-           : unsigned(((unsigned long long)seg_bytes * unsigned(rp.wi + 1)) >> rp.nw_log2) & ~15u;
-}
-
-// Walks the chunks of row r in a warp's part: segment by segment, each
-// sub-range cut into kFChunk-byte chunks and a shorter last one.  No
-// division on the way: the walk runs once per chunk on the critical path of
-// both roles, where a 64-bit division by a variable chunk count cost as much
-// as the chunk's arithmetic.
+// Walks the chunks of row r in a warp's part: from lo to hi, kFChunk bytes
+// at a time, a chunk ending early where a segment ends.  No division on the
+// way: the walk runs once per chunk on the critical path of both roles,
+// where a 64-bit division by a variable chunk count cost as much as the
+// chunk's arithmetic.  bounds() gives a chunk's byte range inside its
+// segment, addr() its address.
 template <int EB>
 struct RowWalk {
   int seg;
-  unsigned pos, hi;     // the next chunk starts at pos; the warp's share ends at hi
+  unsigned pos, hi;     // the next chunk starts at row byte pos; the warp's range ends at hi
+  unsigned seg_lo, seg_hi;  // row bytes of segment seg
   unsigned char* base;  // the row's first byte in shard seg
   bool ok;
 
-  __device__ __forceinline__ bool seek(const Geo& g, const RowPart& rp, long long r, int from) {
-    for (seg = from > rp.sa ? from : rp.sa; seg < rp.sb; ++seg) {
-      unsigned lo;
-      sub_range(unsigned(g.start[seg + 1] - g.start[seg]) * EB, rp, lo, hi);
-      if (hi > lo) {
-        pos = lo;
-        base = const_cast<unsigned char*>(g.ptr[seg]) + r * g.ld[seg];
-        return ok = true;
-      }
-    }
-    return ok = false;
+  __device__ __forceinline__ void enter(const Geo& g, long long r) {
+    seg_lo = unsigned(g.start[seg]) * EB;
+    seg_hi = unsigned(g.start[seg + 1]) * EB;
+    base = const_cast<unsigned char*>(g.ptr[seg]) + r * g.ld[seg];
   }
-  __device__ __forceinline__ void next(const Geo& g, const RowPart& rp, long long r) {
-    pos += kFChunk;
-    if (pos >= hi) seek(g, rp, r, seg + 1);
+  __device__ __forceinline__ bool seek(const Geo& g, const RowPart& rp, long long r, int /*from*/) {
+    pos = rp.lo;
+    hi = rp.hi;
+    seg = rp.sa;
+    if (pos >= hi) return ok = false;
+    while (unsigned(g.start[seg + 1]) * EB <= pos) ++seg;
+    enter(g, r);
+    return ok = true;
+  }
+  __device__ __forceinline__ void next(const Geo& g, const RowPart& /*rp*/, long long r) {
+    pos = min(min(pos + unsigned(kFChunk), seg_hi), hi);
+    if (pos >= hi) {
+      ok = false;
+      return;
+    }
+    if (pos >= seg_hi) {
+      ++seg;
+      enter(g, r);
+    }
   }
   __device__ __forceinline__ void bounds(unsigned& a, unsigned& b) const {
-    a = pos;
-    b = min(pos + unsigned(kFChunk), hi);
+    a = pos - seg_lo;
+    b = min(min(pos + unsigned(kFChunk), seg_hi), hi) - seg_lo;
   }
   __device__ __forceinline__ unsigned char* addr(unsigned a) const { return base + a; }
 };
@@ -261,9 +276,9 @@ template <int EB>
 __device__ __forceinline__ unsigned row_chunks(const Geo& g, const RowPart& rp) {
   unsigned c = 0;
   for (int i = rp.sa; i < rp.sb; ++i) {
-    unsigned lo, hi;
-    sub_range(unsigned(g.start[i + 1] - g.start[i]) * EB, rp, lo, hi);
-    c += (hi - lo + kFChunk - 1) / kFChunk;
+    const unsigned lo = max(rp.lo, unsigned(g.start[i]) * EB);
+    const unsigned hi = min(rp.hi, unsigned(g.start[i + 1]) * EB);
+    if (hi > lo) c += (hi - lo + kFChunk - 1) / kFChunk;
   }
   return c;
 }
@@ -379,7 +394,7 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
   if (PAIR) cluster_sync_all();
   const Geo& geo = sm.geo;
   const int nt = p.t;
-  const RowPart rp = row_part<NR>(geo, nt, crank, w);  // this warp's part of every row
+  const RowPart rp = row_part<NR, EB>(geo, nt, crank, w);  // this warp's part of every row
 
   const long long r_step = gridDim.x / NR;
   const long long r0 = blockIdx.x / NR;
@@ -542,11 +557,12 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     for (long long r = r0; r < p.s && alive; r += r_step) {
       const long long y = __ldg(p.targets + r);
       if (y == p.ignore_index) {
-        // ignored row: zeros over this warp's share, nothing read
+        // ignored row: zeros over this warp's range, nothing read
         for (int i = rp.sa; i < rp.sb; ++i) {
-          unsigned lo, hi;
-          sub_range(unsigned(geo.start[i + 1] - geo.start[i]) * EB, rp, lo, hi);
-          uint4* d = reinterpret_cast<uint4*>(const_cast<unsigned char*>(geo.ptr[i]) + r * geo.ld[i] + lo);
+          const unsigned s0 = unsigned(geo.start[i]) * EB;
+          const unsigned lo = max(rp.lo, s0), hi = min(rp.hi, unsigned(geo.start[i + 1]) * EB);
+          if (hi <= lo) continue;
+          uint4* d = reinterpret_cast<uint4*>(const_cast<unsigned char*>(geo.ptr[i]) + r * geo.ld[i] + (lo - s0));
           for (unsigned v = lane; v < (hi - lo) >> 4; v += 32) d[v] = make_uint4(0u, 0u, 0u, 0u);
         }
         if (w == 0 && lane == 0 && crank == 0) {
@@ -692,6 +708,7 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
 // All shard pointers, row strides and widths 16-byte aligned (the bulk-copy
 // engine's requirement for the fused kernels).
 bool fused_supported(const ShardSet& sh, int t, int elem) {
+  if ((sh.start[t] - sh.start[0]) * elem >= (1LL << 31)) return false;  // row byte offsets are 32-bit
   for (int i = 0; i < t; ++i) {
     const long long wb = (sh.start[i + 1] - sh.start[i]) * elem;
     if ((reinterpret_cast<uintptr_t>(sh.ptr[i]) & 15u) || (sh.ld_bytes[i] & 15) || (wb & 15)) return false;
