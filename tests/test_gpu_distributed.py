@@ -69,3 +69,42 @@ def test_two_ranks_in_one_process(name, s, split):
         check_row_losses(rl, ref["row_loss"], ref["valid"])
     assert losses[0][0] == losses[1][0]
     np.testing.assert_array_equal(losses[0][1], losses[1][1])
+
+
+def test_distributed_forward_backward_through_nccl_group_of_one():
+    """distributed.forward / backward end to end on the GPU: the library's
+    kernels for the local steps and NCCL for the exchange, in a process
+    group of one (this run has one GPU), checked against the oracle."""
+    import os
+    import socket
+
+    import torch.distributed as dist
+
+    w = synth.WORKLOADS["s8192_v128256"].replace(s=64)
+    vs = synth.even_vocab_start(w.V, w.t)
+    meta = synth.row_meta(w)
+    host = synth.shards_host(w, meta, vs)
+    z = O.assemble(host, vs, w.dtype)
+    ref = O.cross_entropy(z, meta.targets, w.ignore_index)
+    dref = O.dlogits(z, meta.targets, w.ignore_index, grad=1.0)
+    own = not dist.is_initialized()
+    if own:
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        os.environ["MASTER_ADDR"] = "127.0.0.1"
+        os.environ["MASTER_PORT"] = str(port)
+        dist.init_process_group("nccl", rank=0, world_size=1)
+    try:
+        dev = to_device(host, w.dtype)
+        y = torch.from_numpy(meta.targets).cuda()
+        loss, row_loss, ws = distributed.forward(dev, vs, y, w.V, ignore_index=w.ignore_index)
+        distributed.backward(dev, vs, y, ws, ignore_index=w.ignore_index)
+        torch.cuda.synchronize()
+        check_loss(float(loss), ref["loss"])
+        check_row_losses(row_loss.cpu().numpy(), ref["row_loss"], ref["valid"])
+        got = O.assemble([from_device(d, w.dtype) for d in dev], vs, w.dtype)
+        check_dlogits(got, dref, w.dtype, 1.0 / ref["n_valid"])
+    finally:
+        if own:
+            dist.destroy_process_group()
