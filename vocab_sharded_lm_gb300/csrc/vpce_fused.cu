@@ -59,14 +59,21 @@ constexpr int kSSlots = 3;
 constexpr int kDSlots = 4;
 // L2 bytes per CTA the two passes may keep live between them: one row is
 // the least (a row's statistics precede its gradient); rows shorter than
-// this let the stats warps run further ahead.  Measured on GB300: 320 KB per
-// SM (49 MB over 152 SMs) is where the re-reads still hit L2; more slack
-// turns them into HBM reads.
-constexpr unsigned kLiveBytesPerCta = 320u * 1024u;
+// this let the stats warps run further ahead.  Measured on GB300 with each
+// warp taking one contiguous range of the row: 288 KB per SM (44 MB over 152
+// SMs; one 4 KB chunk of slack per stats warp for 250 KB rows) gives
+// 0.664 ms at s = 8192, V = 128256, against 0.685 ms with 320 KB (two
+// chunks), 0.753 ms with 352 KB and 0.715 ms with no slack; 100 KB rows
+// (s = 4096) run the same with 288, 320 or 352 KB.
+constexpr unsigned kLiveBytesPerCta = 288u * 1024u;
+// Rows longer than this are shared by a pair of CTAs; shorter ones run on
+// one CTA, with whatever slack the window above leaves.
+constexpr long long kPairRowBytes = 320ll * 1024ll;
 // The same budget for CTAs that share rows (a cluster per row): their row
-// statistics also cross SMs, and a smaller window measured faster there
-// (s = 32768 bf16 half rows of 250 KB: 6.16 ms with one chunk of slack per
-// stats warp, 6.35 ms with two, 6.37 ms with none).
+// statistics also cross SMs.  Measured (s = 32768 bf16, half rows of 250 KB):
+// 5.80 ms with one chunk of slack per stats warp, 6.20 ms with two, 6.03 ms
+// with none; s = 16384 fp32 (304 KB half rows, no slack) runs the same with
+// 256, 288 or 320 KB, and 4% slower with one chunk of slack forced.
 constexpr unsigned kLiveBytesPerCtaShared = 288u * 1024u;
 // stats warp w and grad warp w walk the same chunks: the credit between them
 // counts those chunks
@@ -669,31 +676,55 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
   __threadfence();
   // Each warp sums whole 256-row blocks: lane l adds rows 8l .. 8l + 7 of the
   // block, then a fixed shuffle tree; a warp adds its blocks in order, and
-  // thread 0 the warps in order (a fixed order for a given s).  A block's
-  // loads are independent of one another: one thread walking 256 rows in
-  // sequence exposed each L2 latency (26 us per call at s = 8192).
+  // thread 0 the warps in order (a fixed order for a given s).  The loads of
+  // kSumBlocks blocks per warp are issued before any of them is added, so
+  // each pass waits for one L2 round trip: with one block per pass the sum
+  // took 8.6 us at s = 8192 and 29 us at s = 32768 (one round trip per block).
+  // The header's count and flag are read at the start, beside those loads:
+  // every other CTA set its flag bits before its ticket (fence, then atomic).
+  constexpr int kSumBlocks = 4;
+  constexpr int kSumWarps = kFThreads / 32;
+  int cnt = 0, flag = 0;
+  if (threadIdx.x == 0) {
+    cnt = __ldcg(&p.hdr->n_valid);
+    flag = __ldcg(&p.hdr->error_flag);
+  }
   double v = 0.0;
   const long long nb = (p.s + 255) / 256;
-  for (long long b = warp; b < nb; b += kFThreads / 32) {
-    double part = 0.0;
+  for (long long b0 = warp; b0 < nb; b0 += (long long)kSumWarps * kSumBlocks) {
+    float x[kSumBlocks][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const long long r = b * 256 + lane * 8 + j;
-      if (r < p.s) part += double(__ldcg(p.rowl + r));
+    for (int i = 0; i < kSumBlocks; ++i) {
+      const long long r0 = (b0 + (long long)i * kSumWarps) * 256 + lane * 8;
+      if (r0 + 8 <= p.s) {  // the workspace is 256-byte aligned: whole 32-byte runs
+        const float4 u = __ldcg(reinterpret_cast<const float4*>(p.rowl + r0));
+        const float4 w4 = __ldcg(reinterpret_cast<const float4*>(p.rowl + r0) + 1);
+        x[i][0] = u.x, x[i][1] = u.y, x[i][2] = u.z, x[i][3] = u.w;
+        x[i][4] = w4.x, x[i][5] = w4.y, x[i][6] = w4.z, x[i][7] = w4.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[i][j] = r0 + j < p.s ? __ldcg(p.rowl + r0 + j) : 0.f;
+      }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_down_sync(kFull, part, o);
-    v += part;
+    for (int i = 0; i < kSumBlocks; ++i) {
+      if (b0 + (long long)i * kSumWarps >= nb) break;
+      double part = 0.0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) part += double(x[i][j]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_down_sync(kFull, part, o);
+      v += part;
+    }
   }
   if (lane == 0) sv[warp] = v;
   __syncthreads();
   if (threadIdx.x == 0) {
     double tot = 0.0;
-    for (int i = 0; i < kFThreads / 32; ++i) tot += sv[i];
-    const int cnt = p.hdr->n_valid;
+    for (int i = 0; i < kSumWarps; ++i) tot += sv[i];
     // a wait that gave up anywhere in the grid leaves rows unfinished: the
     // loss is then NaN rather than a plausible partial sum
-    const bool timed_out = (atomicOr(&p.hdr->error_flag, 0) & VPCE_FLAG_WAIT_TIMEOUT) != 0;
+    const bool timed_out = (flag & VPCE_FLAG_WAIT_TIMEOUT) != 0;
     p.hdr->loss_sum = tot;
     p.hdr->ticket = 0u;
     if (p.loss_out != nullptr)
@@ -765,8 +796,8 @@ int fused_max_clusters(int nr, int sms) {
   return cache[dev];
 }
 
-// CTAs per row: one while a row fits one CTA's live window, else a pair.
-int fused_cluster(long long row_bytes) { return row_bytes > (long long)kLiveBytesPerCta ? 2 : 1; }
+// CTAs per row: one up to kPairRowBytes, else a pair.
+int fused_cluster(long long row_bytes) { return row_bytes > kPairRowBytes ? 2 : 1; }
 
 // CTAs of the persistent grid: one per SM (a cluster of nr SMs per row, as
 // many clusters as fit at once), no more than the rows need.
