@@ -102,7 +102,10 @@ def _run_sampled(w, path):
     err = np.abs(rl[rows][valid] - ref["row_loss"][valid]) / np.maximum(np.abs(ref["row_loss"][valid]), 1.0)
     assert err.max() <= LOSS_RTOL, err.max()
     mean = float(np.sum(rl.astype(np.float64)[y_all != w.ignore_index])) / n_valid
-    assert abs(loss_v - mean) <= 1e-6 * abs(mean)
+    # the batch sum runs in fp64 (two calls) or as a compensated fp32 pair
+    # (fused), either well below the final rounding to fp32 (2^-24 relative);
+    # a plain fp32 sum of 32768 rows would typically miss this bound
+    assert abs(loss_v - mean) <= 2e-7 * abs(mean), (loss_v, mean)
     assert np.all(rl[y_all == w.ignore_index] == 0.0)
     assert np.all(np.isfinite(rl))
 

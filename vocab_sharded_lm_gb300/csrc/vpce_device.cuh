@@ -387,4 +387,84 @@ __device__ __forceinline__ void warp_merge_ms(float& m, float& s) {
   }
 }
 
+// A compensated fp32 sum: hi is the plain recursive sum and lo gathers the
+// rounding error of every addition (Knuth's TwoSum), so hi + lo carries
+// about twice fp32's precision.  A batch loss over thousands of rows summed
+// by one CTA in fp64 spent microseconds in GB300's few fp64 units (8.6 us at
+// s = 8192, 29 us at s = 32768); these adds run on the fp32 pipes.
+struct FSum {
+  float hi = 0.f, lo = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float t = hi + x;
+    const float z = t - hi;
+    lo += (hi - (t - z)) + (x - z);
+    hi = t;
+  }
+  __device__ __forceinline__ void add(const FSum& o) {
+    add(o.hi);
+    lo += o.lo;
+  }
+  // hi + lo in fp64; a non-finite hi (an inf or NaN row loss) as it is, since
+  // lo is then NaN
+  __device__ __forceinline__ double value() const { return isfinite(hi) ? double(hi) + double(lo) : double(hi); }
+};
+
+// Sum of v[0 .. n) by one CTA of NW warps, in a fixed order (a given n and NW
+// always give the same bits): warp w takes the 256-element blocks w, w + NW,
+// ...; lane l adds elements 8l .. 8l + 7 of each, in order, to its FSum; a
+// fixed shuffle tree adds the lanes and thread 0 the warps in order.  The
+// loads of 4 blocks per warp are issued before any of them is added (one L2
+// round trip per pass).  v must be 16-byte aligned; it is read through L2
+// (__ldcg), so values other CTAs wrote before a fence are seen.  `sv` holds
+// NW float2 in shared memory.  Every thread of the CTA must call it; thread
+// 0 gets the sum.
+template <int NW>
+__device__ __forceinline__ double cta_fixed_sum(const float* v, long long n, float2* sv) {
+  constexpr int kSumBlocks = 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  FSum acc;
+  const long long nb = (n + 255) / 256;
+  for (long long b0 = warp; b0 < nb; b0 += (long long)NW * kSumBlocks) {
+    float x[kSumBlocks][8];
+#pragma unroll
+    for (int i = 0; i < kSumBlocks; ++i) {
+      const long long r0 = (b0 + (long long)i * NW) * 256 + lane * 8;
+      if (r0 + 8 <= n) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(v + r0));
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(v + r0) + 1);
+        x[i][0] = a.x, x[i][1] = a.y, x[i][2] = a.z, x[i][3] = a.w;
+        x[i][4] = b.x, x[i][5] = b.y, x[i][6] = b.z, x[i][7] = b.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[i][j] = r0 + j < n ? __ldcg(v + r0 + j) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kSumBlocks; ++i) {
+      if (b0 + (long long)i * NW >= nb) break;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc.add(x[i][j]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    FSum q;
+    q.hi = __shfl_down_sync(kFull, acc.hi, o);
+    q.lo = __shfl_down_sync(kFull, acc.lo, o);
+    acc.add(q);
+  }
+  if (lane == 0) sv[warp] = make_float2(acc.hi, acc.lo);
+  __syncthreads();
+  double tot = 0.0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NW; ++i) {
+      FSum w;
+      w.hi = sv[i].x;
+      w.lo = sv[i].y;
+      tot += w.value();
+    }
+  }
+  return tot;
+}
+
 }  // namespace vpce

@@ -668,60 +668,21 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
   __threadfence();
   __syncthreads();
   // every copy of this CTA has completed: the stats ring is free scratch
-  double* sv = reinterpret_cast<double*>(sm.sring[0][0]);
   int* last = reinterpret_cast<int*>(sm.sring[0][0] + 1024);
   if (threadIdx.x == 0) *last = atomicAdd(&p.hdr->ticket, 1u) == gridDim.x - 1;
   __syncthreads();
   if (!*last) return;
   __threadfence();
-  // Each warp sums whole 256-row blocks: lane l adds rows 8l .. 8l + 7 of the
-  // block, then a fixed shuffle tree; a warp adds its blocks in order, and
-  // thread 0 the warps in order (a fixed order for a given s).  The loads of
-  // kSumBlocks blocks per warp are issued before any of them is added, so
-  // each pass waits for one L2 round trip: with one block per pass the sum
-  // took 8.6 us at s = 8192 and 29 us at s = 32768 (one round trip per block).
-  // The header's count and flag are read at the start, beside those loads:
-  // every other CTA set its flag bits before its ticket (fence, then atomic).
-  constexpr int kSumBlocks = 4;
-  constexpr int kSumWarps = kFThreads / 32;
+  // The row losses in a fixed order (see cta_fixed_sum).  The header's count
+  // and flag are read at the start, beside those loads: every other CTA set
+  // its flag bits before its ticket (fence, then atomic).
   int cnt = 0, flag = 0;
   if (threadIdx.x == 0) {
     cnt = __ldcg(&p.hdr->n_valid);
     flag = __ldcg(&p.hdr->error_flag);
   }
-  double v = 0.0;
-  const long long nb = (p.s + 255) / 256;
-  for (long long b0 = warp; b0 < nb; b0 += (long long)kSumWarps * kSumBlocks) {
-    float x[kSumBlocks][8];
-#pragma unroll
-    for (int i = 0; i < kSumBlocks; ++i) {
-      const long long r0 = (b0 + (long long)i * kSumWarps) * 256 + lane * 8;
-      if (r0 + 8 <= p.s) {  // the workspace is 256-byte aligned: whole 32-byte runs
-        const float4 u = __ldcg(reinterpret_cast<const float4*>(p.rowl + r0));
-        const float4 w4 = __ldcg(reinterpret_cast<const float4*>(p.rowl + r0) + 1);
-        x[i][0] = u.x, x[i][1] = u.y, x[i][2] = u.z, x[i][3] = u.w;
-        x[i][4] = w4.x, x[i][5] = w4.y, x[i][6] = w4.z, x[i][7] = w4.w;
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) x[i][j] = r0 + j < p.s ? __ldcg(p.rowl + r0 + j) : 0.f;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kSumBlocks; ++i) {
-      if (b0 + (long long)i * kSumWarps >= nb) break;
-      double part = 0.0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) part += double(x[i][j]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) part += __shfl_down_sync(kFull, part, o);
-      v += part;
-    }
-  }
-  if (lane == 0) sv[warp] = v;
-  __syncthreads();
+  const double tot = cta_fixed_sum<kFThreads / 32>(p.rowl, p.s, reinterpret_cast<float2*>(sm.sring[0][0]));
   if (threadIdx.x == 0) {
-    double tot = 0.0;
-    for (int i = 0; i < kSumWarps; ++i) tot += sv[i];
     // a wait that gave up anywhere in the grid leaves rows unfinished: the
     // loss is then NaN rather than a plausible partial sum
     const bool timed_out = (flag & VPCE_FLAG_WAIT_TIMEOUT) != 0;

@@ -200,33 +200,13 @@ __global__ void __launch_bounds__(kRowThreads) train_rows_kernel(const __grid_co
   }
 }
 
-// The batch loss from the per-row losses: fixed 256-row blocks, summed in a
-// fixed order in fp64.
+// The batch loss from the per-row losses, summed in a fixed order by one
+// CTA (cta_fixed_sum).
 __global__ void __launch_bounds__(kLossThreads) train_loss_kernel(const float* rowl, long long s, Header* hdr,
                                                                   float* loss_out) {
-  __shared__ double sv[kLossThreads / 32];
-  // each warp sums whole blocks, lane l rows 8l .. 8l + 7, then a fixed
-  // shuffle tree; blocks and warps are added in order (independent loads
-  // instead of one thread walking a block in sequence)
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  double v = 0.0;
-  const long long nb = (s + 255) / 256;
-  for (long long b = warp; b < nb; b += kLossThreads / 32) {
-    double part = 0.0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const long long r = b * 256 + lane * 8 + j;
-      if (r < s) part += double(rowl[r]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_down_sync(kFull, part, o);
-    v += part;
-  }
-  if (lane == 0) sv[warp] = v;
-  __syncthreads();
+  __shared__ float2 sv[kLossThreads / 32];
+  const double tot = cta_fixed_sum<kLossThreads / 32>(rowl, s, sv);
   if (threadIdx.x == 0) {
-    double tot = 0.0;
-    for (int i = 0; i < kLossThreads / 32; ++i) tot += sv[i];
     const int cnt = hdr->n_valid;
     hdr->loss_sum = tot;
     if (loss_out != nullptr)
