@@ -8,7 +8,6 @@
 #include "vpce_kernels.cuh"
 
 namespace vpce {
-cudaError_t set_stats_smem();
 cudaError_t set_backward_smem();
 cudaError_t set_fused_smem();
 bool fused_supported(const ShardSet& sh, int t, int elem);
@@ -87,7 +86,7 @@ vpce_status device_setup(int* sms) {
     }
     if (major != 10 || minor != 3) {
       d.status = VPCE_ERR_UNSUPPORTED_DEVICE;
-    } else if (set_stats_smem() != cudaSuccess || set_backward_smem() != cudaSuccess ||
+    } else if (set_backward_smem() != cudaSuccess ||
                set_fused_smem() != cudaSuccess || set_gemm_smem() != cudaSuccess || set_gemm_bwd_smem() != cudaSuccess ||
                set_embed_smem() != cudaSuccess) {
       cudaGetLastError();
@@ -256,9 +255,13 @@ vpce_status vpce_forward(const void* const* shards, vpce_dtype dtype, int t, int
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   Header* hdr = reinterpret_cast<Header*>(ws);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  // n_valid, the error flag and the combine's ticket start at zero, cleared
-  // in stream order before any block may set a flag bit
-  if ((st = clear_header(hdr, cs)) != VPCE_OK) return st;
+  // n_valid, the error flag, the last block's ticket and the per-row arrival
+  // counts start at zero, cleared in stream order before any block may set
+  // a flag bit (one memset: the counts follow the header)
+  if (cudaMemsetAsync(ws, 0, L.part, cs) != cudaSuccess) {
+    cudaGetLastError();
+    return VPCE_ERR_CUDA;
+  }
 
   if (s > 0) {
     StatsParams p;
@@ -270,10 +273,16 @@ vpce_status vpce_forward(const void* const* shards, vpce_dtype dtype, int t, int
     p.part = reinterpret_cast<float2*>(ws + L.part);
     p.tgt = reinterpret_cast<float*>(ws + L.tgt);
     p.hdr = hdr;
-    const int grid = stream_grid(sms, p.units);
-    if (dtype == VPCE_BF16) launch_stats<__nv_bfloat16>(p, grid, cs);
-    else launch_stats<float>(p, grid, cs);
-    if ((st = launch_status()) != VPCE_OK) return st;
+    p.row_cnt = reinterpret_cast<int*>(ws + L.cnt);
+    p.t = t;
+    p.V = V;
+    p.reduction = int(reduction);
+    p.lse = reinterpret_cast<float*>(ws + L.lse);
+    p.row_loss = row_loss_out;
+    p.loss_out = loss_out;
+    if (dtype == VPCE_BF16) launch_stats<__nv_bfloat16>(p, sms, cs);
+    else launch_stats<float>(p, sms, cs);
+    return launch_status();  // the statistics kernel combines the rows and sums the batch
   }
   CombineParams c;
   c.s = s;
@@ -290,8 +299,7 @@ vpce_status vpce_forward(const void* const* shards, vpce_dtype dtype, int t, int
   c.loss_out = loss_out;
   c.row_loss = row_loss_out;
   c.hdr = hdr;
-  const long long blocks = s > 0 ? (s + kCombineThreads - 1) / kCombineThreads : 1;
-  launch_combine(c, int(blocks), cs);
+  launch_combine(c, 1, cs);  // s = 0: the empty batch's loss
   return launch_status();
 }
 
@@ -524,9 +532,9 @@ vpce_status vpce_partials(const void* const* shards, vpce_dtype dtype, int t, in
   p.part = reinterpret_cast<float2*>(part_out);
   p.tgt = tgt_out;
   p.hdr = reinterpret_cast<Header*>(workspace);
-  const int grid = stream_grid(sms, p.units);
-  if (dtype == VPCE_BF16) launch_stats<__nv_bfloat16>(p, grid, cs);
-  else launch_stats<float>(p, grid, cs);
+  p.row_cnt = nullptr;  // partials only: the caller exchanges and combines them
+  if (dtype == VPCE_BF16) launch_stats<__nv_bfloat16>(p, sms, cs);
+  else launch_stats<float>(p, sms, cs);
   return launch_status();
 }
 

@@ -17,20 +17,11 @@ __device__ __forceinline__ f32x2 exp2_pair(f32x2 x, f32x2 l2e, f32x2 b) {
   return f2_pack(ex2(e0), ex2(e1));
 }
 
-// Running (max m, sum of exp(x - m)) of a lane, updated with the lane's
-// vectors of one chunk: one max over the chunk, one rescale, then the sum.
+// Running (max m, sum of exp(x - m)) of a lane, updated with VPL of its
+// vectors (registers; padding vectors hold -inf): one max over them, one
+// rescale, then the sum.
 template <int VPL>
-__device__ __forceinline__ void stats_chunk(const unsigned char* buf, unsigned n, int lane, float& m, float& sm,
-                                            __nv_bfloat16) {
-  const uint4* v = reinterpret_cast<const uint4*>(buf);
-  const int nv = int(n >> 4);
-  uint4 q[VPL];
-  const uint4 neg = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);  // bf16 -inf x8
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int idx = lane + 32 * j;
-    q[j] = idx < nv ? v[idx] : neg;
-  }
+__device__ __forceinline__ void stats_vecs(const uint4 (&q)[VPL], float& m, float& sm, __nv_bfloat16) {
   __nv_bfloat162 mx = __halves2bfloat162(__ushort_as_bfloat16(0xff80), __ushort_as_bfloat16(0xff80));
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
@@ -62,16 +53,8 @@ __device__ __forceinline__ void stats_chunk(const unsigned char* buf, unsigned n
 }
 
 template <int VPL>
-__device__ __forceinline__ void stats_chunk(const unsigned char* buf, unsigned n, int lane, float& m, float& sm,
-                                            float) {
-  const float4* v = reinterpret_cast<const float4*>(buf);
-  const int nv = int(n >> 4);
-  float4 q[VPL];
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int idx = lane + 32 * j;
-    q[j] = idx < nv ? v[idx] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-  }
+__device__ __forceinline__ void stats_vecs(const uint4 (&qu)[VPL], float& m, float& sm, float) {
+  const float4(&q)[VPL] = reinterpret_cast<const float4(&)[VPL]>(qu);
   float cm = -INFINITY;
 #pragma unroll
   for (int j = 0; j < VPL; ++j) cm = fmaxf(cm, fmaxf(fmaxf(q[j].x, q[j].y), fmaxf(q[j].z, q[j].w)));
@@ -92,6 +75,28 @@ __device__ __forceinline__ void stats_chunk(const unsigned char* buf, unsigned n
   f2_unpack(a0, s0, s1);
   f2_unpack(a1, s2, s3);
   sm += (s0 + s1) + (s2 + s3);
+}
+
+// A vector of -inf in the element type (padding for stats_vecs).
+__device__ __forceinline__ uint4 neg_inf_vec(__nv_bfloat16) {
+  return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+}
+__device__ __forceinline__ uint4 neg_inf_vec(float) {
+  return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+}
+
+// stats_vecs over the lane's vectors of one shared-memory chunk.
+template <int VPL, typename T>
+__device__ __forceinline__ void stats_chunk(const unsigned char* buf, unsigned n, int lane, float& m, float& sm, T) {
+  const uint4* v = reinterpret_cast<const uint4*>(buf);
+  const int nv = int(n >> 4);
+  uint4 q[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int idx = lane + 32 * j;
+    q[j] = idx < nv ? v[idx] : neg_inf_vec(T());
+  }
+  stats_vecs<VPL>(q, m, sm, T());
 }
 
 // In place over the lane's vectors: exp(x - lse) * scale.  The exponent

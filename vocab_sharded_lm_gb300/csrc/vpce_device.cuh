@@ -36,10 +36,11 @@ constexpr int kCombineThreads = 256;
 __host__ __device__ inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t part, tgt, lse, bsum, bcnt, total;
+  size_t cnt, part, tgt, lse, bsum, bcnt, total;
   __host__ __device__ WsLayout(int t, long long s) {
     const long long nb = s > 0 ? (s + kCombineThreads - 1) / kCombineThreads : 1;
-    part = 256;
+    cnt = 256;  // per-row shard arrivals, right after the header (one clear covers both)
+    part = cnt + round256(sizeof(int) * size_t(s));
     tgt = part + round256(sizeof(float2) * size_t(t) * size_t(s));
     lse = tgt + round256(sizeof(float) * size_t(s));
     bsum = lse + round256(sizeof(float) * size_t(s));
