@@ -24,11 +24,16 @@ namespace {
 __device__ __forceinline__ void combine_row_if_last(const StatsParams& p, long long r, long long y, int lane) {
   int last = 0;
   if (lane == 0) {
-    __threadfence();  // this warp's partial (and target logit) before its arrival
-    last = atomicAdd(p.row_cnt + r, 1) == p.t - 1;
+    // release: this warp's partial (and target logit) before its arrival;
+    // acquire: for the last to arrive, every other shard's partial of the row.
+    // (A fence before and after a plain atomic measured 0.3358 against
+    // 0.3336 ms per forward call at s = 8192.)
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.row_cnt + r) : "memory");
+    last = old == p.t - 1;
   }
   if (!__shfl_sync(kFull, last, 0)) return;
-  __threadfence();  // every other shard's partial of the row is visible
+  __syncwarp();  // the other lanes' loads below come after lane 0's acquire
   const float2 none = make_float2(-INFINITY, 0.f);
   const float2 q0 = lane < p.t ? __ldcg(p.part + (long long)lane * p.s + r) : none;
   const float2 q1 = lane + 32 < p.t ? __ldcg(p.part + (long long)(lane + 32) * p.s + r) : none;
