@@ -120,7 +120,9 @@ size_t vpce_workspace_bytes(int t, int64_t s);
  *                out-of-range targets.
  *   workspace    device buffer of workspace_bytes >= vpce_workspace_bytes.
  * Results are bitwise reproducible for fixed inputs and t: the shards fold
- * in ascending index order and the batch sum runs in a fixed order (fp64).
+ * in ascending index order and the batch sum runs in a fixed order (a
+ * compensated fp32 pair per lane, about 48 bits, added across warps in
+ * fp64).
  */
 vpce_status vpce_forward(const void* const* shards, vpce_dtype dtype, int t, int64_t s,
                          const int64_t* vocab_start, int64_t ld,
@@ -281,7 +283,7 @@ vpce_status vpce_fused_plan(vpce_dtype dtype, int t, const int64_t* vocab_start,
  *   - Limit: returns VPCE_ERR_WORKSPACE, launching nothing, when
  *     vpce_workspace_bytes(t, s) > VPCE_STATIC_SCRATCH_BYTES (8 MiB covers,
  *     e.g., t = 16 at s = 32768, t = 8 at s = 65536 and t = 64 at s = 8192;
- *     roughly 8 * t * s + 8 * s bytes are needed).
+ *     roughly 8 * t * s + 12 * s bytes are needed).
  *   - Every call on a device shares the one array and the next call overwrites
  *     it (each call clears what must start at zero), so calls that may
  *     overlap on the GPU -- on different streams, or from different threads --
