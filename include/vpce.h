@@ -186,8 +186,8 @@ vpce_status vpce_backward_rows(void* const* shards, vpce_dtype dtype, int t, int
  * vpce_combine_partials: n_part partials [n_part][s] (all processes' part_out
  * gathered, in a fixed order) and tgt [s] (the sum over processes of tgt_out,
  * exact since one term per row is non-zero) combined into logsumexp, the row
- * losses and the reduced loss exactly as vpce_forward's combine (folded in
- * index order, fp64 batch sum).  V is the whole vocabulary (the bad-target
+ * losses and the reduced loss with vpce_forward's per-row arithmetic (folded
+ * in index order; the batch sum in fp64 over fixed blocks).  V is the whole vocabulary (the bad-target
  * check).  The workspace is laid out for t_local shards so that
  * vpce_backward on this process's t_local shards (with their global
  * vocab_start) reads its logsumexp and n_valid; its header is cleared here.
@@ -229,9 +229,9 @@ vpce_status vpce_fold_partials(const float* part, int t, int64_t s, float* out, 
  * as vpce_forward plus grad_output; the workspace afterwards holds logsumexp
  * and n_valid like a forward's.  Rows that are not 16-byte aligned (shard
  * pointer, row stride or width in bytes) run the two-call path instead, with
- * the same results.  The batch loss is summed in a fixed order (fp64), so
- * results are bitwise reproducible; they agree with the two-call path within
- * rounding.
+ * the same results.  The batch loss is summed in a fixed order (compensated
+ * fp32 pairs, fp64 across warps), so results are bitwise reproducible; they
+ * agree with the two-call path within rounding.
  */
 vpce_status vpce_forward_backward(void* const* shards, vpce_dtype dtype, int t, int64_t s,
                                   const int64_t* vocab_start, int64_t ld,
@@ -383,8 +383,9 @@ vpce_status vpce_lmhead_backward(const void* hidden, int64_t ld_hidden,
  * tensor-core kernels of vpce_lmhead_backward compute dX = dZ W and
  * dW += dZ^T X.
  *   loss_out, row_loss_out, reduction   as vpce_lmhead_forward (the mean
- *                  divides by the batch's n_valid; the loss sum is fp64 over
- *                  fixed 256-row blocks).
+ *                  divides by the batch's n_valid; the loss sum runs over
+ *                  fixed 256-row blocks in compensated fp32 pairs, fp64
+ *                  across warps).
  *   grad_output, grad_rows, grad_hidden, grad_weight_shards, their strides
  *                  as vpce_lmhead_backward.  VPCE_NONE requires grad_rows.
  *   workspace      256-byte aligned.  With
