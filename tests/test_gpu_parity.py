@@ -55,6 +55,24 @@ def test_ragged_shard_widths(widths, dtype):
     check_full(run_full(w, vocab_start=vs))
 
 
+@pytest.mark.parametrize("t", [33, 64])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("path", ["split", "fused"])
+def test_many_shards_many_rows(t, dtype, path):
+    """Thousands of rows over 33 or 64 shards of uneven widths: every row's
+    partials arrive from many warps at once (the forward combines a row in
+    the warp that adds its last partial), and more than 32 partials per row
+    take the combine's second load per lane.  Widths are multiples of 8
+    elements, so the fused kernel runs too."""
+    rng = np.random.default_rng(1000 + t)
+    widths = (rng.integers(1, 26, size=t) * 8).tolist()
+    vs = [0]
+    for x in widths:
+        vs.append(vs[-1] + x)
+    w = synth.Workload("many", 12, 3000, vs[-1], t, dtype, 2.5, "uniform", ignore_frac=0.05)
+    check_full(run_full(w, vocab_start=vs, path=path))
+
+
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 @pytest.mark.parametrize("misalign", [1, 3])
 def test_unaligned_shard_pointers(dtype, misalign):
