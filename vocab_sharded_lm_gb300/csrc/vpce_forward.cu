@@ -8,9 +8,13 @@
 //
 // Kernel 1 (partial_stats) streams every (shard, row) segment into registers,
 // one warp per segment at a time, and keeps an online (max, sum-exp) in fp32.
-// Kernel 2 (combine) folds the t partials of each row in ascending shard order
-// (the on-device stand-in for the pages' max / sum / sum all-reduces), masks
-// ignore_index, and reduces the batch in a fixed order in fp64.
+// The combine -- the t partials of a row folded in ascending shard order, the
+// on-device stand-in for the pages' max / sum / sum all-reduces, with
+// ignore_index masked -- runs in the same kernel, in the warp that adds a
+// row's last partial, and its last block sums the batch in a fixed order.
+// Kernel 2 (combine_kernel) is the same combine as a kernel of its own, for
+// partials that come from elsewhere (other processes, the LM-head GEMM); its
+// batch sum is fp64 over fixed blocks.
 #include "vpce_chunk.cuh"
 
 namespace vpce {
