@@ -25,6 +25,9 @@ import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
+# NCCL prints its version banner on stdout at communicator set-up; the bench
+# prints exactly one JSON line there (a caller's own setting wins)
+os.environ.setdefault("NCCL_DEBUG", "WARN")
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
