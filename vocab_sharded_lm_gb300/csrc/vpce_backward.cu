@@ -59,10 +59,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1) backward_kernel(const __grid_c
   const long long u0 = p.units * gw / nw;
   const long long u1 = p.units * (gw + 1) / nw;
 
-  const int n_valid = p.hdr->n_valid;
-  const float scale_all =
-      p.hdr->reduction != VPCE_MEAN ? p.grad : (n_valid > 0 ? p.grad / float(n_valid) : 0.f);
-
   if (lane == 0) {
 #pragma unroll
     for (int k = 0; k < kStages; ++k) mbar_init(&bar[k], 1);
@@ -88,6 +84,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1) backward_kernel(const __grid_c
     ++issued;
     prod.next<EB>(p);
   }
+  // Launched as a programmatic dependent of the kernel ahead (the forward's):
+  // everything above reads only the logits and the targets, which the caller
+  // leaves as the forward saw them; n_valid and logsumexp are the forward's,
+  // read only after it has completed.
+  grid_dependency_wait();
+  const int n_valid = p.hdr->n_valid;
+  const float scale_all =
+      p.hdr->reduction != VPCE_MEAN ? p.grad : (n_valid > 0 ? p.grad / float(n_valid) : 0.f);
 
   unsigned kc = 0;
   bool alive = true;
@@ -186,7 +190,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1) backward_kernel(const __grid_c
 
 template <typename T>
 void launch_backward(const BackwardParams& p, int grid, cudaStream_t st) {
-  backward_kernel<T><<<grid, kWarps * 32, kRingSmem, st>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = kRingSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, backward_kernel<T>, p);
 }
 template void launch_backward<float>(const BackwardParams&, int, cudaStream_t);
 template void launch_backward<__nv_bfloat16>(const BackwardParams&, int, cudaStream_t);

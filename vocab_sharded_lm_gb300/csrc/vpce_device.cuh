@@ -388,6 +388,15 @@ __device__ __forceinline__ void warp_merge_ms(float& m, float& s) {
   }
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream serialization attribute may start while the kernel ahead of it in
+// the stream still runs; grid_dependency_wait() blocks the calling thread
+// until that kernel has completed and its writes are visible (at once when
+// launched without the attribute), and grid_launch_dependents() in the
+// kernel ahead lets the dependent start.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // A compensated fp32 sum: hi is the plain recursive sum and lo gathers the
 // rounding error of every addition (Knuth's TwoSum), so hi + lo carries
 // about twice fp32's precision.  A batch loss over thousands of rows summed

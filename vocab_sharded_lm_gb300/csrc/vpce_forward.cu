@@ -81,6 +81,9 @@ template <typename T, int U, int B>
 __global__ void __launch_bounds__(kRegThreads, B) partial_stats_kernel(const __grid_constant__ StatsParams p) {
   constexpr int EB = Elem<T>::kBytes;
   const int lane = threadIdx.x & 31;
+  // the backward that follows may start its ring set-up and first loads on
+  // SMs this grid leaves; it waits for this grid before reading its results
+  grid_launch_dependents();
   WarpUnits w;
 #pragma unroll 1
   for (w.start(p.s); w.u < p.units; w.next(p.s)) {

@@ -36,16 +36,10 @@ namespace {
 
 constexpr int kPrepThreads = 1024;
 
-// Programmatic dependent launch.  The fused kernel is launched with the
-// programmatic stream serialization attribute, so it may start while the
-// prologue kernel ahead of it is still running; grid_dependency_wait() blocks
-// the calling thread until the prologue has completed and its writes are
-// visible (at once when launched without the attribute), and the prologue's
-// grid_launch_dependents() lets the fused kernel start.  Measured on GB300:
-// 0.7129 -> 0.7071 ms per call at s = 8192 (the same change on the split
-// path's combine and backward kernels gained nothing and was left out).
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+// The fused kernel is the prologue's programmatic dependent (see
+// grid_dependency_wait): it may start while the prologue still runs, and
+// only its grad warps, and every thread before the batch-loss ticket, wait
+// for it.  Measured on GB300: 0.7129 -> 0.7071 ms per call at s = 8192.
 constexpr int kSW = 8;         // stats warps
 constexpr int kSWLog2 = 3;
 constexpr int kDW = 8;         // grad warps
