@@ -1,9 +1,11 @@
 // Per-chunk arithmetic of the streaming kernels: what a warp does with one
 // shared-memory chunk of logits.  A chunk is n bytes (a multiple of 16) of
 // 16-byte vectors; lane l takes vectors l, l + 32, ...; VPL bounds the vectors
-// per lane (chunk capacity / 512 bytes).  Pairs of elements go through packed
-// fp32x2 instructions; every exponential is one ex2 on the special-function
-// unit.
+// per lane (chunk capacity / 512 bytes).  The chunk always sits at the start
+// of a ring slot of VPL * 512 bytes, and the forms below may read (the fused
+// kernel's gradient form also write) the whole slot: only the first n bytes
+// ever reach global memory.  Pairs of elements go through packed fp32x2
+// instructions; every exponential is one ex2 on the special-function unit.
 #pragma once
 
 #include "vpce_kernels.cuh"
@@ -85,17 +87,31 @@ __device__ __forceinline__ uint4 neg_inf_vec(float) {
   return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
 }
 
+// The lane's vectors of a chunk: the whole slot is loaded, and only a short
+// chunk (the end of a range) replaces the vectors past n with pad, so a full
+// chunk costs no per-vector predicate or select.  Measured on GB300 in the
+// fused kernel: s = 32768, V = 256000 (CTA pairs) 5.81 -> 5.72 ms, s = 8192
+// 0.662 -> 0.660 ms, s = 4096 0.169 -> 0.167 ms.  The split backward keeps
+// its predicated loop (unpredicated, its registers rose from 91 to 249 and
+// it ran 1.3% slower).
+template <int VPL>
+__device__ __forceinline__ void load_slot(const unsigned char* buf, unsigned n, int lane, uint4 (&q)[VPL], uint4 pad) {
+  const uint4* v = reinterpret_cast<const uint4*>(buf);
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) q[j] = v[lane + 32 * j];
+  if (n < unsigned(VPL) * 512u) {
+    const int nv = int(n >> 4);
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+      if (lane + 32 * j >= nv) q[j] = pad;
+  }
+}
+
 // stats_vecs over the lane's vectors of one shared-memory chunk.
 template <int VPL, typename T>
 __device__ __forceinline__ void stats_chunk(const unsigned char* buf, unsigned n, int lane, float& m, float& sm, T) {
-  const uint4* v = reinterpret_cast<const uint4*>(buf);
-  const int nv = int(n >> 4);
   uint4 q[VPL];
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int idx = lane + 32 * j;
-    q[j] = idx < nv ? v[idx] : neg_inf_vec(T());
-  }
+  load_slot<VPL>(buf, n, lane, q, neg_inf_vec(T()));
   stats_vecs<VPL>(q, m, sm, T());
 }
 
@@ -178,15 +194,8 @@ __device__ __forceinline__ void grad_chunk(unsigned char* buf, unsigned n, int l
 template <int VPL>
 __device__ __forceinline__ void stats_chunk_fused(const unsigned char* buf, unsigned n, int lane, float& m,
                                                   float& sm, __nv_bfloat16) {
-  const uint4* v = reinterpret_cast<const uint4*>(buf);
-  const int nv = int(n >> 4);
   uint4 q[VPL];
-  const uint4 neg = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);  // bf16 -inf x8
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int idx = lane + 32 * j;
-    q[j] = idx < nv ? v[idx] : neg;
-  }
+  load_slot<VPL>(buf, n, lane, q, neg_inf_vec(__nv_bfloat16()));
   __nv_bfloat162 mx = __halves2bfloat162(__ushort_as_bfloat16(0xff80), __ushort_as_bfloat16(0xff80));
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
@@ -247,21 +256,15 @@ __device__ __forceinline__ void grad_chunk_fused(unsigned char* buf, unsigned n,
     grad_chunk<__nv_bfloat16, VPL>(buf, n, lane, c, scale, cb);
     return;
   }
+  // the whole slot: the bytes past n are never stored to global memory
   uint4* v = reinterpret_cast<uint4*>(buf);
-  const int nv = int(n >> 4);
   uint4 q[VPL];
 #pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int idx = lane + 32 * j;
-    q[j] = idx < nv ? v[idx] : make_uint4(0u, 0u, 0u, 0u);
-  }
+  for (int j = 0; j < VPL; ++j) q[j] = v[lane + 32 * j];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) q[j] = grad_vec_fused(q[j], cb, __nv_bfloat16());
 #pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int idx = lane + 32 * j;
-    if (idx < nv) v[idx] = q[j];
-  }
+  for (int j = 0; j < VPL; ++j) v[lane + 32 * j] = q[j];
 }
 
 }  // namespace vpce
