@@ -229,10 +229,26 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, unsigned rank) {
   return a;
 }
 
-// arrive on the mbarrier at `bar` in CTA `rank`, releasing this thread's
-// earlier writes at cluster scope
-__device__ __forceinline__ void mbar_arrive_cluster(const uint64_t* bar, unsigned rank) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr(bar, rank))
+// arrive on the mbarrier at `bar` in CTA `rank` without a release: for an
+// arrival that only reports that this thread's earlier loads are done (their
+// values already used).  A release at cluster scope would make the thread
+// wait for a fence.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(const uint64_t* bar, unsigned rank) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr(bar, rank))
+               : "memory");
+}
+
+// Stores into another CTA's shared memory (dst, bar: shared::cluster
+// addresses) that count their bytes on that CTA's mbarrier: the barrier's
+// phase completes only once the data has landed, so the sender needs no
+// release fence.
+__device__ __forceinline__ void st_async_f2(uint32_t dst, float a, float b, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(dst), "f"(a),
+               "f"(b), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t dst, float a, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(dst), "f"(a), "r"(bar)
                : "memory");
 }
 

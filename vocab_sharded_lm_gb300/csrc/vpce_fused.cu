@@ -15,7 +15,8 @@
 //     the streaming pattern of the split forward;
 //   * per row they leave 8 partials (and the target logit) in a two-deep
 //     shared-memory mailbox -- the on-chip stand-in for the pages' max / sum /
-//     target all-reduces;
+//     target all-reduces (rows over 320 KB are shared by a cluster of two
+//     CTAs, which also send their partials to each other's mailboxes);
 //   * 8 "grad" warps follow about a row behind: they fold the partials in warp
 //     order into logsumexp, re-read the same bytes (L2 hits: the stats warps
 //     fetched them microseconds earlier), turn them into dlogits in shared
@@ -349,10 +350,11 @@ __device__ __forceinline__ void target_of(const Geo& g, int t, long long y, int&
 // NR > 1: a cluster of NR CTAs shares each row, CTA c taking the c-th part
 // of every warp role's column split (NR kSW stats warps per row).  Each CTA's
 // live L2 window then holds part rows, which keeps rows longer than the
-// live budget re-read from L2.  The stats warps of all NR CTAs post their
-// partials to every CTA's mailbox barrier (NR kSW arrivals), and every grad
-// warp folds the NR kSW partials (one per lane, then a fixed butterfly), so
-// all CTAs reach the same logsumexp.
+// live budget re-read from L2.  Each stats warp posts its partial to every
+// CTA's mailbox: to its own with a store and an arrival on the row barrier
+// (kSW arrivals), to the others with st.async, whose bytes the receiving
+// barrier counts.  Every grad warp folds the NR kSW partials (one per lane,
+// then a fixed butterfly), so all CTAs reach the same logsumexp.
 template <typename T, int NR>
 __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid_constant__ FusedParams p) {
   constexpr int EB = Elem<T>::kBytes;
@@ -376,8 +378,8 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     if (stats) sm.sdone[w] = 0u;
     else sm.gdone[w] = 0u;
     if (warp == 0) {
-      mbar_init(&sm.rowdone[0], NR * kSW);
-      mbar_init(&sm.rowdone[1], NR * kSW);
+      mbar_init(&sm.rowdone[0], kSW);
+      mbar_init(&sm.rowdone[1], kSW);
       mbar_init(&sm.rowfree[0], NR * kDW);
       mbar_init(&sm.rowfree[1], NR * kDW);
     }
@@ -396,20 +398,15 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
   const Geo& geo = sm.geo;
   const int nt = p.t;
   const RowPart rp = row_part<NR, EB>(geo, nt, crank, w);  // this warp's part of every row
+  // this CTA's bytes of a row (the union of its warps' ranges)
+  const unsigned cta_lo = PAIR ? row_part<NR, EB>(geo, nt, crank, 0).lo : 0u;
+  const unsigned cta_hi = PAIR ? row_part<NR, EB>(geo, nt, crank, kSW - 1).hi : 0u;
 
   const long long r_step = gridDim.x / NR;
   const long long r0 = blockIdx.x / NR;
   bool alive = true;
   auto wait_row_bar = [&](uint64_t* bar, uint32_t parity) {
     return PAIR ? mbar_wait_warp_cluster(bar, parity) : mbar_wait_warp(bar, parity);
-  };
-  auto arrive_row_bar = [&](uint64_t* bar) {  // one lane only
-    if (PAIR) {
-#pragma unroll
-      for (int c = 0; c < NR; ++c) mbar_arrive_cluster(bar, unsigned(c));
-    } else {
-      mbar_arrive_local(bar);
-    }
   };
 
   if (stats) {
@@ -488,30 +485,37 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
         alive = false;
         break;
       }
-      // lane 1 posts the row: lane 0 issues this warp's bulk copies, and a
-      // release at cluster scope from that thread measured 1.8 us per row
-      // against 0.7 us from another lane (s = 32768, CTA pairs)
+      // lane 1 posts the row (lane 0 issues this warp's bulk copies).  The
+      // other CTAs' copies go by st.async, counted in bytes on their row
+      // barriers, so no release at cluster scope (a fence) is on this path:
+      // with stores and a release arrival per CTA the pair took 5.59 ms at
+      // s = 32768 against 5.16 ms (measured on GB300); s = 16384 (fp32) is
+      // unchanged.
       if (lane == 1) {
         // the partial goes to every CTA's mailbox: the grad warps then read
         // all of a row's partials from their own shared memory
         sm.part[buf][crank * kSW + w] = make_float2(m, se);
-#pragma unroll
-        for (int c = 0; c < NR; ++c)
-          if (unsigned(c) != crank)
-            asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(
-                             cluster_addr(&sm.part[buf][crank * kSW + w], unsigned(c))),
-                         "f"(m), "f"(se)
-                         : "memory");
-        if (has_t) {
-          sm.tz[buf] = zt;
-          // the other CTAs' grad warps read the target logit from their own mailbox
+        if (has_t) sm.tz[buf] = zt;
+        if (PAIR) {
 #pragma unroll
           for (int c = 0; c < NR; ++c)
-            if (unsigned(c) != crank)
-              asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr(&sm.tz[buf], unsigned(c))), "f"(zt)
-                           : "memory");
+            if (unsigned(c) != crank) {
+              const uint32_t rb = cluster_addr(&sm.rowdone[buf], unsigned(c));
+              st_async_f2(cluster_addr(&sm.part[buf][crank * kSW + w], unsigned(c)), m, se, rb);
+              if (has_t) st_async_f32(cluster_addr(&sm.tz[buf], unsigned(c)), zt, rb);
+            }
+          if (w == 0) {
+            // this CTA's barrier also waits for the other CTAs' partials, and
+            // for the target logit when another CTA holds it
+            const bool t_other = ty >= 0 && !(unsigned(geo.start[ty]) * EB + toff >= cta_lo &&
+                                                unsigned(geo.start[ty]) * EB + toff < cta_hi);
+            mbar_arrive_expect_tx(&sm.rowdone[buf], unsigned((NR - 1) * kSW * 8 + (t_other ? 4 : 0)));
+          } else {
+            mbar_arrive_local(&sm.rowdone[buf]);
+          }
+        } else {
+          mbar_arrive_local(&sm.rowdone[buf]);
         }
-        arrive_row_bar(&sm.rowdone[buf]);
       }
       ++n;
     }
@@ -602,7 +606,20 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
         zt = sm.tz[buf];
       }
       __syncwarp();
-      if (lane == 1) arrive_row_bar(&sm.rowfree[buf]);  // lane 0 issues the bulk copies (see the stats side)
+      // The slot is free once every lane has read it.  Those reads returned
+      // their values before this point (the fold above used them and the warp
+      // has converged), so the arrival carries no release: at cluster scope a
+      // release made lane 1 wait about 1000 cycles per row for a fence
+      // (measured on GB300, s = 32768: 5.73 -> 5.59 ms; s = 16384 fp32:
+      // 3.139 -> 3.126 ms).  Lane 0 issues the bulk copies (see the stats side).
+      if (lane == 1) {
+        if (PAIR) {
+#pragma unroll
+          for (int c = 0; c < NR; ++c) mbar_arrive_cluster_relaxed(&sm.rowfree[buf], unsigned(c));
+        } else {
+          mbar_arrive_local(&sm.rowfree[buf]);
+        }
+      }
       ++n;
       const float lse = in_range ? M + logf(S) : __int_as_float(0x7fc00000);
       if (w == 0 && lane == 0 && crank == 0) {
