@@ -258,9 +258,9 @@ vpce_status vpce_forward_backward_rows(void* const* shards, vpce_dtype dtype, in
  * device (no launch): *kernel = 0 two-call path (a shard's width in bytes is
  * not a multiple of 16; misaligned pointers or strides also take it),
  * 1 fused streaming kernel on a persistent grid of *grid CTAs, one per SM.
- * *cluster is 1, or 2 when rows are longer than 320 KB: a pair of CTAs then
+ * *cluster is 1, or 2 when rows are longer than 224 KB: a pair of CTAs then
  * shares each row, so that the rows kept live between the two passes still
- * fit in L2.
+ * fit in L2 with room for the statistics pass to run ahead.
  */
 vpce_status vpce_fused_plan(vpce_dtype dtype, int t, const int64_t* vocab_start, int64_t s,
                             int* kernel, int* cluster, int* grid);

@@ -111,9 +111,9 @@ def test_fused_plan(name):
     vs = synth.even_vocab_start(w.V, w.t)
     plan = vpce.vpce_fused_plan(vpce.VPCE_BF16 if w.dtype == "bf16" else vpce.VPCE_FP32, vs, w.s)
     assert plan["kernel"] == "stream" and 0 < plan["grid"] <= w.s
-    # rows over 320 KB are shared by a pair of CTAs (a cluster of 2)
+    # rows over 224 KB are shared by a pair of CTAs (a cluster of 2)
     row_bytes = w.V * (2 if w.dtype == "bf16" else 4)
-    assert plan["cluster"] == (2 if row_bytes > 320 * 1024 else 1)
+    assert plan["cluster"] == (2 if row_bytes > 224 * 1024 else 1)
     assert plan["grid"] % plan["cluster"] == 0
     odd = [0, 3, 10]  # a 3-column bf16 shard is not a 16-byte multiple
     assert vpce.vpce_fused_plan(vpce.VPCE_BF16, odd, 4)["kernel"] == "split"

@@ -15,7 +15,7 @@
 //     the streaming pattern of the split forward;
 //   * per row they leave 8 partials (and the target logit) in a two-deep
 //     shared-memory mailbox -- the on-chip stand-in for the pages' max / sum /
-//     target all-reduces (rows over 320 KB are shared by a cluster of two
+//     target all-reduces (rows over 224 KB are shared by a cluster of two
 //     CTAs, which also send their partials to each other's mailboxes);
 //   * 8 "grad" warps follow about a row behind: they fold the partials in warp
 //     order into logsumexp, re-read the same bytes (L2 hits: the stats warps
@@ -62,8 +62,11 @@ constexpr int kDSlots = 4;
 // (s = 4096) run the same with 288, 320 or 352 KB.
 constexpr unsigned kLiveBytesPerCta = 288u * 1024u;
 // Rows longer than this are shared by a pair of CTAs; shorter ones run on
-// one CTA, with whatever slack the window above leaves.
-constexpr long long kPairRowBytes = 320ll * 1024ll;
+// one CTA, with whatever slack the window above leaves.  Measured on GB300:
+// s = 8192, V = 128256 (250 KB rows) 0.660 ms on one CTA per row against
+// 0.654 ms on pairs (125 KB half rows, five chunks of slack); s = 4096,
+// V = 50304 (98 KB rows) 0.167 ms against 0.206 ms.
+constexpr long long kPairRowBytes = 224ll * 1024ll;
 // The same budget for CTAs that share rows (a cluster per row): their row
 // statistics also cross SMs.  Measured (s = 32768 bf16, half rows of 250 KB):
 // 5.80 ms with one chunk of slack per stats warp, 6.20 ms with two, 6.03 ms
