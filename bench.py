@@ -18,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -144,10 +145,15 @@ _KERNEL_FILES = {"stream_fused_kernel": ("vpce_fused.cu",), "backward_kernel": (
 
 
 def _kernel_source_hash(kernel: str) -> str:
+    """Hash of the code (comments removed, whitespace runs collapsed) of a
+    kernel's source file and the headers it includes: an edit of comments or
+    layout keeps its stored counters."""
     h = hashlib.sha256()
     for f in ("vpce_device.cuh", "vpce_kernels.cuh", "vpce_chunk.cuh", *_KERNEL_FILES[kernel]):
-        with open(os.path.join(ROOT, "vocab_sharded_lm_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "vocab_sharded_lm_gb300", "csrc", f), encoding="utf-8") as fh:
+            code = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        code = re.sub(r"\s+", " ", re.sub(r"//[^\n]*", "", code))
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 

@@ -55,11 +55,11 @@ constexpr int kDSlots = 4;
 // L2 bytes per CTA the two passes may keep live between them: one row is
 // the least (a row's statistics precede its gradient); rows shorter than
 // this let the stats warps run further ahead.  Measured on GB300 with each
-// warp taking one contiguous range of the row: 288 KB per SM (44 MB over 152
-// SMs; one 4 KB chunk of slack per stats warp for 250 KB rows) gives
-// 0.664 ms at s = 8192, V = 128256, against 0.685 ms with 320 KB (two
-// chunks), 0.753 ms with 352 KB and 0.715 ms with no slack; 100 KB rows
-// (s = 4096) run the same with 288, 320 or 352 KB.
+// warp taking one contiguous range of the row and one CTA per row: 288 KB
+// per SM (44 MB over 152 SMs; one 4 KB chunk of slack per stats warp for
+// 250 KB rows) gave 0.664 ms at s = 8192, V = 128256, against 0.685 ms with
+// 320 KB (two chunks), 0.753 ms with 352 KB and 0.715 ms with no slack;
+// 100 KB rows (s = 4096) run the same with 288, 320 or 352 KB.
 constexpr unsigned kLiveBytesPerCta = 288u * 1024u;
 // Rows longer than this are shared by a pair of CTAs; shorter ones run on
 // one CTA, with whatever slack the window above leaves.  Measured on GB300:
@@ -68,10 +68,12 @@ constexpr unsigned kLiveBytesPerCta = 288u * 1024u;
 // V = 50304 (98 KB rows) 0.167 ms against 0.206 ms.
 constexpr long long kPairRowBytes = 224ll * 1024ll;
 // The same budget for CTAs that share rows (a cluster per row): their row
-// statistics also cross SMs.  Measured (s = 32768 bf16, half rows of 250 KB):
-// 5.80 ms with one chunk of slack per stats warp, 6.20 ms with two, 6.03 ms
-// with none; s = 16384 fp32 (304 KB half rows, no slack) runs the same with
-// 256, 288 or 320 KB, and 4% slower with one chunk of slack forced.
+// statistics also cross SMs.  Measured on GB300: s = 32768 bf16 (half rows
+// of 250 KB) 5.16 ms with 288 KB (one chunk of slack per stats warp),
+// 5.34 ms with 320 KB, 5.69 ms with 256 or 352 KB; s = 8192 (125 KB half
+// rows) 0.654 ms, within 0.3% of 224 and 256 KB, 0.672 ms with 320 KB;
+// s = 16384 fp32 (304 KB half rows, no slack) the same with 256, 288 or
+// 320 KB.
 constexpr unsigned kLiveBytesPerCtaShared = 288u * 1024u;
 // stats warp w and grad warp w walk the same chunks: the credit between them
 // counts those chunks
