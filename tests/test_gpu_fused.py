@@ -160,3 +160,31 @@ def test_fused_several_rows_per_cta(name, t):
     s = 3 * units + 7
     assert vpce.vpce_fused_plan(dt, vs, s)["grid"] == plan["grid"]
     check_full(run_full(w, t=t, s=s, path="fused"))
+
+
+@pytest.mark.parametrize("name,t", [("s8192_v128256", 8), ("s8192_v128256", 1), ("s16384_v152064", 8),
+                                    ("s32768_v256000", 16)])
+def test_fused_pair_targets_at_part_edges(name, t):
+    # CTA pairs: the target logit crosses to the other CTA of the pair only
+    # when that CTA's half of the row holds it, and the receiving row barrier
+    # then waits for 4 more bytes.  Targets on both sides of the split, at
+    # shard edges, at the row ends, bad and ignored, in changing order over
+    # three or four rows per pair (so every mailbox slot is reused)
+    w = W[name]
+    vs = synth.even_vocab_start(w.V, t)
+    dt = vpce.VPCE_BF16 if w.dtype == "bf16" else vpce.VPCE_FP32
+    eb = 2 if w.dtype == "bf16" else 4
+    plan = vpce.vpce_fused_plan(dt, vs, w.s)
+    assert plan["cluster"] == 2
+    if t >= 2:  # the shard boundary nearest half the row
+        mid = vs[min(range(1, t), key=lambda i: abs(2 * vs[i] - vs[t]))]
+    else:  # half the row's bytes, rounded down to 16 bytes
+        mid = ((w.V * eb // 2) & ~15) // eb
+    edges = sorted({0, 1, mid - 1, mid, mid + 1, w.V - 2, w.V - 1, vs[1] - 1, min(vs[1], w.V - 1)})
+    pattern = edges + [w.V, w.ignore_index] + edges[::-1] + [-5]
+    units = plan["grid"] // plan["cluster"]
+    s = 3 * units + 11
+    y = np.random.default_rng(5).permutation(np.resize(np.array(pattern, dtype=np.int64), s))
+    res = run_full(w, t=t, s=s, targets=y, path="fused")
+    assert res["flag"] & vpce.VPCE_FLAG_BAD_TARGET and not res["flag"] & vpce.VPCE_FLAG_WAIT_TIMEOUT
+    check_full(res)
