@@ -677,7 +677,15 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
     if (lane == 0) bulk_wait_all<0>();  // every dlogits store has landed
   }
   // no CTA leaves while its peer may still reach its mailbox or barriers
-  if (PAIR) cluster_sync_all();
+  if (PAIR) {
+    cluster_sync_all();
+    // After a wait that gave up, a partial the other CTA sent (st.async: an
+    // asynchronous write, which the barrier above does not order) may still
+    // be on its way to this CTA's mailbox, so the CTA stays resident about
+    // 100 us longer.  Without an error every byte sent was awaited.
+    if (threadIdx.x == 0 && (__ldcg(&p.hdr->error_flag) & VPCE_FLAG_WAIT_TIMEOUT))
+      for (int i = 0; i < 100; ++i) __nanosleep(1000);
+  }
 
   // ---- batch loss: the last block sums the per-row losses in a fixed order
   grid_dependency_wait();  // every thread: the header (ticket) is the prologue's
