@@ -611,11 +611,15 @@ __global__ void __launch_bounds__(kFThreads, 1) stream_fused_kernel(const __grid
         zt = sm.tz[buf];
       }
       __syncwarp();
-      // The slot is free once every lane has read it.  Those reads returned
-      // their values before this point (the fold above used them and the warp
-      // has converged), so the arrival carries no release: at cluster scope a
-      // release made lane 1 wait about 1000 cycles per row for a fence
-      // (measured on GB300, s = 32768: 5.73 -> 5.59 ms; s = 16384 fp32:
+      // The slot is free once every lane has read it.  The partials' reads
+      // returned their values before this point (the fold above used them and
+      // the warp has converged), and the target logit's read was issued
+      // before it; the slot is written again only after every grad warp of
+      // the row's CTAs has arrived and a stats warp has then streamed its part
+      // of a whole further row (microseconds, against tens of nanoseconds for
+      // a shared-memory load).  So the arrival carries no release: at cluster
+      // scope a release made lane 1 wait about 1000 cycles per row for a
+      // fence (measured on GB300, s = 32768: 5.73 -> 5.59 ms; s = 16384 fp32:
       // 3.139 -> 3.126 ms).  Lane 0 issues the bulk copies (see the stats side).
       if (lane == 1) {
         if (PAIR) {
